@@ -1,0 +1,278 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for masked scaled-dot-product attention
+ * under structured sparse masks.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this
+ * file: only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It
+ * shares no code, header or table with the CUDA library.
+ *
+ * What it computes (all indices 0-based):
+ *
+ *   Allowed sets.  A mask is a union of simple rules ("Attention variants",
+ *   sreshtalluri.github.io, §4 Implementation: "Sparse patterns are unions of simple
+ *   rules"), intersected with causality when the mask is causal:
+ *     - causal local window of width w, counting the query itself: 0 <= i-j < w
+ *       ("Sparse attention" glossary, selfmadequant, §Choose the available reads,
+ *       the set S_i = {max(1,i-w+1),...,i} in 1-based form; "Attention variants"
+ *       §4 sliding_window).  w = 0 means no window: the full causal triangle
+ *       (octlm "Sparse attention", §One mask function for every pattern).
+ *     - bidirectional local radius r: |i-j| <= r ("Attention variants" §3 worked
+ *       example, "local radius 2": query 12 reads 10..14).  r = -1: no limit.
+ *     - strided columns: key j with j % s == o is readable by every query (causal:
+ *       every later query).  o = 0 is the octlm convention (columns % stride == 0),
+ *       o = s-1 the "Attention variants" local_strided convention.
+ *     - global tokens G: rows in G read every key, columns in G are read by every
+ *       query ("Attention variants" §4 with_global; ai360xpert "Sparse Attention",
+ *       §Global tokens).  In a causal mask both stay causal ("Attention variants",
+ *       the look-ahead warning after with_global).
+ *
+ *   Attention.  For each query i with allowed set S_i (never empty: j = i is always
+ *   allowed),
+ *       s_ij = scale * q_i . k_j               (j in S_i)
+ *       y_i  = sum_{j in S_i} softmax_j(s_ij) v_j,  softmax over S_i only
+ *       LSE_i = ln sum_{j in S_i} exp(s_ij)
+ *   ("Sparse attention" glossary, §Choose the available reads, the displayed
+ *   equation for y_i and alpha_ij; softmax normalises over allowed keys only.)
+ *   Evaluated in fp64 with the usual max subtraction, which leaves the value
+ *   unchanged.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+  int causal;      /* 1: j <= i only */
+  int64_t window;  /* causal local width, 0 = unbounded */
+  int64_t radius;  /* bidirectional radius, -1 = unbounded */
+  int64_t stride;  /* 0 = none */
+  int64_t offset;  /* strided columns: j % stride == offset */
+  int64_t n_global;
+  const int32_t* global_pos; /* sorted ascending, distinct */
+  int64_t T;
+} omask;
+
+/* ---- spec checks: the readings every valid mask obeys ------------------------- */
+
+/* Returns 0 for a valid mask, a negative code naming the first violated rule. */
+int oracle_validate(int causal, int64_t window, int64_t radius, int64_t stride,
+                    int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T) {
+  if (T <= 0) return -1;
+  if (causal != 0 && causal != 1) return -2;
+  if (causal == 1 && (window < 0 || radius != -1)) return -3;
+  if (causal == 0 && (radius < -1 || window != 0)) return -4;
+  if (stride < 0) return -5;
+  if (stride == 0 && offset != 0) return -6;
+  if (stride > 0 && (offset < 0 || offset >= stride)) return -6;
+  if (n_global < 0 || n_global > T) return -7;
+  for (int64_t a = 0; a < n_global; a++) {
+    if (gpos[a] < 0 || gpos[a] >= T) return -8;
+    if (a > 0 && gpos[a] <= gpos[a - 1]) return -9; /* sorted, distinct */
+  }
+  return 0;
+}
+
+static int in_global(const omask* m, int64_t x) {
+  for (int64_t a = 0; a < m->n_global; a++)
+    if (m->global_pos[a] == x) return 1;
+  return 0;
+}
+
+/* ---- the rule itself, one (i, j) pair at a time --------------------------------- */
+
+static int allowed(const omask* m, int64_t i, int64_t j) {
+  if (m->causal && j > i) return 0;             /* causality prohibits future reads */
+  if (in_global(m, i)) return 1;                /* a global row reads every key */
+  if (in_global(m, j)) return 1;                /* every query reads a global column */
+  if (m->stride > 0 && j % m->stride == m->offset) return 1; /* strided column */
+  if (m->causal) return m->window == 0 || (i - j) < m->window; /* 0 <= i-j < w */
+  return m->radius < 0 || llabs(i - j) <= m->radius;            /* |i-j| <= r */
+}
+
+int oracle_allowed(int causal, int64_t window, int64_t radius, int64_t stride,
+                   int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
+                   int64_t i, int64_t j) {
+  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  return allowed(&m, i, j);
+}
+
+/* S_i by scanning every key and asking the rule: the plainest form. */
+static int64_t row_set_scan(const omask* m, int64_t i, int32_t* out) {
+  int64_t n = 0;
+  for (int64_t j = 0; j < m->T; j++)
+    if (allowed(m, i, j)) {
+      if (out) out[n] = (int32_t)j;
+      n++;
+    }
+  return n;
+}
+
+/* S_i as the literal union of the rule sets (window interval, strided progression,
+ * global columns, or everything for a global row), each enumerated directly, then
+ * merged in ascending order without repeats.  Same set as row_set_scan (a test
+ * checks this); it exists because it costs O(|S_i| + |G|) instead of O(T). */
+static int64_t row_set_union(const omask* m, int64_t i, int32_t* out) {
+  const int64_t T = m->T;
+  const int64_t jmax = m->causal ? i : T - 1; /* causal cut */
+  int64_t n = 0;
+  if (in_global(m, i)) { /* global row: every key causality permits */
+    for (int64_t j = 0; j <= jmax; j++) out[n++] = (int32_t)j;
+    return n;
+  }
+  int64_t lo, hi; /* local interval */
+  if (m->causal) {
+    lo = (m->window == 0) ? 0 : i - m->window + 1;
+    hi = i;
+  } else {
+    lo = (m->radius < 0) ? 0 : i - m->radius;
+    hi = (m->radius < 0) ? T - 1 : i + m->radius;
+  }
+  if (lo < 0) lo = 0;
+  if (hi > jmax) hi = jmax;
+  /* three ascending streams: strided progression, global columns, local interval */
+  int64_t js = (m->stride > 0) ? m->offset : T; /* next strided column */
+  int64_t ag = 0;                                /* next global index */
+  int64_t jl = lo;                               /* next local column */
+  int64_t last = -1;
+  for (;;) {
+    int64_t cs = (js <= jmax) ? js : INT64_MAX;
+    int64_t cg = (ag < m->n_global && m->global_pos[ag] <= jmax) ? m->global_pos[ag]
+                                                                  : INT64_MAX;
+    int64_t cl = (jl <= hi) ? jl : INT64_MAX;
+    int64_t c = cs < cg ? cs : cg;
+    if (cl < c) c = cl;
+    if (c == INT64_MAX) break;
+    if (c != last) out[n++] = (int32_t)c;
+    last = c;
+    if (c == cs) js += m->stride;
+    if (c == cg) ag++;
+    if (c == cl) jl++;
+  }
+  return n;
+}
+
+/* Allowed set of one query, ascending.  method 0: union of rule sets, 1: full scan.
+ * `out` must hold T entries.  Returns |S_i|. */
+int64_t oracle_row_set(int causal, int64_t window, int64_t radius, int64_t stride,
+                       int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
+                       int64_t i, int method, int32_t* out) {
+  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  return method ? row_set_scan(&m, i, out) : row_set_union(&m, i, out);
+}
+
+/* Number of allowed (i, j) pairs: the sum of |S_i| (the glossary's edge count E). */
+int64_t oracle_count_pairs(int causal, int64_t window, int64_t radius, int64_t stride,
+                           int64_t offset, int64_t n_global, const int32_t* gpos,
+                           int64_t T) {
+  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  int64_t total = 0;
+#pragma omp parallel
+  {
+    int32_t* buf = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+#pragma omp for schedule(dynamic, 64) reduction(+ : total)
+    for (int64_t i = 0; i < T; i++) total += row_set_union(&m, i, buf);
+    free(buf);
+  }
+  return total;
+}
+
+/* Histogram of allowed pairs into BM x BN tiles: cnt[(i/BM) * nkb + (j/BN)].
+ * `cnt` has ceil(T/BM) * ceil(T/BN) int32 entries and is overwritten. */
+void oracle_tile_counts(int causal, int64_t window, int64_t radius, int64_t stride,
+                        int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
+                        int64_t BM, int64_t BN, int32_t* cnt) {
+  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  const int64_t nqb = (T + BM - 1) / BM, nkb = (T + BN - 1) / BN;
+  memset(cnt, 0, sizeof(int32_t) * (size_t)(nqb * nkb));
+#pragma omp parallel
+  {
+    int32_t* buf = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+    /* one query block per iteration: its rows only touch its own row of tiles */
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t qb = 0; qb < nqb; qb++) {
+      for (int64_t i = qb * BM; i < (qb + 1) * BM && i < T; i++) {
+        int64_t n = row_set_union(&m, i, buf);
+        for (int64_t a = 0; a < n; a++) cnt[qb * nkb + buf[a] / BN] += 1;
+      }
+    }
+    free(buf);
+  }
+}
+
+/* ---- attention over the allowed sets ------------------------------------------- */
+
+static double load_elem(const void* p, int dtype, int64_t idx) {
+  if (dtype == 0) return (double)((const float*)p)[idx];
+  /* dtype 1: bf16 bit patterns; a bf16 value is the top half of an fp32 */
+  uint32_t bits = (uint32_t)((const uint16_t*)p)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* One head.  Q, K, V: [T][d] row-major, dtype 0 = fp32, 1 = bf16 bits.
+ * rows: the query indices to evaluate (n_rows of them).
+ * O: [n_rows][d] fp64, LSE: [n_rows] fp64 (natural log).  Returns total |S_i|. */
+int64_t oracle_attention_head(int causal, int64_t window, int64_t radius, int64_t stride,
+                              int64_t offset, int64_t n_global, const int32_t* gpos,
+                              int64_t T, int64_t d, int dtype, const void* Q,
+                              const void* K, const void* V, double scale,
+                              const int64_t* rows, int64_t n_rows, double* O,
+                              double* LSE) {
+  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  int64_t total = 0;
+#pragma omp parallel
+  {
+    int32_t* set = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+    double* s = (double*)malloc(sizeof(double) * (size_t)T);
+    double* q = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4) reduction(+ : total)
+    for (int64_t r = 0; r < n_rows; r++) {
+      const int64_t i = rows[r];
+      const int64_t n = row_set_union(&m, i, set);
+      total += n;
+      for (int64_t k = 0; k < d; k++) q[k] = load_elem(Q, dtype, i * d + k);
+      /* logits over the allowed keys only */
+      double mx = -INFINITY;
+      for (int64_t a = 0; a < n; a++) {
+        const int64_t j = set[a];
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; k++) acc += q[k] * load_elem(K, dtype, j * d + k);
+        s[a] = scale * acc;
+        if (s[a] > mx) mx = s[a];
+      }
+      /* normaliser over S_i */
+      double l = 0.0;
+      for (int64_t a = 0; a < n; a++) l += exp(s[a] - mx);
+      /* weighted values */
+      double* y = O + r * d;
+      for (int64_t k = 0; k < d; k++) y[k] = 0.0;
+      for (int64_t a = 0; a < n; a++) {
+        const double alpha = exp(s[a] - mx) / l;
+        const int64_t j = set[a];
+        for (int64_t k = 0; k < d; k++) y[k] += alpha * load_elem(V, dtype, j * d + k);
+      }
+      LSE[r] = mx + log(l);
+    }
+    free(set);
+    free(s);
+    free(q);
+  }
+  return total;
+}
+
+/* Number of OpenMP threads the oracle uses (1 when built without OpenMP). */
+int oracle_num_threads(void) {
+  int n = 1;
+#ifdef _OPENMP
+#pragma omp parallel
+  {
+#pragma omp single
+    n = omp_get_num_threads();
+  }
+#endif
+  return n;
+}

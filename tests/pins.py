@@ -1,0 +1,385 @@
+"""Checks that pin the CPU oracle to something other than itself.
+
+Each ``check_*`` function returns a list of failure strings (empty = pass), so the
+same checks serve the oracle tests and the mutation tests (which must see at least
+one failure for every planted mistake).  What each check leans on:
+
+  * numbers printed on the pages (tests/golden/page_counts.json, each with its source);
+  * closed forms: the glossary's edge count E = n w - w(w-1)/2, n(n+1)/2 for the
+    causal triangle, the L-layer reach L(w-1)+1, window = 0 / window >= n equal causal;
+  * an independent dense-boolean restatement of the mask rules written here in numpy
+    (np.indices grids, the style the pages use) and an independent inclusion-exclusion
+    pair counter;
+  * library routines: torch's scaled_dot_product_attention and logsumexp in fp64;
+  * exact special cases: w = 1 gives y_i = v_i, Q = 0 gives the mean of the allowed
+    values, and a constant shift of every key leaves y unchanged.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                     "page_counts.json")))
+
+
+def mask_of(e) -> oracle.Mask:
+    return oracle.Mask(e["T"], e.get("causal", 1), e.get("window", 0),
+                       e.get("radius", -1), e.get("stride", 0), e.get("offset", 0),
+                       e.get("global_pos", []))
+
+
+# ---------------------------------------------------------------- independent rules
+
+def np_dense_mask(T, causal, window, radius, stride, offset, gpos) -> np.ndarray:
+    """Dense boolean mask, True = may attend, from index grids (independent of oracle.c)."""
+    i, j = np.indices((T, T))
+    past = j <= i
+    if causal:
+        local = past & ((i - j < window) if window > 0 else np.ones_like(past))
+    else:
+        local = (np.abs(i - j) <= radius) if radius >= 0 else np.ones_like(past)
+    m = local.copy()
+    if stride > 0:
+        col = (j % stride == offset)
+        m |= (col & past) if causal else col
+    g = np.zeros(T, dtype=bool)
+    g[np.asarray(gpos, dtype=np.int64)] = True
+    gcol = np.broadcast_to(g[None, :], (T, T))
+    grow = np.broadcast_to(g[:, None], (T, T))
+    m |= (gcol & past) if causal else gcol
+    m |= (grow & past) if causal else grow
+    return m
+
+
+def closed_form_pairs(T, causal, window, radius, stride, offset, gpos) -> int:
+    """Pair count by inclusion-exclusion per row: |L| + |S minus L| + |G minus (L u S)|."""
+    i = np.arange(T, dtype=np.int64)
+    jmax = i if causal else np.full(T, T - 1, dtype=np.int64)
+    if causal:
+        lo = np.zeros(T, np.int64) if window == 0 else np.maximum(0, i - window + 1)
+        hi = i.copy()
+    else:
+        lo = np.zeros(T, np.int64) if radius < 0 else np.maximum(0, i - radius)
+        hi = np.full(T, T - 1, np.int64) if radius < 0 else np.minimum(T - 1, i + radius)
+    n_local = hi - lo + 1
+
+    def ap_upto(x):  # #{0 <= j <= x : j % stride == offset}
+        if stride == 0:
+            return np.zeros_like(x)
+        return np.where(x >= offset, (x - offset) // stride + 1, 0)
+
+    n_strided_out = ap_upto(jmax) - (ap_upto(hi) - ap_upto(lo - 1))
+    G = np.asarray(gpos, dtype=np.int64)
+    if len(G):
+        gg = G[None, :]
+        inrange = gg <= jmax[:, None]
+        inlocal = (gg >= lo[:, None]) & (gg <= hi[:, None])
+        strided = (gg % stride == offset) if stride > 0 else np.zeros_like(gg, bool)
+        n_g = (inrange & ~inlocal & ~strided).sum(axis=1)
+    else:
+        n_g = 0
+    per_row = n_local + n_strided_out + n_g
+    isg = np.zeros(T, bool)
+    isg[G] = True
+    per_row = np.where(isg, jmax + 1, per_row)
+    return int(per_row.sum())
+
+
+def reach_after(M: np.ndarray, layers: int) -> np.ndarray:
+    """Boolean matrix power: which originals can influence each position."""
+    R = np.eye(len(M), dtype=bool)
+    Mi = M.astype(np.int64)
+    for _ in range(layers):
+        R = (Mi @ R.astype(np.int64)) > 0
+    return R
+
+
+def oracle_dense(m: oracle.Mask) -> np.ndarray:
+    D = np.zeros((m.T, m.T), dtype=bool)
+    for i in range(m.T):
+        D[i, m.row_set(i)] = True
+    return D
+
+
+def small_specs(seed=0, n=60):
+    """Seeded sweep of small masks covering every rule and edge (ragged T, w=1,
+    w >= T, r = 0, stride 1..17, offsets, globals overlapping the window/stride)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        T = int(rng.integers(1, 90))
+        causal = int(rng.integers(0, 2))
+        window = int(rng.choice([0, 1, 2, 3, 5, 8, T, T + 3])) if causal else 0
+        radius = -1 if causal else int(rng.choice([-1, 0, 1, 2, 7, T]))
+        stride = int(rng.choice([0, 0, 1, 2, 3, 4, 17]))
+        offset = int(rng.integers(0, stride)) if stride else 0
+        g = int(rng.choice([0, 0, 1, 3, 5]))
+        gpos = np.sort(rng.choice(T, size=min(g, T), replace=False)).tolist()
+        out.append(dict(T=T, causal=causal, window=window, radius=radius, stride=stride,
+                        offset=offset, global_pos=gpos))
+    return out
+
+
+# ---------------------------------------------------------------- count / set pins
+
+def check_page_counts():
+    bad = []
+    for e in GOLDEN["pair_counts"]:
+        got = mask_of(e).count_pairs()
+        if got != e["pairs"]:
+            bad.append(f"pairs {e['source']}: got {got}, page says {e['pairs']}")
+    return bad
+
+
+def check_row_sets():
+    bad = []
+    for e in GOLDEN["row_sets"]:
+        got = mask_of(e).row_set(e["row"]).tolist()
+        want = e["set"] if "set" in e else list(range(e["range"][0], e["range"][1] + 1))
+        if got != want:
+            bad.append(f"row set {e['source']}: got {got[:8]}..({len(got)}), want "
+                       f"{want[:8]}..({len(want)})")
+    return bad
+
+
+def check_reach():
+    bad = []
+    for e in GOLDEN["reach"]:
+        m = oracle.Mask(e["T"], 1, e["window"])
+        R = reach_after(oracle_dense(m), e["layers"])
+        got = np.nonzero(R[e["row"]])[0].tolist()
+        if "set" in e and got != e["set"]:
+            bad.append(f"reach {e['source']}: got {got}")
+        if "width" in e and len(got) != e["width"]:
+            bad.append(f"reach width {e['source']}: got {len(got)}")
+    # the closed form at every depth and every row (glossary reach formula)
+    for T, w in [(16, 4), (6, 2), (32, 8), (20, 1)]:
+        M = oracle_dense(oracle.Mask(T, 1, w))
+        for L in range(0, 7):
+            R = reach_after(M, L)
+            for i in range(T):
+                want = list(range(max(0, i - L * (w - 1)), i + 1))
+                got = np.nonzero(R[i])[0].tolist()
+                if got != want:
+                    bad.append(f"reach T={T} w={w} L={L} i={i}: {got} != {want}")
+                    break
+    # exercise: n = 32, w = 8: last token reaches the first after ceil(31/7) = 5 layers
+    M = oracle_dense(oracle.Mask(32, 1, 8))
+    first = next(L for L in range(1, 40) if reach_after(M, L)[31, 0])
+    if first != 5:
+        bad.append(f"n=32 w=8 layers to reach first token: {first} != 5")
+    return bad
+
+
+def check_edge_formula():
+    bad = []
+    for n in range(1, 41):
+        for w in range(1, n + 1):
+            got = oracle.Mask(n, 1, w).count_pairs()
+            want = n * w - w * (w - 1) // 2
+            if got != want:
+                bad.append(f"E(n={n}, w={w}) = {got} != {want}")
+    # the exercise's n = 32, w = 8 (answer not printed; formula gives 228)
+    if oracle.Mask(32, 1, 8).count_pairs() != 228:
+        bad.append("n=32 w=8 != 228")
+    # the 32K / W=4096 workload: exact E, the page's 134M is N*W
+    if oracle.Mask(32768, 1, 4096).count_pairs() != 32768 * 4096 - 4096 * 4095 // 2:
+        bad.append("E(32768, 4096)")
+    return bad
+
+
+def check_causal_equivalences():
+    bad = []
+    for T in [1, 2, 5, 16, 33]:
+        tri = T * (T + 1) // 2
+        for s in [0, 3]:
+            if oracle.Mask(T, 1, 0, -1, s, 0).count_pairs() != tri:
+                bad.append(f"window=0 stride={s} T={T} is not the triangle")
+        for w in [T, T + 1, 5 * T]:
+            for i in range(T):
+                if oracle.Mask(T, 1, w).row_set(i).tolist() != list(range(i + 1)):
+                    bad.append(f"window={w} >= T={T} row {i} is not causal")
+                    break
+        if oracle.Mask(T, 0, 0, -1).count_pairs() != T * T:
+            bad.append(f"unbounded bidirectional T={T} is not full")
+    return bad
+
+
+def check_against_numpy_rules(seed=0):
+    bad = []
+    for e in small_specs(seed):
+        m = mask_of(e)
+        if m.validate() != 0:
+            bad.append(f"valid spec rejected: {e}")
+            continue
+        D = np_dense_mask(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
+                          e["offset"], e["global_pos"])
+        for i in range(e["T"]):
+            u = m.row_set(i, "union").tolist()
+            s = m.row_set(i, "scan").tolist()
+            ref = np.nonzero(D[i])[0].tolist()
+            if u != ref or s != ref:
+                bad.append(f"row {i} of {e}: union {u[:6]} scan {s[:6]} numpy {ref[:6]}")
+                break
+        if m.count_pairs() != int(D.sum()):
+            bad.append(f"count of {e}")
+        if closed_form_pairs(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
+                             e["offset"], e["global_pos"]) != int(D.sum()):
+            bad.append(f"closed form of {e}")
+        for BM, BN in [(4, 4), (8, 16), (128, 128)]:
+            cnt = m.tile_counts(BM, BN)
+            T = e["T"]
+            nq, nk = -(-T // BM), -(-T // BN)
+            P = np.zeros((nq * BM, nk * BN), dtype=np.int64)
+            P[:T, :T] = D
+            ref = P.reshape(nq, BM, nk, BN).sum(axis=(1, 3))
+            if not np.array_equal(cnt, ref):
+                bad.append(f"tiles {BM}x{BN} of {e}")
+    return bad
+
+
+def check_rejects_invalid():
+    bad = []
+    cases = [
+        dict(T=0), dict(T=8, causal=2), dict(T=8, causal=1, window=-1),
+        dict(T=8, causal=1, radius=2), dict(T=8, causal=0, radius=-2),
+        dict(T=8, causal=0, window=3, radius=1), dict(T=8, stride=-1),
+        dict(T=8, stride=4, offset=4), dict(T=8, stride=0, offset=1),
+        dict(T=8, global_pos=[8]), dict(T=8, global_pos=[-1]),
+        dict(T=8, global_pos=[3, 3]),
+    ]
+    for c in cases:
+        if mask_of(c).validate() == 0:
+            bad.append(f"invalid spec accepted: {c}")
+    return bad
+
+
+# ---------------------------------------------------------------- attention pins
+
+def _rand(T, d, seed, scale_std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return [(torch.randn(T, d, generator=g, dtype=torch.float32) * scale_std)
+            for _ in range(3)]
+
+
+def _oracle_attn(m, Q, K, V, scale, rows=None):
+    return oracle.attention(m, Q.numpy(), K.numpy(), V.numpy(), scale, rows)
+
+
+def check_sdpa_dense():
+    """Unrestricted masks against torch's fp64 SDPA (a library routine)."""
+    bad = []
+    for T, d, seed in [(37, 16, 1), (64, 64, 2), (129, 32, 3)]:
+        Q, K, V = _rand(T, d, seed)
+        sc = 1.0 / math.sqrt(d)
+        q, k, v = (x.double()[None, None] for x in (Q, K, V))
+        full = torch.nn.functional.scaled_dot_product_attention(q, k, v)[0, 0].numpy()
+        caus = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, is_causal=True)[0, 0].numpy()
+        logits = (q @ k.transpose(-1, -2))[0, 0] * sc
+        lse_full = torch.logsumexp(logits, dim=-1).numpy()
+        tri = torch.ones(T, T, dtype=torch.bool).tril()
+        lse_caus = torch.logsumexp(logits.masked_fill(~tri, -math.inf), dim=-1).numpy()
+        O, L = _oracle_attn(oracle.Mask(T, 0, 0, -1), Q, K, V, sc)
+        if not (np.allclose(O, full, rtol=0, atol=1e-12) and
+                np.allclose(L, lse_full, rtol=0, atol=1e-12)):
+            bad.append(f"all-true mask vs SDPA T={T} d={d}: "
+                       f"{np.abs(O - full).max():.3g} {np.abs(L - lse_full).max():.3g}")
+        O, L = _oracle_attn(oracle.Mask(T, 1, 0), Q, K, V, sc)
+        if not (np.allclose(O, caus, rtol=0, atol=1e-12) and
+                np.allclose(L, lse_caus, rtol=0, atol=1e-12)):
+            bad.append(f"window=0 vs causal SDPA T={T} d={d}")
+    return bad
+
+
+def check_sdpa_masked(seed=5):
+    """Every sweep mask against SDPA with the independent numpy boolean mask."""
+    bad = []
+    for n, e in enumerate(small_specs(seed, n=25)):
+        T = e["T"]
+        d = 8 + 8 * (n % 3)
+        Q, K, V = _rand(T, d, 100 + n)
+        sc = 0.7 / math.sqrt(d)
+        D = torch.from_numpy(np_dense_mask(T, e["causal"], e["window"], e["radius"],
+                                           e["stride"], e["offset"], e["global_pos"]))
+        q, k, v = (x.double()[None, None] for x in (Q, K, V))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, attn_mask=D[None, None], scale=sc)[0, 0].numpy()
+        lse = torch.logsumexp(((q @ k.transpose(-1, -2))[0, 0] * sc).masked_fill(
+            ~D, -math.inf), dim=-1).numpy()
+        O, L = _oracle_attn(mask_of(e), Q, K, V, sc)
+        if not (np.allclose(O, ref, rtol=0, atol=1e-12) and
+                np.allclose(L, lse, rtol=0, atol=1e-12)):
+            bad.append(f"masked SDPA mismatch for {e}: {np.abs(O - ref).max():.3g}")
+    return bad
+
+
+def check_special_values():
+    bad = []
+    T, d = 50, 16
+    Q, K, V = _rand(T, d, 11)
+    sc = 1.0 / math.sqrt(d)
+    # w = 1: S_i = {i}, so y_i = v_i exactly and LSE_i = scale q_i.k_i
+    O, L = _oracle_attn(oracle.Mask(T, 1, 1), Q, K, V, sc)
+    if not np.array_equal(O, V.double().numpy()):
+        bad.append("w=1 does not return V")
+    s_ii = sc * (Q.double() * K.double()).sum(-1).numpy()
+    if not np.allclose(L, s_ii, rtol=0, atol=1e-13):
+        bad.append("w=1 LSE is not the self logit")
+    # Q = 0: uniform weights over S_i: y_i = mean of allowed values, LSE = ln |S_i|
+    for e in small_specs(9, n=8) + [dict(T=T, causal=1, window=7, stride=5, offset=2,
+                                         global_pos=[3, 40])]:
+        m = mask_of(e)
+        Tn = e["T"]
+        Qz = torch.zeros(Tn, d)
+        _, Kr, Vr = _rand(Tn, d, 12)
+        O, L = _oracle_attn(m, Qz, Kr, Vr, sc)
+        for i in range(Tn):
+            S = m.row_set(i)
+            want = Vr.double().numpy()[S].mean(axis=0)
+            if not np.allclose(O[i], want, rtol=0, atol=1e-13) or not math.isclose(
+                    L[i], math.log(len(S)), abs_tol=1e-13):
+                bad.append(f"Q=0 row {i} of {e}")
+                break
+    # shift invariance: k_j -> k_j + u adds scale q_i.u to every logit of row i
+    m = oracle.Mask(T, 0, 0, 3, 4, 1, [7, 30])
+    u = torch.randn(d, generator=torch.Generator().manual_seed(13))
+    O1, L1 = _oracle_attn(m, Q, K, V, sc)
+    O2, L2 = _oracle_attn(m, Q, K + u, V, sc)
+    shift = sc * (Q.double() @ u.double()).numpy()
+    if not (np.allclose(O1, O2, rtol=0, atol=1e-6) and
+            np.allclose(L2 - L1, shift, rtol=0, atol=1e-5)):
+        bad.append("key-shift invariance")
+    # bf16 bit-pattern input path equals the fp32 path on the same (exact) values
+    Qb, Kb, Vb = (x.to(torch.bfloat16) for x in (Q, K, V))
+    Ob, Lb = oracle.attention(m, oracle.bf16_bits(Qb), oracle.bf16_bits(Kb),
+                              oracle.bf16_bits(Vb), sc)
+    Of, Lf = _oracle_attn(m, Qb.float(), Kb.float(), Vb.float(), sc)
+    if not (np.array_equal(Ob, Of) and np.array_equal(Lb, Lf)):
+        bad.append("bf16-bits input path differs from the fp32 path")
+    # row subsets give the same rows as the full evaluation
+    rows = np.array([0, 5, 49, 17], dtype=np.int64)
+    Os, Ls = _oracle_attn(m, Q, K, V, sc, rows)
+    if not (np.array_equal(Os, O1[rows]) and np.array_equal(Ls, L1[rows])):
+        bad.append("row subset differs")
+    # renormalising over S_i is not the same as deleting weights after a full
+    # softmax (glossary, §Choose the available reads)
+    full = torch.softmax(sc * Q.double() @ K.double().T, dim=-1)
+    D = torch.from_numpy(np_dense_mask(T, 0, 0, 3, 4, 1, [7, 30]))
+    deleted = (full * D) @ V.double()
+    if np.allclose(O1, deleted.numpy(), atol=1e-3):
+        bad.append("renormalised result equals the deleted-weights result")
+    return bad
+
+
+COUNT_CHECKS = [check_page_counts, check_row_sets, check_reach, check_edge_formula,
+                check_causal_equivalences, check_against_numpy_rules,
+                check_rejects_invalid]
+ATTENTION_CHECKS = [check_sdpa_dense, check_sdpa_masked, check_special_values]

@@ -1,0 +1,54 @@
+"""Planted mistakes: each mutant copy of oracle.c must fail at least one pin.
+
+A mutant is oracle.c with one plausible slip (window off by one, the other stride
+phase, a dropped scale, a transposed or wrong operand, a sign error, a missing causal
+cut).  It is compiled to a temporary library and run against the same checks as the
+real oracle; a mutant that passes every check would show a hole in the pins.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from pins import ATTENTION_CHECKS, COUNT_CHECKS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "window_off_by_one_rule": ("(i - j) < m->window", "(i - j) <= m->window"),
+    "window_off_by_one_set": ("i - m->window + 1;", "i - m->window;"),
+    "stride_phase_zero": ("j % m->stride == m->offset", "j % m->stride == 0"),
+    "stride_start_zero": ("(m->stride > 0) ? m->offset : T", "(m->stride > 0) ? 0 : T"),
+    "global_row_not_causal": ("const int64_t jmax = m->causal ? i : T - 1;",
+                              "const int64_t jmax = T - 1;"),
+    "radius_exclusive": ("llabs(i - j) <= m->radius", "llabs(i - j) < m->radius"),
+    "radius_set_short": ("i + m->radius;", "i + m->radius - 1;"),
+    "global_col_ignored": ("if (in_global(m, j)) return 1;", ""),
+    "dropped_scale": ("s[a] = scale * acc;", "s[a] = acc;"),
+    "normaliser_unshifted": ("l += exp(s[a] - mx);", "l += exp(s[a]);"),
+    "lse_sign": ("LSE[r] = mx + log(l);", "LSE[r] = mx - log(l);"),
+    "value_of_query_row": ("load_elem(V, dtype, j * d + k)", "load_elem(V, dtype, i * d + k)"),
+    "key_transposed": ("load_elem(K, dtype, j * d + k)", "load_elem(K, dtype, k * d + j % d)"),
+    "first_key_skipped": ("for (int64_t a = 0; a < n; a++) l +=", "for (int64_t a = 1; a < n; a++) l +="),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(oracle_mod, tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    c = tmp_path / "mut.c"
+    so = tmp_path / "libmut.so"
+    c.write_text(mutated)
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                           str(c), "-lm"])
+    failures = []
+    with oracle.use_library(str(so)):
+        for check in COUNT_CHECKS + ATTENTION_CHECKS:
+            failures += check()
+            if failures:
+                break
+    assert failures, f"mutant {name} passed every pin"
