@@ -1,0 +1,368 @@
+"""Benchmark: allowed-pair TFLOP/s of the block-sparse masked attention forward pass.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one spattn_fwd call over the whole batch (every (batch, head)) of the
+workload, inputs already resident in HBM.  value = 4 d B H pairs_per_head / t_step
+(2d flops for q.k and 2d for the weighted values per allowed pair: the glossary's
+O(E (d_k + d_v)) cost, "Sparse attention", section "When the cost is linear").
+Under torchrun each rank runs its own copy of the workload on its GPU (heads are
+independent; there is no collective on the data path), and value sums over ranks.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this method) on a
+bounded sample of query rows of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import spattn_workloads as W  # noqa: E402
+
+METRIC = "allowed-pair TFLOP/s (4·d·pairs/s) & % of B300 bf16 tensor peak, 1 GPU"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "t32k_w4096"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM bytes (read + write) per launch of the tensor-core forward kernel on the
+# 32K / W=4096 workload, from the ncu capture summarised in
+# profiles/fwd_tc_t32k_w4096.md, valid for the kernel source with this hash.
+TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+
+
+def kernel_sha() -> str:
+    p = os.path.join(ROOT, "sparse_masked_attention_plan_b300", "csrc", "fwd_tc.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def mask_desc(p):
+    if p["causal"]:
+        s = f"causal window={p['window'] or 'none'}"
+    else:
+        s = f"bidirectional radius={p['radius']}"
+    if p["stride"]:
+        s += f", stride={p['stride']} offset={p['offset']}"
+    if len(p["global_pos"]):
+        s += f", {len(p['global_pos'])} global tokens"
+    return s
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample_rate(cfg, p, Q, K, V, budget_s: float, seed: int = 0):
+    """Time the oracle (as it stands) on seeded sampled query rows of head (0, 0).
+
+    Returns (pairs per second, pairs processed, rows, seconds, threads)."""
+    import oracle
+    oracle.build()
+    T, d = cfg["T"], cfg["d"]
+    m = oracle.Mask(T, p["causal"], p["window"], p["radius"], p["stride"], p["offset"],
+                    p["global_pos"])
+    q, k, v = (oracle.bf16_bits(x[0, 0]) for x in (Q, K, V))
+    scale = 1.0 / math.sqrt(d)
+    # calibrate on a few rows, then size the sample to the budget
+    rows = W.sample_rows(T, 32, seed)
+    t0 = time.perf_counter()
+    oracle.attention(m, q, k, v, scale, rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(T, max(32, 32 * budget_s / dt)))
+    rows = W.sample_rows(T, n, seed + 1)
+    pairs = sum(len(m.row_set(int(r))) for r in rows)
+    t0 = time.perf_counter()
+    oracle.attention(m, q, k, v, scale, rows)
+    secs = time.perf_counter() - t0
+    return pairs / secs, pairs, len(rows), secs, oracle.num_threads()
+
+
+def run_reference(args, cfg, p):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    oracle.build()
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    g = torch.Generator().manual_seed(0)
+    # one head's inputs are all the oracle sample touches
+    Q, K, V = (torch.randn(1, 1, T, d, generator=g).to(torch.bfloat16) for _ in range(3))
+    m = oracle.Mask(T, p["causal"], p["window"], p["radius"], p["stride"], p["offset"],
+                    p["global_pos"])
+    q, k, v = (oracle.bf16_bits(x[0, 0]) for x in (Q, K, V))
+    scale = 1.0 / math.sqrt(d)
+    step_budget = 2.0
+    rows = W.sample_rows(T, 32, 11)
+    t0 = time.perf_counter()
+    oracle.attention(m, q, k, v, scale, rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(T, max(32, 32 * step_budget / dt)))
+    samples = [W.sample_rows(T, n, 100 + s) for s in range(args.warmup + args.steps)]
+    pairs = [sum(len(m.row_set(int(r))) for r in rs) for rs in samples]
+    for s in range(args.warmup):
+        oracle.attention(m, q, k, v, scale, samples[s])
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        oracle.attention(m, q, k, v, scale, samples[s])
+    secs = time.perf_counter() - t0
+    done = sum(pairs[args.warmup:])
+    value = 4 * d * done / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d,
+                   "mask": mask_desc(p),
+                   "step": f"{n} seeded query rows of one head per step (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} steps x {n} rows of head (0,0), "
+                                   f"{done} allowed pairs"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_ours(args, cfg, p):
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    import sparse_masked_attention_plan_b300 as sp
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    # seeded inputs drawn on the host (pinned, reused for the end-to-end leg)
+    Qh, Kh, Vh = W.qkv(B, H, T, d, seed=rank, dtype=torch.bfloat16)
+    Qh, Kh, Vh = (x.pin_memory() for x in (Qh, Kh, Vh))
+    with torch.cuda.stream(stream):
+        q, k, v = (x.to(dev, non_blocking=True) for x in (Qh, Kh, Vh))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    stream.synchronize()
+    t_plan = time.perf_counter()
+    plan = sp.Plan(T, d, **p, stream=stream)
+    stream.synchronize()
+    t_plan = time.perf_counter() - t_plan
+    info = plan.info()
+    pairs_total = info["pairs_per_head"] * B * H
+    flops_step = 4.0 * d * pairs_total
+    items, ents, products = plan.schedule(0)
+    packing = plan.columns().size > 0 or len(p["global_pos"]) > 0
+    launches_per_step = 1 + (1 if packing else 0)
+    in_bytes = 3 * q.numel() * q.element_size()
+    out_bytes = o.numel() * o.element_size() + lse.numel() * 4
+
+    def step():
+        sp.fwd(plan, q, k, v, scale, out=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    plan.check_device(stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for s in range(args.steps):
+            step()
+            ev[s + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    plan.check_device(stream)
+    per = [ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step / (ms_per_step / 1e3) / 1e12
+
+    # end to end through the host-buffer C-ABI entry: H2D of q, k, v, the forward,
+    # D2H of O and LSE, every step
+    oh = torch.empty_like(Qh).pin_memory()
+    lh = torch.empty(B, H, T, dtype=torch.float32).pin_memory()
+    bufs = (q, k, v, o, lse)
+    e2e_steps = max(2, min(args.steps, 5))
+    sp.fwd_host(plan, Qh, Kh, Vh, scale, oh, lh, bufs, stream=stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        sp.fwd_host(plan, Qh, Kh, Vh, scale, oh, lh, bufs, stream=stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = world * flops_step * e2e_steps / e2e_s / 1e12
+
+    peaks, peak_src = load_peaks()
+    kernel_ms = statistics.mean(per) if not packing else None
+    line = None
+    if rank == 0:
+        achieved = flops_step / (kernel_ms / 1e3) / 1e12 if kernel_ms else value / world
+        traffic = (TRAFFIC["bytes_per_launch"]
+                   if TRAFFIC["kernel_sha"] == kernel_sha() else None)
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            rate, pairs_done, nrows, secs, threads = oracle_sample_rate(cfg, p, Qh, Kh, Vh,
+                                                                        args.cpu_budget)
+            cpu = {"value": 4 * d * rate / 1e12, "unit": UNIT, "cores": threads,
+                   "kind": "oracle",
+                   "sample": f"{nrows} seeded query rows of head (0,0) ({pairs_done} allowed "
+                             f"pairs, {secs:.1f} s); pairs/s = {rate:.4g}"}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d,
+                       "mask": mask_desc(p), "pairs_per_head": info["pairs_per_head"],
+                       "tiles_full_partial_empty": [info["n_full"], info["n_partial"],
+                                                    info["n_empty"]],
+                       "tile_products_per_head": products,
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V)",
+                       "plan_build_ms": round(1e3 * t_plan, 2)},
+            "pct_of_bf16_peak": 100.0 * (value / world) / peaks["bf16_tflops"],
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "kernel": "fwd_tc_kernel<%d>" % d,
+                         "kernel_ms": kernel_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+                    "d2h_bytes_per_step": out_bytes,
+                    "api": "spattn_fwd_host (pinned host buffers)"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = W.WORKLOADS[args.workload]
+    p = W.mask_params(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, cfg, p)
+    return run_ours(args, cfg, p)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,209 @@
+/*
+ * spattn.h -- C ABI of the block-sparse masked attention library (libspattn.so).
+ *
+ * The library computes the forward pass of masked scaled-dot-product attention
+ * under structured sparse masks on one NVIDIA B300 (sm_103a):
+ *
+ *     y_i   = sum_{j in S_i} alpha_ij v_j,
+ *     alpha_ij = exp(scale q_i.k_j) / sum_{l in S_i} exp(scale q_i.k_l),
+ *     LSE_i = ln sum_{j in S_i} exp(scale q_i.k_j)
+ *
+ * with the softmax normalised over the allowed set S_i only ("Sparse attention"
+ * glossary, glossary.selfmadequant.com, section "Choose the available reads", the
+ * displayed equation for y_i and alpha_ij).  S_i is a union of simple rules
+ * ("Attention variants", sreshtalluri.github.io, section 4 "Build it from
+ * scratch": causal, sliding_window, local_strided, with_global), intersected with
+ * causality when the mask is causal.  All indices are 0-based.
+ *
+ * Conventions for every call:
+ *   - Every function returns a spattn_status; nothing throws or exits across the
+ *     ABI.  spattn_last_error() gives a message for the last failure on the
+ *     calling thread.
+ *   - Device pointers are CUDA device addresses on the current device; the caller
+ *     owns them.  Q, K, V and O are [B, H, T, d] contiguous row-major tensors of the
+ *     input dtype, 16-byte aligned; LSE is [B, H, T] fp32.
+ *   - `cuda_stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - A plan is reusable across B, H, dtypes and calls (the mask is shared by all
+ *     batches and heads, as create_block_mask(..., B=None, H=None) shares it in
+ *     "Attention variants", section "Use the library").  Distinct plans may be used
+ *     concurrently from different threads; one plan must not be used by two
+ *     concurrent spattn_fwd calls (it owns the packing scratch they would share).
+ */
+#ifndef SPATTN_H_
+#define SPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPATTN_OK = 0,
+  SPATTN_ERR_INVALID_SPEC = 1, /* mask fields outside their domain            */
+  SPATTN_ERR_SHAPE = 2,        /* T, d, B, H or a capacity out of range        */
+  SPATTN_ERR_DTYPE = 3,        /* dtype not supported for this head dim        */
+  SPATTN_ERR_ALIGN = 4,        /* a device pointer is not 16-byte aligned      */
+  SPATTN_ERR_NULL = 5,         /* a required pointer is NULL                   */
+  SPATTN_ERR_CUDA = 6,         /* a CUDA runtime / driver call failed          */
+  SPATTN_ERR_TIMEOUT = 7,      /* a device-side wait ran out of its time budget */
+  SPATTN_ERR_UNSUPPORTED = 8   /* valid request this build does not implement  */
+} spattn_status;
+
+typedef enum { SPATTN_BF16 = 0, SPATTN_FP32 = 1 } spattn_dtype;
+
+/*
+ * Mask specification.  Allowed pairs (i, j), 0 <= i, j < T:
+ *   causal = 1:  j <= i and (0 <= i-j < window  or  window == 0 (no window)
+ *                 or j strided or j global or i global)
+ *   causal = 0:  |i-j| <= radius  (radius == -1: no limit)
+ *                 or j strided or j global or i global
+ * where "j strided" means stride > 0 and j % stride == stride_offset, and
+ * "global" means a member of global_pos.
+ * Sources: window counts the query itself (glossary, "Choose the available
+ * reads": S_i = {max(1,i-w+1),...,i}); window 0 is the full causal triangle and
+ * strided columns are read by every later query (octlm.ramaa.tech "Sparse
+ * attention", section "One mask function for every pattern"); stride_offset 0 is
+ * that page's j % s == 0, stride-1 is local_strided's j % s == s-1 ("Attention
+ * variants", section 4); a bidirectional radius r reads 2r+1 keys ("Attention
+ * variants", section 3, "local radius 2": query 12 reads 10..14); global rows
+ * read every key and global columns are read by every query, and both stay
+ * causal in a causal mask (with_global and the look-ahead warning after it).
+ * Domains: causal in {0,1}; causal: window >= 0 and radius == -1; bidirectional:
+ * radius >= -1 and window == 0; stride >= 0; 0 <= stride_offset < stride (or 0
+ * when stride == 0); 0 <= n_global <= T; global_pos is a HOST array of n_global
+ * distinct positions in [0, T), any order (it is copied; the caller keeps
+ * ownership).  Anything else is SPATTN_ERR_INVALID_SPEC.
+ */
+typedef struct {
+  int32_t causal;
+  int64_t window;
+  int64_t radius;
+  int64_t stride;
+  int64_t stride_offset;
+  int32_t n_global;
+  const int32_t* global_pos;
+} spattn_mask_spec;
+
+typedef struct spattn_plan spattn_plan; /* opaque, owned by the library */
+
+/* Validate a mask spec for sequence length T on the host only (no CUDA call).
+ * Same rules as spattn_plan_create.  SPATTN_OK or SPATTN_ERR_INVALID_SPEC /
+ * SPATTN_ERR_SHAPE (T < 1 or T > 2^30) / SPATTN_ERR_NULL. */
+spattn_status spattn_mask_validate(const spattn_mask_spec* spec, int64_t T);
+
+/*
+ * Build the block-sparse plan of a mask for sequence length T and head dim
+ * head_dim (64 or 128) on the current device.  The plan is the compiled block
+ * mask of "Attention variants" (section "Use the library": create_block_mask,
+ * "never loading zero blocks"): every (query block, key block) tile of the
+ * BM x BN = 128 x 128 grid is classified empty / full / partial from an exact
+ * per-tile count of allowed pairs; strided and global key columns outside each
+ * query group's band are compacted into a dense column list; and the execution
+ * schedule walks only non-empty work.  Kernels run on `cuda_stream`; the call is
+ * synchronous on return.  *out receives a new plan (free with
+ * spattn_plan_destroy).  Errors: NULL, INVALID_SPEC, SHAPE (T out of range or
+ * head_dim not 64/128), CUDA.
+ */
+spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_t head_dim,
+                                 void* cuda_stream, spattn_plan** out);
+
+/* Totals of the natural 128 x 128 grid: allowed pairs per (batch, head) (the
+ * glossary's edge count E, "When the cost is linear"), tile class counts, and
+ * the tile sizes.  Any output pointer may be NULL. */
+spattn_status spattn_plan_info(const spattn_plan* plan, int64_t* pairs_per_head,
+                               int64_t* n_full, int64_t* n_partial, int64_t* n_empty,
+                               int32_t* bm, int32_t* bn);
+
+/* Copy the non-empty tiles of the natural grid to HOST arrays, in canonical order
+ * (qb ascending, then kb ascending): query block, key block, exact allowed-pair
+ * count, class (1 = full: every cell of the tile inside [0,T)^2 is allowed;
+ * 2 = partial).  `cap` is the capacity of each array; *n receives the number of
+ * non-empty tiles (if *n > cap only cap entries are written and the call returns
+ * SPATTN_ERR_SHAPE).  Any of qb/kb/cnt/cls may be NULL to skip it. */
+spattn_status spattn_plan_copy_tiles(const spattn_plan* plan, int32_t* qb, int32_t* kb,
+                                     int32_t* cnt, uint8_t* cls, int64_t cap, int64_t* n);
+
+/* Copy the compacted sparse-column list C = sorted(strided columns U global
+ * columns) to a HOST array (same capacity rules as spattn_plan_copy_tiles). */
+spattn_status spattn_plan_copy_columns(const spattn_plan* plan, int32_t* cols, int64_t cap,
+                                       int64_t* n);
+
+/*
+ * Execution schedule the forward kernels walk, copied to HOST arrays.
+ * which = 0: the bf16 tensor-core kernel (groups of 256 query rows = two 128-row
+ * query tiles); which = 1: the fp32 kernel (groups of 64 rows).
+ * items:   4 int32 per work item  {q_row0, entry_offset, entry_count, flags}
+ *          flags bit 0: rows are global rows gathered from global_pos.
+ * entries: 4 int32 per entry {src_row, flags, kb, lim}
+ *          flags bits 0/1: query tile 0/1 computes this key tile,
+ *          bits 2/3: the tile needs no predicate for query tile 0/1,
+ *          bits 4-5: kind (0 band tile of the natural grid, 1 packed sparse
+ *          columns [src_row, lim) of C, 2 dense causal walk for global rows).
+ * *n_items / *n_entries receive the sizes; arrays shorter than that are an
+ * error (SPATTN_ERR_SHAPE) and nothing is written.  items/entries may be NULL to
+ * query the sizes.  *tile_products receives the number of (query tile, key tile)
+ * products one (batch, head) computes.
+ */
+spattn_status spattn_plan_copy_schedule(const spattn_plan* plan, int32_t which, int32_t* items,
+                                        int64_t item_cap, int64_t* n_items, int32_t* entries,
+                                        int64_t entry_cap, int64_t* n_entries,
+                                        int64_t* tile_products);
+
+/* Enable (1) or disable (0) the device walk counter: every (query tile, key tile)
+ * product the forward kernels compute adds one to a device counter, read with
+ * spattn_plan_walk_count (synchronises the device).  Enabling resets it to 0. */
+spattn_status spattn_plan_set_walk_counter(spattn_plan* plan, int32_t enable);
+spattn_status spattn_plan_walk_count(const spattn_plan* plan, int64_t* count);
+
+/*
+ * Forward pass on device buffers, asynchronous on `cuda_stream`.
+ * Q, K, V: [B, H, T, d] of `dtype` (bf16 or fp32), O: same shape and dtype,
+ * LSE: [B, H, T] fp32 natural log (may be NULL to skip it).  scale > 0 and finite
+ * (the glossary's 1/sqrt(d_k) is the usual choice).  bf16 runs on the tcgen05
+ * tensor-core kernel (fp32 accumulation, fp32 online softmax); fp32 runs on FP32
+ * FMA units.  The first call for a given B*H may allocate the plan's packing
+ * scratch (cudaMalloc); later calls with the same or smaller B*H allocate
+ * nothing.  Device-side waits are bounded: a wait that runs out sets a device
+ * error word which the next spattn_fwd or spattn_plan_check_device call reports
+ * as SPATTN_ERR_TIMEOUT.  Errors: NULL, SHAPE, DTYPE, ALIGN, INVALID_SPEC
+ * (scale), CUDA, TIMEOUT.
+ */
+spattn_status spattn_fwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_dtype dtype,
+                         const void* Q, const void* K, const void* V, float scale, void* O,
+                         float* LSE, void* cuda_stream);
+
+/*
+ * The same forward pass from HOST buffers: copies Q/K/V host -> device, runs
+ * spattn_fwd, copies O and LSE device -> host, all on `cuda_stream`, and returns
+ * after the stream is synchronised.  Host buffers should be pinned for full copy
+ * bandwidth.  The caller provides the device buffers (same shapes) so that this
+ * call allocates nothing beyond spattn_fwd's scratch.  LSE pointers may both be
+ * NULL.
+ */
+spattn_status spattn_fwd_host(const spattn_plan* plan, int32_t B, int32_t H,
+                              spattn_dtype dtype, const void* Q_host, const void* K_host,
+                              const void* V_host, float scale, void* O_host, float* LSE_host,
+                              void* Q_dev, void* K_dev, void* V_dev, void* O_dev,
+                              float* LSE_dev, void* cuda_stream);
+
+/* Synchronise `cuda_stream` and report (then clear) the plan's device error word:
+ * SPATTN_OK, SPATTN_ERR_TIMEOUT or SPATTN_ERR_CUDA. */
+spattn_status spattn_plan_check_device(const spattn_plan* plan, void* cuda_stream);
+
+/* Free a plan and its device memory (NULL is a no-op).  Synchronises the device
+ * first so no in-flight kernel still reads it. */
+void spattn_plan_destroy(spattn_plan* plan);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* spattn_last_error(void);
+
+/* Library version string. */
+const char* spattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPATTN_H_ */

@@ -1,0 +1,250 @@
+"""Block-sparse masked attention for B300 (sm_103a): Python binding of libspattn.so.
+
+A thin ctypes layer over the C ABI declared in ``include/spattn.h``.  It only
+marshals arguments (torch tensors -> device pointers, streams -> handles); every
+step of the computation runs in the library's CUDA kernels.  If the library is
+missing, importing the binding's functions raises: there is no fallback path.
+
+    import torch, sparse_masked_attention_plan_b300 as sp
+    plan = sp.Plan(T=32768, head_dim=128, causal=1, window=4096)
+    o, lse = sp.fwd(plan, q, k, v, scale=128 ** -0.5)      # q, k, v: [B, H, T, d] bf16 cuda
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspattn.so")
+
+OK, ERR_INVALID_SPEC, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_NULL, ERR_CUDA, ERR_TIMEOUT, \
+    ERR_UNSUPPORTED = range(9)
+BF16, FP32 = 0, 1
+
+# Every symbol include/spattn.h declares.
+EXPORTS = ("spattn_mask_validate", "spattn_plan_create", "spattn_plan_info",
+           "spattn_plan_copy_tiles", "spattn_plan_copy_columns", "spattn_plan_copy_schedule",
+           "spattn_plan_set_walk_counter", "spattn_plan_walk_count", "spattn_fwd",
+           "spattn_fwd_host", "spattn_plan_check_device", "spattn_plan_destroy",
+           "spattn_last_error", "spattn_version")
+
+
+class SpattnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"spattn status {status}: {msg}")
+        self.status = status
+
+
+class MaskSpec(ctypes.Structure):
+    _fields_ = [("causal", ctypes.c_int32), ("window", ctypes.c_int64),
+                ("radius", ctypes.c_int64), ("stride", ctypes.c_int64),
+                ("stride_offset", ctypes.c_int64), ("n_global", ctypes.c_int32),
+                ("global_pos", ctypes.POINTER(ctypes.c_int32))]
+
+
+_lib = None
+_lock = threading.Lock()
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_vp = ctypes.c_void_p
+
+
+def lib():
+    """The loaded libspattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with "
+                                  "`python -m sparse_masked_attention_plan_b300.build_lib`")
+            L = ctypes.CDLL(LIB_PATH)
+            st = ctypes.c_int
+            L.spattn_mask_validate.argtypes = [ctypes.POINTER(MaskSpec), ctypes.c_int64]
+            L.spattn_plan_create.argtypes = [ctypes.POINTER(MaskSpec), ctypes.c_int64,
+                                             ctypes.c_int32, _vp, ctypes.POINTER(_vp)]
+            L.spattn_plan_info.argtypes = [_vp, _i64p, _i64p, _i64p, _i64p, _i32p, _i32p]
+            L.spattn_plan_copy_tiles.argtypes = [_vp, _i32p, _i32p, _i32p, _u8p, ctypes.c_int64,
+                                                 _i64p]
+            L.spattn_plan_copy_columns.argtypes = [_vp, _i32p, ctypes.c_int64, _i64p]
+            L.spattn_plan_copy_schedule.argtypes = [_vp, ctypes.c_int32, _i32p, ctypes.c_int64,
+                                                    _i64p, _i32p, ctypes.c_int64, _i64p, _i64p]
+            L.spattn_plan_set_walk_counter.argtypes = [_vp, ctypes.c_int32]
+            L.spattn_plan_walk_count.argtypes = [_vp, _i64p]
+            L.spattn_fwd.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, _vp, _vp,
+                                     _vp, ctypes.c_float, _vp, _vp, _vp]
+            L.spattn_fwd_host.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, _vp,
+                                          _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp,
+                                          _vp, _vp]
+            L.spattn_plan_check_device.argtypes = [_vp, _vp]
+            L.spattn_plan_destroy.argtypes = [_vp]
+            L.spattn_plan_destroy.restype = None
+            L.spattn_last_error.restype = ctypes.c_char_p
+            L.spattn_version.restype = ctypes.c_char_p
+            for name in EXPORTS:
+                if name not in ("spattn_plan_destroy", "spattn_last_error", "spattn_version"):
+                    getattr(L, name).restype = st
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise SpattnError(status, lib().spattn_last_error().decode())
+
+
+def make_spec(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=()):
+    """(MaskSpec, keepalive array) for the mask fields (see include/spattn.h)."""
+    g = np.ascontiguousarray(np.asarray(global_pos, dtype=np.int32))
+    spec = MaskSpec(int(causal), int(window), int(radius), int(stride), int(offset), len(g),
+                    g.ctypes.data_as(_i32p) if len(g) else None)
+    return spec, g
+
+
+def validate(T, **mask) -> int:
+    """Host-only spec check: returns the status code (0 = valid)."""
+    spec, _keep = make_spec(**mask)
+    return lib().spattn_mask_validate(ctypes.byref(spec), int(T))
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """Block-sparse plan of one mask for sequence length T (owns device memory)."""
+
+    def __init__(self, T, head_dim, causal=1, window=0, radius=-1, stride=0, offset=0,
+                 global_pos=(), stream=None):
+        self.T = int(T)
+        self.head_dim = int(head_dim)
+        self.mask = dict(causal=int(causal), window=int(window), radius=int(radius),
+                         stride=int(stride), offset=int(offset),
+                         global_pos=np.asarray(global_pos, dtype=np.int32))
+        spec, keep = make_spec(causal, window, radius, stride, offset, global_pos)
+        h = _vp()
+        _check(lib().spattn_plan_create(ctypes.byref(spec), self.T, self.head_dim,
+                                        _stream_handle(stream), ctypes.byref(h)))
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            lib().spattn_plan_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def info(self) -> dict:
+        v = [ctypes.c_int64() for _ in range(4)]
+        bm, bn = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().spattn_plan_info(self._h, *[ctypes.byref(x) for x in v], ctypes.byref(bm),
+                                      ctypes.byref(bn)))
+        return dict(pairs_per_head=v[0].value, n_full=v[1].value, n_partial=v[2].value,
+                    n_empty=v[3].value, bm=bm.value, bn=bn.value)
+
+    def tiles(self):
+        """(qb, kb, cnt, cls) of the non-empty tiles, canonical order."""
+        n = ctypes.c_int64()
+        lib().spattn_plan_copy_tiles(self._h, None, None, None, None, 0, ctypes.byref(n))
+        k = n.value
+        qb = np.zeros(k, np.int32)
+        kb = np.zeros(k, np.int32)
+        cnt = np.zeros(k, np.int32)
+        cls = np.zeros(k, np.uint8)
+        _check(lib().spattn_plan_copy_tiles(self._h, qb.ctypes.data_as(_i32p),
+                                            kb.ctypes.data_as(_i32p), cnt.ctypes.data_as(_i32p),
+                                            cls.ctypes.data_as(_u8p), k, ctypes.byref(n)))
+        return qb, kb, cnt, cls
+
+    def columns(self) -> np.ndarray:
+        n = ctypes.c_int64()
+        lib().spattn_plan_copy_columns(self._h, None, 0, ctypes.byref(n))
+        out = np.zeros(n.value, np.int32)
+        _check(lib().spattn_plan_copy_columns(self._h, out.ctypes.data_as(_i32p), n.value,
+                                              ctypes.byref(n)))
+        return out
+
+    def schedule(self, which=0):
+        """(items [n,4], entries [m,4], tile_products) of the execution schedule."""
+        ni, ne, tp = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().spattn_plan_copy_schedule(self._h, int(which), None, 0, ctypes.byref(ni),
+                                               None, 0, ctypes.byref(ne), ctypes.byref(tp)))
+        items = np.zeros((ni.value, 4), np.int32)
+        ents = np.zeros((ne.value, 4), np.int32)
+        _check(lib().spattn_plan_copy_schedule(self._h, int(which), items.ctypes.data_as(_i32p),
+                                               ni.value, ctypes.byref(ni),
+                                               ents.ctypes.data_as(_i32p), ne.value,
+                                               ctypes.byref(ne), ctypes.byref(tp)))
+        return items, ents, tp.value
+
+    def set_walk_counter(self, enable=True):
+        _check(lib().spattn_plan_set_walk_counter(self._h, 1 if enable else 0))
+
+    def walk_count(self) -> int:
+        v = ctypes.c_int64()
+        _check(lib().spattn_plan_walk_count(self._h, ctypes.byref(v)))
+        return v.value
+
+    def check_device(self, stream=None):
+        _check(lib().spattn_plan_check_device(self._h, _stream_handle(stream)))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def fwd(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None, want_lse=True):
+    """Forward pass on device tensors q, k, v: [B, H, T, d] (bf16 or fp32, contiguous).
+
+    Returns (O, LSE); O has q's dtype, LSE is fp32 [B, H, T].  Asynchronous on
+    `stream` (default: torch's current stream)."""
+    import torch
+    B, H, T, d = q.shape
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, H, T, d):
+            raise ValueError("q, k, v must be contiguous CUDA tensors of equal shape")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    _check(lib().spattn_fwd(plan.handle, B, H, _dtype_code(q), q.data_ptr(), k.data_ptr(),
+                            v.data_ptr(), float(scale), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None,
+                            _stream_handle(stream)))
+    return out, lse
+
+
+def fwd_host(plan: Plan, q_host, k_host, v_host, scale: float, o_host, lse_host, dev_bufs,
+             stream=None):
+    """End-to-end call from host tensors (pinned): copies in, computes, copies out.
+
+    dev_bufs = (q_dev, k_dev, v_dev, o_dev, lse_dev) preallocated on the device."""
+    B, H, T, d = q_host.shape
+    qd, kd, vd, od, ld = dev_bufs
+    _check(lib().spattn_fwd_host(plan.handle, B, H, _dtype_code(q_host), q_host.data_ptr(),
+                                 k_host.data_ptr(), v_host.data_ptr(), float(scale),
+                                 o_host.data_ptr(),
+                                 lse_host.data_ptr() if lse_host is not None else None,
+                                 qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                                 ld.data_ptr() if ld is not None else None,
+                                 _stream_handle(stream)))
+    return o_host, lse_host

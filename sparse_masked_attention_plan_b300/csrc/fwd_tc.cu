@@ -1,0 +1,482 @@
+// fwd_tc.cu -- bf16 forward pass of block-sparse masked attention on the fifth-
+// generation tensor cores (tcgen05) of sm_103a.
+//
+// What it computes, per (batch, head) and query row i with allowed set S_i:
+//     y_i = sum_{j in S_i} softmax_j(scale q_i.k_j) v_j,  LSE_i = ln sum exp(...)
+// with the softmax normalised over S_i only ("Sparse attention" glossary,
+// glossary.selfmadequant.com, section "Choose the available reads", the displayed
+// equation).  Only the schedule's tiles are computed: band tiles of the natural
+// 128 x 128 grid and packed tiles of strided / global columns; empty tiles are never
+// loaded ("Attention variants", sreshtalluri.github.io, section "Use the library":
+// block-level skipping; "Sparse attention" glossary, "When the cost is linear":
+// block computation that skips excluded regions).
+//
+// One CTA = one work item = two 128-row query tiles of one (batch, head) sharing a
+// stream of key/value tiles.  Warp roles (320 threads):
+//   warps 0-3  softmax + correction + epilogue for query tile 0 (TMEM lanes 0-127)
+//   warps 4-7  the same for query tile 1
+//   warp 8     TMA producer: Q tiles once, then K and V tiles into a ring of slots
+//   warp 9     MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V, tcgen05
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+// P_t (bf16) overwrites the first 64 columns of S_t and feeds the PV product
+// directly from TMEM.  The MMA issue order
+//     S0(n), PV1(n-1), S1(n), PV0(n)
+// lets the softmax of one query tile overlap the other tile's two products.
+// Online softmax in fp32 with the exp2 form and a conditional rescale: the running
+// maximum moves (and O is rescaled) only when a row maximum grows by more than
+// 2^8; the final O / l and LSE use the same stale maximum, so the result is exact.
+// One thread owns one query row (its TMEM lane), so row max and row sum need no
+// cross-thread reduction.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "predicate.cuh"
+#include "ptx.cuh"
+
+namespace spattn {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct TcCfg {
+  static constexpr int kChunkBytes = kTile * 64 * 2;  // 128 rows x 64 bf16, one swizzle span
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kSmemQ = 2 * kTileBytes;
+  static constexpr int kSmemKV = kStages * kTileBytes;
+  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_final
+  static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
+                       kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
+                       kBarO = 2 * kStages + 5, kNumBars = 2 * kStages + 6;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;       // S / P of query tile 0, 1
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;  // O of query tile 0, 1
+};
+
+struct KParams {
+  __nv_bfloat16* O;
+  float* LSE;
+  float scale_log2;
+  const uint32_t* colmask;
+  MaskDev mask;
+  const int4* items;
+  const int4* entries;
+  unsigned long long* walk;
+  int* err;
+  uint64_t budget;
+};
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  using C = TcCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc_sw128(a_smem + off, 16, 1024), smem_desc_sw128(b_smem + off, 16, 1024),
+           C::kIdescQK, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  using C = TcCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 16 * 128, C::kChunkBytes, 1024),
+           C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQg,
+                  const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
+                  const KParams p) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_addr(smem);
+  const uint32_t sKV = sQ + C::kSmemQ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemQ + C::kSmemKV);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  const uint32_t bar0 = smem_addr(bars);
+#define BAR(k) (bar0 + 8u * static_cast<uint32_t>(k))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int4 item = p.items[blockIdx.x];
+  const int bh = blockIdx.y;
+  const int n_ent = item.z;
+  const int4* ents = p.entries + item.y;
+  const bool gathered = (item.w & kItemGathered) != 0;
+  const MaskDev& m = p.mask;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(BAR(C::kBarFull + s), 1);
+      mbar_init(BAR(C::kBarEmpty + s), 1);
+    }
+    mbar_init(BAR(C::kBarQ), 1);
+    mbar_init(BAR(C::kBarS + 0), 1);
+    mbar_init(BAR(C::kBarS + 1), 1);
+    mbar_init(BAR(C::kBarP + 0), 128);
+    mbar_init(BAR(C::kBarP + 1), 128);
+    mbar_init(BAR(C::kBarO), 1);
+    fence_barrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(gathered ? &tmQg : &tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const void* mapQ = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
+      mbar_arrive_expect_tx(BAR(C::kBarQ), 2 * C::kTileBytes);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64,
+                      item.x + t * kTile, bh);
+      int issued = 0;
+      for (int n = 0; n < n_ent; ++n) {
+        const int4 e = ents[n];
+        const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
+        bool ok = true;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * n + kv;
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout)) {
+            ok = false;
+            break;
+          }
+          const void* map = kv ? (packed ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV))
+                               : (packed ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK));
+          mbar_arrive_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
+                        c * 64, e.x, bh);
+          ++issued;
+        }
+        if (!ok) break;
+      }
+      // Drain: wait until the last load issued into each slot has landed, so no
+      // copy is still writing this CTA's shared memory when it exits.
+      for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+        mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
+                  kErrTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      unsigned long long walked = 0;
+      if (mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout)) {
+        tc_fence_after();
+        int pend1 = -1;
+        uint32_t pend_vs = 0;
+        uint32_t pph[2] = {0u, 0u};
+        bool oinit[2] = {false, false};
+        bool ok = true;
+        for (int n = 0; n < n_ent && ok; ++n) {
+          const int4 e = ents[n];
+          const bool a0 = (e.y & kActive0) != 0, a1 = (e.y & kActive1) != 0;
+          const int kit = 2 * n, vit = 2 * n + 1;
+          const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
+          if (!mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1, p.budget, p.err,
+                         kErrTimeout)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_smem = sKV + ks * C::kTileBytes;
+          if (a0) {
+            issue_qk<D>(tmem + C::kColS0, sQ, k_smem);
+            mma_commit(BAR(C::kBarS + 0));
+            ++walked;
+          }
+          if (pend1 >= 0) {
+            if (!mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout)) { ok = false; break; }
+            pph[1] ^= 1u;
+            tc_fence_after();
+            issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, sKV + pend_vs * C::kTileBytes, oinit[1]);
+            oinit[1] = true;
+            mma_commit(BAR(C::kBarEmpty + pend_vs));
+            pend1 = -1;
+          }
+          if (a1) {
+            issue_qk<D>(tmem + C::kColS1, sQ + C::kTileBytes, k_smem);
+            mma_commit(BAR(C::kBarS + 1));
+            ++walked;
+          }
+          mma_commit(BAR(C::kBarEmpty + ks));
+          if (!mbar_wait(BAR(C::kBarFull + vs), (vit / C::kStages) & 1, p.budget, p.err,
+                         kErrTimeout)) { ok = false; break; }
+          tc_fence_after();
+          if (a0) {
+            if (!mbar_wait(BAR(C::kBarP + 0), pph[0], p.budget, p.err, kErrTimeout)) { ok = false; break; }
+            pph[0] ^= 1u;
+            tc_fence_after();
+            issue_pv<D>(tmem + C::kColO0, tmem + C::kColS0, sKV + vs * C::kTileBytes, oinit[0]);
+            oinit[0] = true;
+          }
+          if (a1) {
+            pend1 = n;
+            pend_vs = vs;
+          } else {
+            mma_commit(BAR(C::kBarEmpty + vs));
+          }
+        }
+        if (ok && pend1 >= 0) {
+          if (mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout)) {
+            tc_fence_after();
+            issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, sKV + pend_vs * C::kTileBytes, oinit[1]);
+            mma_commit(BAR(C::kBarEmpty + pend_vs));
+          }
+        }
+      }
+      // Arrives when every product issued above has completed; the epilogue reads
+      // O after it, and waiting here keeps TMEM allocated until no product runs.
+      mma_commit(BAR(C::kBarO));
+      mbar_wait(BAR(C::kBarO), 0, p.budget, p.err, kErrTimeout);
+      if (p.walk && walked) atomicAdd(p.walk, walked);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int wg = warp >> 2;
+    const int r = ((warp & 3) << 5) | lane;
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
+    const uint32_t colS = wg ? C::kColS1 : C::kColS0, colO = wg ? C::kColO1 : C::kColO0;
+    const int local = wg * kTile + r;
+    int i;
+    bool valid;
+    if (gathered) {
+      const int a = item.x + local;
+      valid = a < m.n_global;
+      i = valid ? m.gpos[a] : 0;
+    } else {
+      i = item.x + local;
+      valid = i < m.T;
+    }
+    const float c2 = p.scale_log2;
+    float mrow = -INFINITY, lrow = 0.f;
+    uint32_t sph = 0;
+    int n_done = 0;
+    for (int n = 0; n < n_ent; ++n) {
+      const int4 e = ents[n];
+      if (!(e.y & (kActive0 << wg))) continue;
+      const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
+      if (!__all_sync(0xffffffffu, got)) break;
+      sph ^= 1u;
+      tc_fence_after();
+      // pass 1: row maximum of the allowed logits (S stays in TMEM)
+      const bool full = (e.y & (kFull0 << wg)) != 0;
+      RowPredicate pr;
+      if (!full) pr = make_predicate(m, p.colmask, e, i);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + colS + 32 * q, v);
+#pragma unroll
+        for (int b = 0; b < 32; ++b) {
+          const float x = __uint_as_float(v[b]);
+          mx = (full || pred_allowed(pr, 32 * q + b)) ? fmaxf(mx, x) : mx;
+        }
+      }
+      const float mcand = fmaxf(mrow, mx * c2);
+      const bool need = mcand > mrow + kRescaleThreshold;
+      float corr = 1.f;
+      if (need) {
+        corr = fast_exp2(mrow - mcand);
+        mrow = mcand;
+        lrow *= corr;
+      }
+      const float msub = (mrow == -INFINITY) ? 0.f : mrow;
+      // pass 2: P = 2^(s * scale * log2 e - m), stored as bf16 over the first half of S
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + colS + 32 * q, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          const int c0 = 32 * q + 2 * b;
+          float x0 = fmaf(__uint_as_float(v[2 * b]), c2, -msub);
+          float x1 = fmaf(__uint_as_float(v[2 * b + 1]), c2, -msub);
+          if (!full) {
+            x0 = pred_allowed(pr, c0) ? x0 : -INFINITY;
+            x1 = pred_allowed(pr, c0 + 1) ? x1 : -INFINITY;
+          }
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          sum += p0 + p1;
+          pk[b] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(lane_base + colS + 16 * q, pk);
+      }
+      lrow += sum;
+      if (n_done > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + colO + 32 * q, o);
+#pragma unroll
+          for (int b = 0; b < 32; ++b) o[b] = __float_as_uint(__uint_as_float(o[b]) * corr);
+          tmem_st32(lane_base + colO + 32 * q, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(C::kBarP + wg));
+      ++n_done;
+    }
+    // ---------------------------------------------------------- epilogue
+    if (n_done > 0) {
+      const bool got = mbar_wait(BAR(C::kBarO), 0, p.budget, p.err, kErrTimeout);
+      if (__all_sync(0xffffffffu, got)) {
+        tc_fence_after();
+        const bool write = valid && (gathered || !m.rowglobal[i]);
+        const float inv = (write && lrow > 0.f) ? 1.f / lrow : 0.f;
+        const size_t row = static_cast<size_t>(bh) * m.T + i;
+        uint4* dst = reinterpret_cast<uint4*>(p.O + row * D);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + colO + 32 * q, o);
+          if (write) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+              dst[4 * q + v4] = w;
+            }
+          }
+        }
+        if (write && p.LSE) p.LSE[row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+#undef BAR
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [BH][rows][D] bf16, boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap* map, const void* base, int D, long long rows, long long BH) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  if (rows < 1) rows = 1;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
+  using C = TcCfg<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const long long T = a.mask.T;
+  CUtensorMap mQ, mK, mV, mQg, mKc, mVc;
+  bool ok = make_map(&mQ, a.Q, D, T, a.BH) && make_map(&mK, a.K, D, T, a.BH) &&
+            make_map(&mV, a.V, D, T, a.BH);
+  ok = ok && (a.n_cols > 0 ? make_map(&mKc, a.Kc, D, a.n_cols, a.BH) && make_map(&mVc, a.Vc, D, a.n_cols, a.BH)
+                           : (mKc = mK, mVc = mV, true));
+  ok = ok && (a.mask.n_global > 0 ? make_map(&mQg, a.Qg, D, a.mask.n_global, a.BH) : (mQg = mQ, true));
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  KParams kp;
+  kp.O = static_cast<__nv_bfloat16*>(a.O);
+  kp.LSE = a.LSE;
+  kp.scale_log2 = a.scale * 1.4426950408889634f;
+  kp.colmask = a.colmask;
+  kp.mask = a.mask;
+  kp.items = a.items;
+  kp.entries = a.entries;
+  kp.walk = a.walk;
+  kp.err = a.err;
+  kp.budget = a.wait_budget_ns;
+  dim3 grid(a.n_items, a.BH);
+  fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(mQ, mK, mV, mQg, mKc, mVc, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why) {
+  if (a.n_items == 0) return cudaSuccess;
+  if (d == 64) return launch_d<64>(a, st, why);
+  if (d == 128) return launch_d<128>(a, st, why);
+  *why = "head dim must be 64 or 128";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace spattn

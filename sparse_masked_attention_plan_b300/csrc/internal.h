@@ -1,0 +1,153 @@
+// internal.h -- library-internal types shared by the host API and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+namespace spattn {
+
+constexpr int kTile = 128;  // BM = BN of the natural grid
+
+// Entry flag layout (see spattn_plan_copy_schedule in spattn.h).
+constexpr int kActive0 = 1, kActive1 = 2, kFull0 = 4, kFull1 = 8;
+constexpr int kKindShift = 4;
+constexpr int kKindBand = 0, kKindPacked = 1, kKindDense = 2;
+constexpr int kItemGathered = 1;
+
+// Device error word bits.
+constexpr int kErrTimeout = 1;
+
+// Normalised mask, as the kernels see it.  T <= 2^30, so rows and columns fit int32.
+struct MaskDev {
+  int32_t T;
+  int32_t causal;
+  int32_t window;  // causal local width, 0 = none
+  int32_t radius;  // bidirectional radius, -1 = none
+  int32_t stride;  // 0 = none
+  int32_t offset;
+  int32_t n_global;
+  int32_t n_gns;               // globals that are not strided columns
+  const int32_t* gpos;         // sorted distinct global positions [n_global]
+  const int32_t* gpos_ns;      // sorted globals that are not strided [n_gns]
+  const uint8_t* rowglobal;    // [T] 1 where the row is a global token
+};
+
+struct Schedule {
+  int32_t group_rows = 0;  // query rows per work item
+  int32_t qtile_rows = 0;  // rows per query tile
+  int32_t n_qtiles = 0;    // query tiles per work item
+  std::vector<int32_t> items;    // 4 per item, launch order
+  std::vector<int32_t> entries;  // 4 per entry
+  int4* d_items = nullptr;
+  int4* d_entries = nullptr;
+  int64_t tile_products = 0;  // (query tile x key tile) products per (batch, head)
+};
+
+}  // namespace spattn
+
+struct spattn_plan {
+  // normalised spec
+  int32_t causal = 1;
+  int64_t window = 0, radius = -1, stride = 0, offset = 0;
+  int64_t T = 0;
+  int32_t d = 0;
+  int device = 0;
+  std::vector<int32_t> gpos;     // sorted distinct
+  std::vector<int32_t> gpos_ns;  // globals that are not strided columns
+  // natural grid
+  int32_t nqb = 0, nkb = 0;
+  int64_t pairs = 0, n_full = 0, n_partial = 0, n_empty = 0, n_nonempty = 0;
+  int32_t* d_tile_qb = nullptr;
+  int32_t* d_tile_kb = nullptr;
+  int32_t* d_tile_cnt = nullptr;
+  uint8_t* d_tile_cls = nullptr;
+  // sparse columns
+  int32_t n_cols = 0;
+  std::vector<int32_t> cols;  // host copy of the compacted columns
+  int32_t* d_cols = nullptr;
+  uint32_t* d_colmask = nullptr;  // [nkb][4] bit c: column kb*128+c is strided or global
+  uint8_t* d_rowglobal = nullptr;
+  int32_t* d_gpos = nullptr;
+  int32_t* d_gpos_ns = nullptr;
+  // execution schedules: [0] tensor-core bf16 kernel, [1] fp32 kernel
+  spattn::Schedule sched[2];
+  // packing scratch (packed K, V of the sparse columns and gathered global-row Q)
+  void* d_scratch = nullptr;
+  size_t scratch_bytes = 0;
+  // debug walk counter and device error word
+  unsigned long long* d_walk = nullptr;
+  int32_t walk_enabled = 0;
+  int* d_err = nullptr;
+  uint64_t wait_budget_ns = 4000000000ull;
+
+  spattn::MaskDev mask_dev() const {
+    spattn::MaskDev m;
+    m.T = static_cast<int32_t>(T);
+    m.causal = causal;
+    m.window = static_cast<int32_t>(window);
+    m.radius = static_cast<int32_t>(radius);
+    m.stride = static_cast<int32_t>(stride);
+    m.offset = static_cast<int32_t>(offset);
+    m.n_global = static_cast<int32_t>(gpos.size());
+    m.n_gns = static_cast<int32_t>(gpos_ns.size());
+    m.gpos = d_gpos;
+    m.gpos_ns = d_gpos_ns;
+    m.rowglobal = d_rowglobal;
+    return m;
+  }
+};
+
+// ---- launchers implemented in the .cu files (host side, return cudaError_t) ----
+namespace spattn {
+
+// plan_kernels.cu
+cudaError_t launch_column_flags(const MaskDev& m, uint8_t* flags, uint8_t* rowglobal,
+                                cudaStream_t st);
+cudaError_t launch_compact_columns(const uint8_t* flags, int32_t T, int32_t* cols,
+                                   int32_t* n_cols, cudaStream_t st);
+cudaError_t launch_colmask(const uint8_t* flags, int32_t T, int32_t nkb, uint32_t* colmask,
+                           cudaStream_t st);
+cudaError_t launch_tile_count(const MaskDev& m, const uint32_t* colmask, int32_t nqb,
+                              int32_t nkb, int32_t* q_nonempty, int32_t* q_full,
+                              long long* q_pairs, cudaStream_t st);
+cudaError_t launch_tile_fill(const MaskDev& m, const uint32_t* colmask, int32_t nqb,
+                             int32_t nkb, const int32_t* q_offset, int32_t* tile_qb,
+                             int32_t* tile_kb, int32_t* tile_cnt, uint8_t* tile_cls,
+                             cudaStream_t st);
+
+// pack_kernel.cu: gathers rows of K and V at `cols` and rows of Q at `gpos`.
+cudaError_t launch_pack(const void* Q, const void* K, const void* V, void* Kc, void* Vc,
+                        void* Qg, const int32_t* cols, int32_t n_cols, const int32_t* gpos,
+                        int32_t n_global, int64_t BH, int64_t T, int32_t row_bytes,
+                        cudaStream_t st);
+
+// fwd_tc.cu (bf16 tensor-core forward)
+struct TcArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* Kc;
+  const void* Vc;
+  const void* Qg;
+  void* O;
+  float* LSE;
+  int32_t BH;
+  int32_t n_cols;
+  float scale;
+  const uint32_t* colmask;
+  MaskDev mask;
+  const int4* items;
+  const int4* entries;
+  int32_t n_items;
+  unsigned long long* walk;
+  int* err;
+  uint64_t wait_budget_ns;
+};
+cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why);
+
+// fwd_simt.cu (fp32 forward)
+cudaError_t launch_fwd_simt(int d, const TcArgs& a, cudaStream_t st);
+
+}  // namespace spattn

@@ -1,0 +1,75 @@
+// predicate.cuh -- the per-element mask predicate the forward kernels apply inside
+// tiles that are not entirely allowed.
+//
+// For query row i and a key tile whose column c maps to key j, every schedule
+// entry kind reduces to one test:
+//     allowed(c) = (lo <= c <= hi)  or  (bit c of the tile's column mask and c <= hb)
+// * band tile of the natural grid (keys k0..k0+127): [lo, hi] is the local window
+//   of row i (causal: i-w+1 .. i, "Sparse attention" glossary, section "Choose the
+//   available reads"; bidirectional: i-r .. i+r, "Attention variants" section 3),
+//   the column mask marks strided and global columns, readable up to hb (= i in a
+//   causal mask, octlm "Sparse attention", "One mask function for every pattern").
+// * packed sparse columns [src, lim): every packed column is a strided or global
+//   column that lies before the group's band (causal) or anywhere (bidirectional),
+//   so only c < lim - src is tested.
+// * dense walk of a global row: every key j <= i (causal) or every key
+//   ("Attention variants", section 4, with_global).
+// Keys at or past T (ragged last tile) fall outside [lo, hi] and past hb.
+#pragma once
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace spattn {
+
+struct RowPredicate {
+  int lo, hi, hb;
+  uint32_t bits[4];
+};
+
+__device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const uint32_t* colmask,
+                                                       int4 e, int i) {
+  RowPredicate p;
+  const int kind = (e.y >> kKindShift) & 3;
+  const int k0 = e.x;
+  p.bits[0] = p.bits[1] = p.bits[2] = p.bits[3] = 0u;
+  p.hb = -1;
+  if (kind == kKindBand) {
+    int lo, hi, hb;
+    if (m.causal) {
+      lo = m.window ? i - m.window + 1 : 0;
+      hi = i;
+      hb = i;
+    } else {
+      lo = m.radius >= 0 ? i - m.radius : 0;
+      hi = m.radius >= 0 ? i + m.radius : m.T - 1;
+      hb = m.T - 1;
+    }
+    hi = min(hi, m.T - 1);
+    hb = min(hb, m.T - 1);
+    p.lo = lo - k0;
+    p.hi = hi - k0;
+    p.hb = hb - k0;
+    const uint4 w = *reinterpret_cast<const uint4*>(colmask + 4 * e.z);
+    p.bits[0] = w.x;
+    p.bits[1] = w.y;
+    p.bits[2] = w.z;
+    p.bits[3] = w.w;
+  } else if (kind == kKindPacked) {
+    p.lo = 0;
+    p.hi = e.w - e.x - 1;
+  } else {
+    p.lo = 0;
+    p.hi = (m.causal ? min(i, m.T - 1) : m.T - 1) - k0;
+  }
+  return p;
+}
+
+__device__ __forceinline__ bool pred_allowed(const RowPredicate& p, int c) {
+  const bool in_band = c >= p.lo && c <= p.hi;
+  const bool in_cols = ((p.bits[c >> 5] >> (c & 31)) & 1u) && c <= p.hb;
+  return in_band || in_cols;
+}
+
+}  // namespace spattn

@@ -1,0 +1,573 @@
+// spattn_api.cu -- the C ABI (include/spattn.h): spec validation, plan building
+// (GPU kernels + host scheduler), forward dispatch, errors.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "spattn.h"
+
+using spattn::kTile;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+spattn_status fail(spattn_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define CUDA_TRY(expr)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (expr);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(SPATTN_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));     \
+  } while (0)
+
+constexpr int64_t kMaxT = int64_t(1) << 30;
+
+template <typename T>
+cudaError_t dev_alloc(T** p, size_t n) {
+  return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(n, 1) * sizeof(T));
+}
+
+void free_plan_memory(spattn_plan* p) {
+  void* ptrs[] = {p->d_tile_qb, p->d_tile_kb, p->d_tile_cnt, p->d_tile_cls, p->d_cols,
+                  p->d_colmask, p->d_rowglobal, p->d_gpos, p->d_gpos_ns, p->d_scratch,
+                  p->d_walk, p->d_err, p->sched[0].d_items, p->sched[0].d_entries,
+                  p->sched[1].d_items, p->sched[1].d_entries};
+  for (void* q : ptrs)
+    if (q) cudaFree(q);
+}
+
+// ---- host scheduler ---------------------------------------------------------------
+//
+// A work item is a group of `group_rows` query rows split into `n_qtiles` query
+// tiles of `qtile_rows`.  Its entries are (1) the band key tiles of the natural grid
+// that the local rule of its rows reaches, and (2) chunks of up to 128 packed sparse
+// columns that lie outside that band.  Each entry records which query tiles have at
+// least one allowed pair in it (the others skip it) and which need no predicate.
+// Global rows get their own items that walk every key tile their causality permits.
+
+struct Sched {
+  const spattn_plan* p;
+  int64_t lower(int64_t v) const {  // #C < v
+    return std::lower_bound(p->cols.begin(), p->cols.end(), static_cast<int32_t>(
+                                std::min<int64_t>(v, INT32_MAX))) - p->cols.begin();
+  }
+  int64_t upper(int64_t v) const {  // #C <= v
+    return std::upper_bound(p->cols.begin(), p->cols.end(), static_cast<int32_t>(
+                                std::min<int64_t>(v, INT32_MAX))) - p->cols.begin();
+  }
+  // Any (i in [a,b], j in [k0,k1]) allowed by the local rule?
+  bool local_meets(int64_t a, int64_t b, int64_t k0, int64_t k1) const {
+    if (p->causal) {
+      if (k0 > b) return false;
+      return p->window == 0 || std::max<int64_t>(0, a - k1) < p->window;
+    }
+    if (p->radius < 0) return true;
+    return std::max<int64_t>(0, std::max(k0 - b, a - k1)) <= p->radius;
+  }
+  // Every (i in [a,b], j in [k0,k1]) allowed by the local rule?
+  bool local_covers(int64_t a, int64_t b, int64_t k0, int64_t k1) const {
+    if (p->causal) return k1 <= a && (p->window == 0 || b - k0 < p->window);
+    if (p->radius < 0) return true;
+    return b - k0 <= p->radius && k1 - a <= p->radius;
+  }
+  bool cols_in(int64_t x, int64_t y) const { return y >= x && upper(y) - lower(x) > 0; }
+};
+
+void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, int qtile_rows,
+                    int n_qtiles, bool longest_first) {
+  using namespace spattn;
+  Sched h{p};
+  const int64_t T = p->T;
+  const int64_t nc = p->n_cols;
+  s->group_rows = group_rows;
+  s->qtile_rows = qtile_rows;
+  s->n_qtiles = n_qtiles;
+  s->items.clear();
+  s->entries.clear();
+  s->tile_products = 0;
+  struct Item { int32_t q0, off, cnt, flags; };
+  std::vector<Item> items;
+  auto push = [&](int32_t src, int32_t flags, int32_t kb, int32_t lim) {
+    s->entries.insert(s->entries.end(), {src, flags, kb, lim});
+    s->tile_products += ((flags & kActive0) ? 1 : 0) + ((flags & kActive1) ? 1 : 0);
+  };
+  const int64_t n_groups = (T + group_rows - 1) / group_rows;
+  for (int64_t g = 0; g < n_groups; ++g) {
+    const int64_t r0 = g * group_rows, r1 = std::min<int64_t>(r0 + group_rows, T) - 1;
+    int64_t jlo, jhi;
+    if (p->causal) {
+      jlo = p->window ? std::max<int64_t>(0, r0 - p->window + 1) : 0;
+      jhi = r1;
+    } else {
+      jlo = p->radius >= 0 ? std::max<int64_t>(0, r0 - p->radius) : 0;
+      jhi = p->radius >= 0 ? std::min<int64_t>(T - 1, r1 + p->radius) : T - 1;
+    }
+    const int64_t kb_lo = jlo / kTile, kb_hi = jhi / kTile;
+    const int32_t off = static_cast<int32_t>(s->entries.size() / 4);
+    for (int64_t kb = kb_lo; kb <= kb_hi; ++kb) {
+      const int64_t k0 = kb * kTile, k1 = std::min<int64_t>(k0 + kTile, T) - 1;
+      const bool ragged = k0 + kTile > T;
+      int32_t flags = kKindBand << kKindShift;
+      for (int t = 0; t < n_qtiles; ++t) {
+        const int64_t a = r0 + int64_t(t) * qtile_rows;
+        if (a >= T) continue;
+        const int64_t b = std::min<int64_t>(a + qtile_rows, T) - 1;
+        const bool active = h.local_meets(a, b, k0, k1) ||
+                            h.cols_in(k0, p->causal ? std::min(k1, b) : k1);
+        if (!active) continue;
+        flags |= kActive0 << t;
+        if (!ragged && h.local_covers(a, b, k0, k1)) flags |= kFull0 << t;
+      }
+      if (flags & (kActive0 | kActive1)) push(static_cast<int32_t>(k0), flags, static_cast<int32_t>(kb), 0);
+    }
+    if (nc > 0) {
+      const int64_t a_idx = h.lower(kb_lo * kTile), b_idx = h.lower((kb_hi + 1) * kTile);
+      const int64_t e_idx = p->causal ? h.upper(r1) : nc;
+      const int64_t ranges[2][2] = {{0, std::min(a_idx, e_idx)}, {b_idx, e_idx}};
+      for (auto& rg : ranges) {
+        for (int64_t s0 = rg[0]; s0 < rg[1]; s0 += kTile) {
+          const int64_t lim = rg[1];
+          int32_t flags = kKindPacked << kKindShift;
+          for (int t = 0; t < n_qtiles; ++t) {
+            const int64_t a = r0 + int64_t(t) * qtile_rows;
+            if (a >= T) continue;
+            const int64_t b = std::min<int64_t>(a + qtile_rows, T) - 1;
+            // causal: packed columns precede the band, so every row reads them
+            if (p->causal && p->cols[s0] > b) continue;
+            flags |= kActive0 << t;
+            const bool whole = s0 + kTile <= lim &&
+                               (!p->causal || p->cols[s0 + kTile - 1] <= a);
+            if (whole) flags |= kFull0 << t;
+          }
+          if (flags & (kActive0 | kActive1))
+            push(static_cast<int32_t>(s0), flags, -1, static_cast<int32_t>(lim));
+        }
+      }
+    }
+    const int32_t cnt = static_cast<int32_t>(s->entries.size() / 4) - off;
+    if (cnt > 0) items.push_back({static_cast<int32_t>(r0), off, cnt, 0});
+  }
+  // global rows: every key that causality permits
+  const int64_t ng = static_cast<int64_t>(p->gpos.size());
+  for (int64_t q0 = 0; q0 < ng; q0 += group_rows) {
+    const int32_t off = static_cast<int32_t>(s->entries.size() / 4);
+    const int64_t last = p->gpos[std::min<int64_t>(q0 + group_rows, ng) - 1];
+    const int64_t kb_hi = (p->causal ? last : T - 1) / kTile;
+    for (int64_t kb = 0; kb <= kb_hi; ++kb) {
+      const int64_t k0 = kb * kTile, k1 = std::min<int64_t>(k0 + kTile, T) - 1;
+      const bool ragged = k0 + kTile > T;
+      int32_t flags = kKindDense << kKindShift;
+      for (int t = 0; t < n_qtiles; ++t) {
+        const int64_t a = q0 + int64_t(t) * qtile_rows;
+        if (a >= ng) continue;
+        const int64_t b = std::min<int64_t>(a + qtile_rows, ng) - 1;
+        const int64_t rmin = p->gpos[a], rmax = p->gpos[b];
+        if (p->causal && k0 > rmax) continue;
+        flags |= kActive0 << t;
+        if (!ragged && (!p->causal || k1 <= rmin)) flags |= kFull0 << t;
+      }
+      if (flags & (kActive0 | kActive1)) push(static_cast<int32_t>(k0), flags, static_cast<int32_t>(kb), 0);
+    }
+    const int32_t cnt = static_cast<int32_t>(s->entries.size() / 4) - off;
+    if (cnt > 0) items.push_back({static_cast<int32_t>(q0), off, cnt, kItemGathered});
+  }
+  if (longest_first)
+    std::stable_sort(items.begin(), items.end(),
+                     [](const Item& x, const Item& y) { return x.cnt > y.cnt; });
+  for (const Item& it : items) s->items.insert(s->items.end(), {it.q0, it.off, it.cnt, it.flags});
+}
+
+spattn_status upload_schedule(spattn::Schedule* s) {
+  const size_t ni = s->items.size() / 4, ne = s->entries.size() / 4;
+  CUDA_TRY(dev_alloc(&s->d_items, ni));
+  CUDA_TRY(dev_alloc(&s->d_entries, ne));
+  if (ni) CUDA_TRY(cudaMemcpy(s->d_items, s->items.data(), ni * sizeof(int4), cudaMemcpyHostToDevice));
+  if (ne)
+    CUDA_TRY(cudaMemcpy(s->d_entries, s->entries.data(), ne * sizeof(int4), cudaMemcpyHostToDevice));
+  return SPATTN_OK;
+}
+
+spattn_status check_ptr(const void* p, const char* name) {
+  if (!p) return fail(SPATTN_ERR_NULL, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+    return fail(SPATTN_ERR_ALIGN, "%s is not 16-byte aligned", name);
+  return SPATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spattn_last_error(void) { return g_last_error.c_str(); }
+
+const char* spattn_version(void) { return "spattn 0.1 (sm_103a tcgen05)"; }
+
+spattn_status spattn_mask_validate(const spattn_mask_spec* spec, int64_t T) {
+  if (!spec) return fail(SPATTN_ERR_NULL, "spec is NULL");
+  if (T < 1 || T > kMaxT) return fail(SPATTN_ERR_SHAPE, "T=%lld outside [1, 2^30]", (long long)T);
+  if (spec->causal != 0 && spec->causal != 1)
+    return fail(SPATTN_ERR_INVALID_SPEC, "causal must be 0 or 1");
+  if (spec->causal) {
+    if (spec->window < 0) return fail(SPATTN_ERR_INVALID_SPEC, "window must be >= 0");
+    if (spec->radius != -1) return fail(SPATTN_ERR_INVALID_SPEC, "causal mask takes radius = -1");
+  } else {
+    if (spec->radius < -1) return fail(SPATTN_ERR_INVALID_SPEC, "radius must be >= -1");
+    if (spec->window != 0) return fail(SPATTN_ERR_INVALID_SPEC, "bidirectional mask takes window = 0");
+  }
+  if (spec->stride < 0) return fail(SPATTN_ERR_INVALID_SPEC, "stride must be >= 0");
+  if (spec->stride == 0 && spec->stride_offset != 0)
+    return fail(SPATTN_ERR_INVALID_SPEC, "stride_offset must be 0 without a stride");
+  if (spec->stride > 0 && (spec->stride_offset < 0 || spec->stride_offset >= spec->stride))
+    return fail(SPATTN_ERR_INVALID_SPEC, "stride_offset must lie in [0, stride)");
+  if (spec->n_global < 0 || spec->n_global > T)
+    return fail(SPATTN_ERR_INVALID_SPEC, "n_global must lie in [0, T]");
+  if (spec->n_global > 0) {
+    if (!spec->global_pos) return fail(SPATTN_ERR_NULL, "global_pos is NULL");
+    std::vector<int32_t> g(spec->global_pos, spec->global_pos + spec->n_global);
+    for (int32_t x : g)
+      if (x < 0 || x >= T) return fail(SPATTN_ERR_INVALID_SPEC, "global position %d outside [0, T)", x);
+    std::sort(g.begin(), g.end());
+    for (size_t a = 1; a < g.size(); ++a)
+      if (g[a] == g[a - 1]) return fail(SPATTN_ERR_INVALID_SPEC, "duplicate global position %d", g[a]);
+  }
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_t head_dim,
+                                 void* cuda_stream, spattn_plan** out) {
+  if (!out) return fail(SPATTN_ERR_NULL, "out is NULL");
+  *out = nullptr;
+  spattn_status st = spattn_mask_validate(spec, T);
+  if (st != SPATTN_OK) return st;
+  if (head_dim != 64 && head_dim != 128)
+    return fail(SPATTN_ERR_SHAPE, "head_dim %d not supported (64 or 128)", head_dim);
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+
+  spattn_plan* p = new spattn_plan();
+  auto bail = [&](spattn_status s) {
+    free_plan_memory(p);
+    delete p;
+    return s;
+  };
+  // normalise: widths beyond T describe the same set as T
+  p->T = T;
+  p->d = head_dim;
+  p->causal = spec->causal;
+  p->window = std::min<int64_t>(spec->window, T);
+  p->radius = spec->radius < 0 ? -1 : std::min<int64_t>(spec->radius, T);
+  p->stride = spec->stride;
+  p->offset = spec->stride_offset;
+  if (p->stride > T) {  // at most one strided column, j == offset
+    if (p->offset < T) p->stride = T; else { p->stride = 0; p->offset = 0; }
+  }
+  p->gpos.assign(spec->global_pos, spec->global_pos + spec->n_global);
+  std::sort(p->gpos.begin(), p->gpos.end());
+  for (int32_t x : p->gpos)
+    if (!(p->stride > 0 && x % p->stride == p->offset)) p->gpos_ns.push_back(x);
+  if (cudaGetDevice(&p->device) != cudaSuccess)
+    return bail(fail(SPATTN_ERR_CUDA, "no CUDA device"));
+
+  p->nqb = static_cast<int32_t>((T + kTile - 1) / kTile);
+  p->nkb = p->nqb;
+  const int32_t Ti = static_cast<int32_t>(T);
+  uint8_t* d_flags = nullptr;
+  int32_t* d_ncols = nullptr;
+  int32_t *d_qne = nullptr, *d_qfull = nullptr, *d_qoff = nullptr;
+  long long* d_qpairs = nullptr;
+  auto cleanup_tmp = [&] {
+    cudaFree(d_flags);
+    cudaFree(d_ncols);
+    cudaFree(d_qne);
+    cudaFree(d_qfull);
+    cudaFree(d_qoff);
+    cudaFree(d_qpairs);
+  };
+#define PLAN_TRY(expr)                                                                 \
+  do {                                                                                 \
+    cudaError_t e_ = (expr);                                                           \
+    if (e_ != cudaSuccess) {                                                           \
+      cleanup_tmp();                                                                   \
+      return bail(fail(SPATTN_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_))); \
+    }                                                                                  \
+  } while (0)
+
+  PLAN_TRY(dev_alloc(&p->d_gpos, p->gpos.size()));
+  PLAN_TRY(dev_alloc(&p->d_gpos_ns, p->gpos_ns.size()));
+  if (!p->gpos.empty())
+    PLAN_TRY(cudaMemcpy(p->d_gpos, p->gpos.data(), p->gpos.size() * 4, cudaMemcpyHostToDevice));
+  if (!p->gpos_ns.empty())
+    PLAN_TRY(cudaMemcpy(p->d_gpos_ns, p->gpos_ns.data(), p->gpos_ns.size() * 4, cudaMemcpyHostToDevice));
+  PLAN_TRY(dev_alloc(&p->d_rowglobal, T));
+  PLAN_TRY(dev_alloc(&p->d_colmask, size_t(p->nkb) * 4));
+  PLAN_TRY(dev_alloc(&p->d_cols, T));
+  PLAN_TRY(dev_alloc(&d_flags, T));
+  PLAN_TRY(dev_alloc(&d_ncols, 1));
+  PLAN_TRY(dev_alloc(&p->d_walk, 1));
+  PLAN_TRY(dev_alloc(&p->d_err, 1));
+  PLAN_TRY(cudaMemsetAsync(p->d_walk, 0, sizeof(unsigned long long), stream));
+  PLAN_TRY(cudaMemsetAsync(p->d_err, 0, sizeof(int), stream));
+  const spattn::MaskDev m = p->mask_dev();
+
+  // sparse columns: flags -> compacted list -> per-key-block bit masks
+  PLAN_TRY(spattn::launch_column_flags(m, d_flags, p->d_rowglobal, stream));
+  PLAN_TRY(spattn::launch_compact_columns(d_flags, Ti, p->d_cols, d_ncols, stream));
+  PLAN_TRY(spattn::launch_colmask(d_flags, Ti, p->nkb, p->d_colmask, stream));
+  int32_t ncols = 0;
+  PLAN_TRY(cudaMemcpyAsync(&ncols, d_ncols, 4, cudaMemcpyDeviceToHost, stream));
+  PLAN_TRY(cudaStreamSynchronize(stream));
+  p->n_cols = ncols;
+  p->cols.resize(ncols);
+  if (ncols) PLAN_TRY(cudaMemcpy(p->cols.data(), p->d_cols, size_t(ncols) * 4, cudaMemcpyDeviceToHost));
+
+  // natural-grid classification: count pass, offsets, fill pass
+  PLAN_TRY(dev_alloc(&d_qne, p->nqb));
+  PLAN_TRY(dev_alloc(&d_qfull, p->nqb));
+  PLAN_TRY(dev_alloc(&d_qoff, p->nqb));
+  PLAN_TRY(dev_alloc(&d_qpairs, p->nqb));
+  PLAN_TRY(spattn::launch_tile_count(m, p->d_colmask, p->nqb, p->nkb, d_qne, d_qfull, d_qpairs, stream));
+  std::vector<int32_t> qne(p->nqb), qfull(p->nqb), qoff(p->nqb);
+  std::vector<long long> qpairs(p->nqb);
+  PLAN_TRY(cudaMemcpyAsync(qne.data(), d_qne, size_t(p->nqb) * 4, cudaMemcpyDeviceToHost, stream));
+  PLAN_TRY(cudaMemcpyAsync(qfull.data(), d_qfull, size_t(p->nqb) * 4, cudaMemcpyDeviceToHost, stream));
+  PLAN_TRY(cudaMemcpyAsync(qpairs.data(), d_qpairs, size_t(p->nqb) * 8, cudaMemcpyDeviceToHost, stream));
+  PLAN_TRY(cudaStreamSynchronize(stream));
+  int64_t total = 0;
+  for (int32_t q = 0; q < p->nqb; ++q) {
+    qoff[q] = static_cast<int32_t>(total);
+    total += qne[q];
+    p->n_full += qfull[q];
+    p->pairs += qpairs[q];
+  }
+  p->n_nonempty = total;
+  p->n_partial = total - p->n_full;
+  p->n_empty = int64_t(p->nqb) * p->nkb - total;
+  PLAN_TRY(dev_alloc(&p->d_tile_qb, total));
+  PLAN_TRY(dev_alloc(&p->d_tile_kb, total));
+  PLAN_TRY(dev_alloc(&p->d_tile_cnt, total));
+  PLAN_TRY(dev_alloc(&p->d_tile_cls, total));
+  PLAN_TRY(cudaMemcpyAsync(d_qoff, qoff.data(), size_t(p->nqb) * 4, cudaMemcpyHostToDevice, stream));
+  PLAN_TRY(spattn::launch_tile_fill(m, p->d_colmask, p->nqb, p->nkb, d_qoff, p->d_tile_qb,
+                                    p->d_tile_kb, p->d_tile_cnt, p->d_tile_cls, stream));
+  PLAN_TRY(cudaStreamSynchronize(stream));
+  cleanup_tmp();
+#undef PLAN_TRY
+
+  // execution schedules
+  build_schedule(p, &p->sched[0], 2 * kTile, kTile, 2, true);
+  build_schedule(p, &p->sched[1], 64, 64, 1, true);
+  for (auto& s : p->sched) {
+    spattn_status us = upload_schedule(&s);
+    if (us != SPATTN_OK) return bail(us);
+  }
+  *out = p;
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_info(const spattn_plan* p, int64_t* pairs, int64_t* n_full,
+                               int64_t* n_partial, int64_t* n_empty, int32_t* bm, int32_t* bn) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  if (pairs) *pairs = p->pairs;
+  if (n_full) *n_full = p->n_full;
+  if (n_partial) *n_partial = p->n_partial;
+  if (n_empty) *n_empty = p->n_empty;
+  if (bm) *bm = kTile;
+  if (bn) *bn = kTile;
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_copy_tiles(const spattn_plan* p, int32_t* qb, int32_t* kb, int32_t* cnt,
+                                     uint8_t* cls, int64_t cap, int64_t* n) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  if (n) *n = p->n_nonempty;
+  const int64_t k = std::min(cap, p->n_nonempty);
+  if (k > 0) {
+    if (qb) CUDA_TRY(cudaMemcpy(qb, p->d_tile_qb, size_t(k) * 4, cudaMemcpyDeviceToHost));
+    if (kb) CUDA_TRY(cudaMemcpy(kb, p->d_tile_kb, size_t(k) * 4, cudaMemcpyDeviceToHost));
+    if (cnt) CUDA_TRY(cudaMemcpy(cnt, p->d_tile_cnt, size_t(k) * 4, cudaMemcpyDeviceToHost));
+    if (cls) CUDA_TRY(cudaMemcpy(cls, p->d_tile_cls, size_t(k), cudaMemcpyDeviceToHost));
+  }
+  if (cap < p->n_nonempty) return fail(SPATTN_ERR_SHAPE, "capacity %lld < %lld tiles", (long long)cap,
+                                       (long long)p->n_nonempty);
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_copy_columns(const spattn_plan* p, int32_t* cols, int64_t cap, int64_t* n) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  if (n) *n = p->n_cols;
+  const int64_t k = std::min<int64_t>(cap, p->n_cols);
+  if (cols && k > 0) std::memcpy(cols, p->cols.data(), size_t(k) * 4);
+  if (cap < p->n_cols) return fail(SPATTN_ERR_SHAPE, "capacity %lld < %d columns", (long long)cap, p->n_cols);
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_copy_schedule(const spattn_plan* p, int32_t which, int32_t* items,
+                                        int64_t item_cap, int64_t* n_items, int32_t* entries,
+                                        int64_t entry_cap, int64_t* n_entries,
+                                        int64_t* tile_products) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  if (which != 0 && which != 1) return fail(SPATTN_ERR_SHAPE, "which must be 0 or 1");
+  const spattn::Schedule& s = p->sched[which];
+  const int64_t ni = s.items.size() / 4, ne = s.entries.size() / 4;
+  if (n_items) *n_items = ni;
+  if (n_entries) *n_entries = ne;
+  if (tile_products) *tile_products = s.tile_products;
+  if ((items && item_cap < ni) || (entries && entry_cap < ne))
+    return fail(SPATTN_ERR_SHAPE, "schedule arrays too small");
+  if (items && ni) std::memcpy(items, s.items.data(), size_t(ni) * 16);
+  if (entries && ne) std::memcpy(entries, s.entries.data(), size_t(ne) * 16);
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_set_walk_counter(spattn_plan* p, int32_t enable) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  p->walk_enabled = enable ? 1 : 0;
+  CUDA_TRY(cudaMemset(p->d_walk, 0, sizeof(unsigned long long)));
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_walk_count(const spattn_plan* p, int64_t* count) {
+  if (!p || !count) return fail(SPATTN_ERR_NULL, "plan or count is NULL");
+  CUDA_TRY(cudaDeviceSynchronize());
+  unsigned long long v = 0;
+  CUDA_TRY(cudaMemcpy(&v, p->d_walk, sizeof v, cudaMemcpyDeviceToHost));
+  *count = static_cast<int64_t>(v);
+  return SPATTN_OK;
+}
+
+spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dtype dtype,
+                         const void* Q, const void* K, const void* V, float scale, void* O,
+                         float* LSE, void* cuda_stream) {
+  if (!cp) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  spattn_plan* p = const_cast<spattn_plan*>(cp);  // owns mutable scratch
+  spattn_status st;
+  if ((st = check_ptr(Q, "Q")) || (st = check_ptr(K, "K")) || (st = check_ptr(V, "V")) ||
+      (st = check_ptr(O, "O")))
+    return st;
+  if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4) return fail(SPATTN_ERR_ALIGN, "LSE misaligned");
+  if (B < 1 || H < 1) return fail(SPATTN_ERR_SHAPE, "B and H must be >= 1");
+  const int64_t BH = int64_t(B) * H;
+  if (BH > 65535) return fail(SPATTN_ERR_SHAPE, "B*H = %lld exceeds 65535", (long long)BH);
+  if (dtype != SPATTN_BF16 && dtype != SPATTN_FP32) return fail(SPATTN_ERR_DTYPE, "unknown dtype");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(SPATTN_ERR_INVALID_SPEC, "scale must be positive and finite");
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const int esize = dtype == SPATTN_BF16 ? 2 : 4;
+  const int64_t ng = static_cast<int64_t>(p->gpos.size());
+  const size_t row_bytes = size_t(p->d) * esize;
+  const size_t kc_bytes = size_t(BH) * p->n_cols * row_bytes;
+  const size_t qg_bytes = size_t(BH) * ng * row_bytes;
+  const size_t need = 2 * kc_bytes + qg_bytes;
+  if (need > p->scratch_bytes) {
+    if (p->d_scratch) {
+      CUDA_TRY(cudaStreamSynchronize(stream));
+      CUDA_TRY(cudaFree(p->d_scratch));
+      p->d_scratch = nullptr;
+      p->scratch_bytes = 0;
+    }
+    CUDA_TRY(cudaMalloc(&p->d_scratch, need));
+    p->scratch_bytes = need;
+  }
+  uint8_t* base = static_cast<uint8_t*>(p->d_scratch);
+  void* Kc = need ? base : nullptr;
+  void* Vc = need ? base + kc_bytes : nullptr;
+  void* Qg = need ? base + 2 * kc_bytes : nullptr;
+  if (need)
+    CUDA_TRY(spattn::launch_pack(Q, K, V, Kc, Vc, Qg, p->d_cols, p->n_cols, p->d_gpos,
+                                 static_cast<int32_t>(ng), BH, p->T, static_cast<int32_t>(row_bytes),
+                                 stream));
+  spattn::TcArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.Kc = Kc ? Kc : K;
+  a.Vc = Vc ? Vc : V;
+  a.Qg = Qg ? Qg : Q;
+  a.O = O;
+  a.LSE = LSE;
+  a.BH = static_cast<int32_t>(BH);
+  a.n_cols = p->n_cols;
+  a.scale = scale;
+  a.colmask = p->d_colmask;
+  a.mask = p->mask_dev();
+  a.walk = p->walk_enabled ? p->d_walk : nullptr;
+  a.err = p->d_err;
+  a.wait_budget_ns = p->wait_budget_ns;
+  const spattn::Schedule& s = p->sched[dtype == SPATTN_BF16 ? 0 : 1];
+  a.items = s.d_items;
+  a.entries = s.d_entries;
+  a.n_items = static_cast<int32_t>(s.items.size() / 4);
+  if (dtype == SPATTN_BF16) {
+    const char* why = "";
+    cudaError_t e = spattn::launch_fwd_tc(p->d, a, stream, &why);
+    if (e != cudaSuccess)
+      return fail(SPATTN_ERR_CUDA, "tensor-core forward launch: %s (%s)", cudaGetErrorString(e), why);
+  } else {
+    cudaError_t e = spattn::launch_fwd_simt(p->d, a, stream);
+    if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "fp32 forward launch: %s", cudaGetErrorString(e));
+  }
+  return SPATTN_OK;
+}
+
+spattn_status spattn_fwd_host(const spattn_plan* p, int32_t B, int32_t H, spattn_dtype dtype,
+                              const void* Qh, const void* Kh, const void* Vh, float scale, void* Oh,
+                              float* LSEh, void* Qd, void* Kd, void* Vd, void* Od, float* LSEd,
+                              void* cuda_stream) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  if (!Qh || !Kh || !Vh || !Oh) return fail(SPATTN_ERR_NULL, "a host buffer is NULL");
+  if ((LSEh == nullptr) != (LSEd == nullptr))
+    return fail(SPATTN_ERR_NULL, "LSE_host and LSE_dev must both be set or both be NULL");
+  if (B < 1 || H < 1) return fail(SPATTN_ERR_SHAPE, "B and H must be >= 1");
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const size_t esize = dtype == SPATTN_BF16 ? 2 : 4;
+  const size_t rows = size_t(B) * H * p->T;
+  const size_t bytes = rows * p->d * esize;
+  spattn_status st;
+  if ((st = check_ptr(Qd, "Q_dev")) || (st = check_ptr(Kd, "K_dev")) || (st = check_ptr(Vd, "V_dev")) ||
+      (st = check_ptr(Od, "O_dev")))
+    return st;
+  CUDA_TRY(cudaMemcpyAsync(Qd, Qh, bytes, cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemcpyAsync(Kd, Kh, bytes, cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemcpyAsync(Vd, Vh, bytes, cudaMemcpyHostToDevice, stream));
+  st = spattn_fwd(p, B, H, dtype, Qd, Kd, Vd, scale, Od, LSEd, cuda_stream);
+  if (st != SPATTN_OK) return st;
+  CUDA_TRY(cudaMemcpyAsync(Oh, Od, bytes, cudaMemcpyDeviceToHost, stream));
+  if (LSEh) CUDA_TRY(cudaMemcpyAsync(LSEh, LSEd, rows * 4, cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_check_device(const spattn_plan* p, void* cuda_stream) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
+  int e = 0;
+  CUDA_TRY(cudaMemcpy(&e, p->d_err, sizeof e, cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(p->d_err, 0, sizeof(int)));
+  if (e & spattn::kErrTimeout)
+    return fail(SPATTN_ERR_TIMEOUT, "a device-side wait ran out of its time budget");
+  return SPATTN_OK;
+}
+
+void spattn_plan_destroy(spattn_plan* p) {
+  if (!p) return;
+  cudaDeviceSynchronize();
+  free_plan_memory(p);
+  delete p;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI on
+seeded inputs and compare with the fp64 oracle on the same (bf16-rounded) values.
+
+Tolerances (from the workload statement, checked element by element):
+  * bf16 inputs, fp32 accumulation: max |O - O_ref| <= 1e-2 and
+    ||O - O_ref||_2 / ||O_ref||_2 <= 5e-3;
+  * fp32 inputs: max |O - O_ref| <= 1e-5;
+  * LSE (fp32 in both paths; not named by the statement): the logits, their
+    maximum and the fp32 sum of exponentials carry relative error ~1e-6, so
+    |LSE - LSE_ref| <= 1e-4 (fp32 inputs: 1e-5) leaves a wide margin.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import spattn_workloads as W
+import sparse_masked_attention_plan_b300 as sp
+
+TOL = {"bf16": dict(max_abs=1e-2, rel_l2=5e-3, lse=1e-4),
+       "fp32": dict(max_abs=1e-5, rel_l2=None, lse=1e-5)}
+
+
+def torch_dtype(name):
+    return torch.bfloat16 if name == "bf16" else torch.float32
+
+
+def host_view(t):
+    """Oracle input view of a CPU tensor: fp32 values, or bf16 bit patterns."""
+    if t.dtype == torch.bfloat16:
+        return oracle.bf16_bits(t)
+    return t.contiguous().numpy()
+
+
+def edge_rows(T, mask, tile=128):
+    """Rows where the mask or the tiling changes: ends, window edges, block edges,
+    global rows and their neighbours."""
+    w = mask.get("window", 0)
+    r = mask.get("radius", -1)
+    rows = {0, 1, 2, T - 1, T - 2, T // 2}
+    for x in (w - 1, w, w + 1, r, r + 1, 2 * r):
+        rows.add(x)
+    for b in range(0, T, tile * 16):
+        rows.update({b - 1, b, b + 1})
+    for k in (1, 2, 3, 255, 256, 257):
+        rows.add(tile * k - 1)
+        rows.add(tile * k)
+    for g in np.asarray(mask.get("global_pos", ()))[:64]:
+        rows.update({int(g) - 1, int(g), int(g) + 1})
+    s = mask.get("stride", 0)
+    if s:
+        rows.update({s - 1, s, s + 1, 3 * s})
+    return sorted(x for x in rows if 0 <= x < T)
+
+
+def run_and_compare(B, H, T, d, mask, dtype="bf16", seed=0, heads=None, rows=None,
+                    scale=None, plan=None):
+    """Run spattn_fwd on seeded [B,H,T,d] inputs; compare the chosen heads/rows with
+    the oracle.  Returns a dict of the observed errors; asserts the tolerances."""
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    Q, K, V = W.qkv(B, H, T, d, seed, torch_dtype(dtype))
+    if plan is None:
+        plan = sp.Plan(T, d, **mask)
+    q, k, v = (x.cuda() for x in (Q, K, V))
+    o, lse = sp.fwd(plan, q, k, v, scale)
+    torch.cuda.synchronize()
+    plan.check_device()
+    O = o.float().cpu().numpy()
+    L = lse.cpu().numpy()
+    m = oracle.Mask(T, mask.get("causal", 1), mask.get("window", 0), mask.get("radius", -1),
+                    mask.get("stride", 0), mask.get("offset", 0), mask.get("global_pos", ()))
+    heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
+    tol = TOL[dtype]
+    worst = dict(max_abs=0.0, rel_l2=0.0, lse=0.0)
+    for (b, h) in heads:
+        rr = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+        Oref, Lref = oracle.attention(m, host_view(Q[b, h]), host_view(K[b, h]),
+                                      host_view(V[b, h]), scale, rr)
+        got = O[b, h][rr].astype(np.float64)
+        assert np.all(np.isfinite(got)), f"non-finite output in head {(b, h)}"
+        err = np.abs(got - Oref)
+        max_abs = float(err.max()) if err.size else 0.0
+        rel = float(np.linalg.norm(got - Oref) / max(np.linalg.norm(Oref), 1e-30))
+        lerr = float(np.abs(L[b, h][rr].astype(np.float64) - Lref).max()) if rr.size else 0.0
+        worst["max_abs"] = max(worst["max_abs"], max_abs)
+        worst["rel_l2"] = max(worst["rel_l2"], rel)
+        worst["lse"] = max(worst["lse"], lerr)
+        where = int(np.unravel_index(np.argmax(err), err.shape)[0]) if err.size else -1
+        assert max_abs <= tol["max_abs"], (
+            f"head {(b, h)}: max-abs {max_abs:.3g} at row {rr[where] if where >= 0 else -1}")
+        if tol["rel_l2"] is not None:
+            assert rel <= tol["rel_l2"], f"head {(b, h)}: rel-L2 {rel:.3g}"
+        assert lerr <= tol["lse"], f"head {(b, h)}: LSE error {lerr:.3g}"
+    return worst
+
+
+def workload(name):
+    cfg = W.WORKLOADS[name]
+    return cfg, W.mask_params(name)

@@ -1,0 +1,110 @@
+"""Forward parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element.  Small cases compare every row of every
+head; the full-size workloads compare sampled rows (edges, window and block
+boundaries, global rows) of a few heads, in the launch configuration the
+benchmark times."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import spattn_workloads as W
+import sparse_masked_attention_plan_b300 as sp
+from gpu_cases import edge_rows, run_and_compare, workload
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["t512_w128_s0", "t512_w128_s64", "t512_full_causal"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workloads_every_row(oracle_mod, name, dtype):
+    cfg, p = workload(name)
+    run_and_compare(cfg["B"], cfg["H"], cfg["T"], cfg["d"], p, dtype, seed=0)
+
+
+SWEEP = [
+    # (B, H, T, d, mask)
+    (1, 2, 1, 64, dict(causal=1, window=0)),
+    (1, 1, 37, 128, dict(causal=1, window=5)),
+    (2, 3, 128, 64, dict(causal=1, window=1)),
+    (1, 2, 129, 128, dict(causal=0, radius=0)),
+    (1, 2, 300, 64, dict(causal=1, window=300)),
+    (1, 2, 300, 128, dict(causal=1, window=77, stride=3, offset=2)),
+    (2, 1, 513, 64, dict(causal=0, radius=40, stride=64, offset=63, global_pos=[0, 77, 512])),
+    (1, 2, 777, 128, dict(causal=1, window=130, stride=17, offset=5,
+                          global_pos=[0, 3, 129, 500, 776])),
+    (1, 2, 1000, 64, dict(causal=0, radius=-1, global_pos=[999])),
+    (1, 1, 1000, 128, dict(causal=0, radius=128, stride=16, offset=0,
+                           global_pos=list(range(0, 1000, 97)))),
+    (1, 2, 1100, 64, dict(causal=1, window=0, stride=64)),
+    (1, 1, 1300, 128, dict(causal=0, radius=300, global_pos=list(range(5, 1300, 4)))),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("k", range(len(SWEEP)))
+def test_sweep_every_row(oracle_mod, k, dtype):
+    B, H, T, d, mask = SWEEP[k]
+    run_and_compare(B, H, T, d, mask, dtype, seed=k + 1)
+
+
+@pytest.mark.parametrize("name", ["t2048_w256_s0", "t2048_w256_s64"])
+def test_t2048_workloads(oracle_mod, name):
+    cfg, p = workload(name)
+    run_and_compare(cfg["B"], cfg["H"], cfg["T"], cfg["d"], p, "bf16", seed=1,
+                    heads=[(0, 0), (1, 5), (3, 11)])
+
+
+@pytest.mark.parametrize("name", ["t32k_w4096", "t16k_r256_s16_g128", "t8k_full_causal",
+                                  "t128k_w4096_s1024"])
+def test_large_workloads_sampled_rows(oracle_mod, name):
+    cfg, p = workload(name)
+    T = cfg["T"]
+    rows = W.sample_rows(T, 192, seed=3, must=edge_rows(T, p))
+    heads = [(0, 0), (cfg["B"] - 1, cfg["H"] - 1)]
+    run_and_compare(cfg["B"], cfg["H"], T, cfg["d"], p, "bf16", seed=2, heads=heads,
+                    rows=rows)
+
+
+def test_scale_and_repeat_calls_are_stable(oracle_mod):
+    cfg, p = workload("t512_w128_s64")
+    plan = sp.Plan(cfg["T"], cfg["d"], **p)
+    for scale in (0.05, 1.0 / math.sqrt(cfg["d"]), 0.9):
+        run_and_compare(cfg["B"], cfg["H"], cfg["T"], cfg["d"], p, "bf16", seed=9, scale=scale,
+                        plan=plan)
+
+
+def test_bad_arguments_are_rejected():
+    plan = sp.Plan(256, 64, causal=1, window=16)
+    q = torch.zeros(1, 1, 256, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(sp.SpattnError) as ei:
+        sp.fwd(plan, q, q, q, -1.0)
+    assert ei.value.status == sp.ERR_INVALID_SPEC
+    flat = torch.zeros(256 * 64 + 8, device="cuda", dtype=torch.bfloat16)
+    qm = flat[1:1 + 256 * 64].view(1, 1, 256, 64)  # 2 bytes off a 16-byte boundary
+    with pytest.raises(sp.SpattnError) as ei:
+        sp.fwd(plan, qm, qm, qm, 1.0)
+    assert ei.value.status == sp.ERR_ALIGN
+    with pytest.raises(sp.SpattnError) as ei:
+        sp.Plan(256, 96, causal=1, window=16)
+    assert ei.value.status == sp.ERR_SHAPE
+
+
+def test_host_buffer_entry_matches_device_entry(oracle_mod):
+    cfg, p = workload("t512_w128_s64")
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    Q, K, V = W.qkv(B, H, T, d, 4, torch.bfloat16)
+    plan = sp.Plan(T, d, **p)
+    o_dev, l_dev = sp.fwd(plan, Q.cuda(), K.cuda(), V.cuda(), 0.125)
+    hq, hk, hv = (x.pin_memory() for x in (Q, K, V))
+    ho = torch.empty_like(Q).pin_memory()
+    hl = torch.empty(B, H, T, dtype=torch.float32).pin_memory()
+    bufs = (torch.empty_like(Q, device="cuda"), torch.empty_like(K, device="cuda"),
+            torch.empty_like(V, device="cuda"), torch.empty_like(Q, device="cuda"),
+            torch.empty(B, H, T, dtype=torch.float32, device="cuda"))
+    sp.fwd_host(plan, hq, hk, hv, 0.125, ho, hl, bufs)
+    assert torch.equal(ho, o_dev.cpu())
+    assert torch.equal(hl, l_dev.cpu())

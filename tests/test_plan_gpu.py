@@ -1,0 +1,187 @@
+"""Plan builder on the GPU against the oracle: pair counts, the non-empty tile list
+(block, count, class) and the compacted column list must match bit for bit; the
+execution schedule must compute only non-empty tiles and cover every allowed pair
+exactly once."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import spattn_workloads as W
+import sparse_masked_attention_plan_b300 as sp
+from pins import small_specs
+
+pytestmark = pytest.mark.gpu
+
+EDGE_SPECS = [
+    dict(T=1, causal=1, window=0),
+    dict(T=1, causal=0, radius=0),
+    dict(T=300, causal=1, window=1),
+    dict(T=300, causal=1, window=300),
+    dict(T=300, causal=1, window=10_000),
+    dict(T=257, causal=0, radius=0),
+    dict(T=257, causal=0, radius=1000),
+    dict(T=500, causal=1, window=37, stride=1, offset=0),
+    dict(T=777, causal=1, window=130, stride=17, offset=5, global_pos=[0, 3, 129, 500, 776]),
+    dict(T=777, causal=0, radius=60, stride=128, offset=127, global_pos=[5, 6, 7, 640]),
+    dict(T=1000, causal=0, radius=-1, global_pos=[999]),
+    dict(T=1024, causal=1, window=0, stride=64, offset=0),
+    dict(T=600, causal=1, window=200, stride=1000, offset=3),
+    dict(T=600, causal=1, window=200, stride=1000, offset=700),
+]
+
+
+def oracle_mask(T, p):
+    return oracle.Mask(T, p.get("causal", 1), p.get("window", 0), p.get("radius", -1),
+                       p.get("stride", 0), p.get("offset", 0), p.get("global_pos", ()))
+
+
+def expected_columns(T, p):
+    """Strided U global columns, straight from the definition (numpy)."""
+    j = np.arange(T)
+    s = p.get("stride", 0)
+    sel = (j % s == p.get("offset", 0)) if s else np.zeros(T, bool)
+    g = np.asarray(p.get("global_pos", ()), dtype=np.int64)
+    sel[g] = True
+    return np.nonzero(sel)[0].astype(np.int32)
+
+
+def check_plan(T, p, d=64):
+    m = oracle_mask(T, p)
+    plan = sp.Plan(T, d, **{k: p[k] for k in p if k != "T"})
+    info = plan.info()
+    assert info["pairs_per_head"] == m.count_pairs()
+    qb, kb, cnt, cls, (nf, npart, ne) = oracle.tile_list(m, 128, 128)
+    gq, gk, gc, gcl = plan.tiles()
+    assert np.array_equal(gq, qb) and np.array_equal(gk, kb)
+    assert np.array_equal(gc, cnt)
+    assert np.array_equal(gcl, cls)
+    assert (info["n_full"], info["n_partial"], info["n_empty"]) == (nf, npart, ne)
+    assert np.array_equal(plan.columns(), expected_columns(T, p))
+    return plan, m
+
+
+@pytest.mark.parametrize("name", sorted(W.WORKLOADS))
+def test_workload_plan_matches_oracle(oracle_mod, name):
+    cfg = W.WORKLOADS[name]
+    p = W.mask_params(name)
+    plan, m = check_plan(cfg["T"], p, cfg["d"])
+    # the page-derived pair count of the 32K / W=4096 workload
+    if name == "t32k_w4096":
+        assert plan.info()["pairs_per_head"] == 125_831_168
+
+
+@pytest.mark.parametrize("k", range(len(EDGE_SPECS)))
+def test_edge_spec_plan_matches_oracle(oracle_mod, k):
+    e = dict(EDGE_SPECS[k])
+    T = e.pop("T")
+    check_plan(T, e)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_random_spec_plans_match_oracle(oracle_mod, seed):
+    for e in small_specs(seed, n=40):
+        e = dict(e)
+        T = e.pop("T")
+        check_plan(T, e)
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(12):  # longer sequences, several tiles, ragged tails
+        T = int(rng.integers(129, 1500))
+        causal = int(rng.integers(0, 2))
+        s = int(rng.choice([0, 1, 3, 17, 64, 200]))
+        e = dict(causal=causal, window=int(rng.choice([0, 1, 50, 129, 700])) if causal else 0,
+                 radius=-1 if causal else int(rng.choice([-1, 0, 20, 128, 400])),
+                 stride=s, offset=int(rng.integers(0, s)) if s else 0,
+                 global_pos=np.sort(rng.choice(T, int(rng.choice([0, 1, 9])), replace=False)))
+        check_plan(T, e)
+
+
+def covered_keys(plan_sched, cols, T, group_rows, qtile_rows, i, grow, p):
+    """Keys the schedule lets row i read: band tiles via the predicate rule of the
+    kernels' definition (local window U strided/global bits), packed chunks via C."""
+    items, ents, _ = plan_sched
+    keys = []
+    colset = set(cols.tolist())
+    causal = p.get("causal", 1)
+    for it in items:
+        q0, off, cnt, fl = it
+        if fl & 1:  # gathered global rows
+            rows = p["global_pos_sorted"][q0:q0 + group_rows]
+            if i not in rows:
+                continue
+            t = int(np.nonzero(rows == i)[0][0]) // qtile_rows
+        else:
+            if grow or not (q0 <= i < q0 + group_rows):
+                continue
+            t = (i - q0) // qtile_rows
+        for (src, f, kb, lim) in ents[off:off + cnt]:
+            if not (f & (1 << t)):
+                continue
+            kind = (f >> 4) & 3
+            full = bool(f & (4 << t))  # the kernels skip the predicate: the whole tile counts
+            if kind == 1:
+                keys += [int(c) for c in (cols[src:src + 128] if full else cols[src:lim])]
+                continue
+            for j in range(src, src + 128):
+                if full:
+                    ok = True
+                elif j >= T:
+                    ok = False
+                elif kind == 2:
+                    ok = (j <= i) if causal else True
+                elif causal:
+                    w = p.get("window", 0)
+                    ok = j <= i and ((w == 0 or i - j < w) or j in colset)
+                else:
+                    r = p.get("radius", -1)
+                    ok = (r < 0 or abs(i - j) <= r) or j in colset
+                if ok:
+                    keys.append(j)
+    return keys
+
+
+@pytest.mark.parametrize("k", range(len(EDGE_SPECS)))
+def test_schedule_covers_each_allowed_pair_once(oracle_mod, k):
+    e = dict(EDGE_SPECS[k])
+    T = e.pop("T")
+    plan, m = check_plan(T, e)
+    qb, kb, cnt, cls, _ = oracle.tile_list(m, 128, 128)
+    nonempty = set(zip(qb.tolist(), kb.tolist()))
+    cols = plan.columns()
+    gpos = np.sort(np.asarray(e.get("global_pos", ()), dtype=np.int64))
+    e["global_pos_sorted"] = gpos
+    for which, (group_rows, qtile_rows) in enumerate([(256, 128), (64, 64)]):
+        sched = plan.schedule(which)
+        items, ents, products = sched
+        # every computed band tile is a non-empty tile of the natural grid
+        n_products = 0
+        for (q0, off, cnt_, fl) in items:
+            for (src, f, kbi, lim) in ents[off:off + cnt_]:
+                for t in range(2):
+                    if not (f & (1 << t)):
+                        continue
+                    n_products += 1
+                    if ((f >> 4) & 3) == 0 and not (fl & 1):
+                        qbi = (q0 + t * qtile_rows) // 128
+                        assert (qbi, kbi) in nonempty, (which, q0, t, kbi)
+        assert n_products == products
+        for i in range(T):
+            grow = i in set(gpos.tolist())
+            got = sorted(covered_keys(sched, cols, T, group_rows, qtile_rows, i, grow, e))
+            assert got == m.row_set(i).tolist(), (which, i)
+
+
+def test_walk_counter_counts_scheduled_products(oracle_mod):
+    T, d = 1000, 64
+    p = dict(causal=1, window=130, stride=17, offset=5, global_pos=[3, 500])
+    plan = sp.Plan(T, d, **p)
+    plan.set_walk_counter(True)
+    B, H = 2, 3
+    q = torch.randn(B, H, T, d, device="cuda", dtype=torch.bfloat16)
+    sp.fwd(plan, q, q, q, 0.125)
+    _, _, products = plan.schedule(0)
+    assert plan.walk_count() == products * B * H
+    plan.set_walk_counter(True)
+    sp.fwd(plan, q.float(), q.float(), q.float(), 0.125)
+    _, _, products32 = plan.schedule(1)
+    assert plan.walk_count() == products32 * B * H
