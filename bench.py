@@ -160,12 +160,17 @@ def oracle_sample_rate(cfg, p, Q, K, V, budget_s: float, seed: int = 0):
                     p["global_pos"])
     q, k, v = (oracle.bf16_bits(x[0, 0]) for x in (Q, K, V))
     scale = 1.0 / math.sqrt(d)
-    # calibrate on a few rows, then size the sample to the budget
-    rows = W.sample_rows(T, 32, seed)
-    t0 = time.perf_counter()
-    oracle.attention(m, q, k, v, scale, rows)
-    dt = max(time.perf_counter() - t0, 1e-3)
-    n = int(min(T, max(32, 32 * budget_s / dt)))
+    # calibrate on growing row counts, then size the sample to the budget
+    n, dt = 32, 0.0
+    while n < T:
+        rows = W.sample_rows(T, n, seed)
+        t0 = time.perf_counter()
+        oracle.attention(m, q, k, v, scale, rows)
+        dt = time.perf_counter() - t0
+        if dt > 0.25 * budget_s / 8 or dt > 0.5:
+            break
+        n *= 4
+    n = int(min(T, max(32, n * budget_s / max(dt, 1e-3))))
     rows = W.sample_rows(T, n, seed + 1)
     pairs = sum(len(m.row_set(int(r))) for r in rows)
     t0 = time.perf_counter()
@@ -354,10 +359,14 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override H (smaller profiling captures; the line then names it)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    cfg = W.WORKLOADS[args.workload]
+    cfg = dict(W.WORKLOADS[args.workload])
+    if args.heads:
+        cfg["H"] = args.heads
     p = W.mask_params(args.workload)
     if args.impl == "reference":
         return run_reference(args, cfg, p)

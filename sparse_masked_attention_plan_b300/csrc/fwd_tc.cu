@@ -295,21 +295,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
       tc_fence_after();
-      // pass 1: row maximum of the allowed logits (S stays in TMEM)
-      const bool full = (e.y & (kFull0 << wg)) != 0;
-      RowPredicate pr;
-      if (!full) pr = make_predicate(m, p.colmask, e, i);
-      float mx = -INFINITY;
+      // the whole S row of this thread (one TMEM load), masked where not allowed
+      uint32_t sr[kTile];
+      tmem_ld128(lane_base + colS, sr);
+      if (!(e.y & (kFull0 << wg))) {
+        uint32_t w[4];
+        row_mask(make_predicate(m, p.colmask, e, i), w);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + colS + 32 * q, v);
-#pragma unroll
-        for (int b = 0; b < 32; ++b) {
-          const float x = __uint_as_float(v[b]);
-          mx = (full || pred_allowed(pr, 32 * q + b)) ? fmaxf(mx, x) : mx;
-        }
+        for (int c = 0; c < kTile; ++c)
+          if (!((w[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
       }
+      float mx8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = __uint_as_float(sr[j]);
+#pragma unroll
+      for (int c = 8; c < kTile; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mcand = fmaxf(mrow, mx * c2);
       const bool need = mcand > mrow + kRescaleThreshold;
       float corr = 1.f;
@@ -319,28 +321,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         lrow *= corr;
       }
       const float msub = (mrow == -INFINITY) ? 0.f : mrow;
-      // pass 2: P = 2^(s * scale * log2 e - m), stored as bf16 over the first half of S
-      float sum = 0.f;
+      // P = 2^(s * scale * log2 e - m), stored as bf16 over the first half of S
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + colS + 32 * q, v);
         uint32_t pk[16];
 #pragma unroll
         for (int b = 0; b < 16; ++b) {
           const int c0 = 32 * q + 2 * b;
-          float x0 = fmaf(__uint_as_float(v[2 * b]), c2, -msub);
-          float x1 = fmaf(__uint_as_float(v[2 * b + 1]), c2, -msub);
-          if (!full) {
-            x0 = pred_allowed(pr, c0) ? x0 : -INFINITY;
-            x1 = pred_allowed(pr, c0 + 1) ? x1 : -INFINITY;
-          }
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          sum += p0 + p1;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c0]), c2, -msub));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c0 + 1]), c2, -msub));
+          sum4[b & 3] += p0 + p1;
           pk[b] = pack_bf16x2(p0, p1);
         }
         tmem_st16(lane_base + colS + 16 * q, pk);
       }
+      const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       lrow += sum;
       if (n_done > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -463,7 +459,7 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
   kp.entries = a.entries;
   kp.walk = a.walk;
   kp.err = a.err;
-  kp.budget = a.wait_budget_ns;
+  kp.budget = a.wait_budget_cycles;
   dim3 grid(a.n_items, a.BH);
   fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(mQ, mK, mV, mQg, mKc, mVc, kp);
   return cudaGetLastError();

@@ -80,7 +80,7 @@ struct spattn_plan {
   unsigned long long* d_walk = nullptr;
   int32_t walk_enabled = 0;
   int* d_err = nullptr;
-  uint64_t wait_budget_ns = 4000000000ull;
+  uint64_t wait_budget_cycles = 8000000000ull;  // ~4 s at the maximum SM clock
 
   spattn::MaskDev mask_dev() const {
     spattn::MaskDev m;
@@ -143,7 +143,7 @@ struct TcArgs {
   int32_t n_items;
   unsigned long long* walk;
   int* err;
-  uint64_t wait_budget_ns;
+  uint64_t wait_budget_cycles;
 };
 cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why);
 

@@ -66,6 +66,22 @@ __device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const u
   return p;
 }
 
+// Bits b of a 32-bit word with lo <= base + b <= hi.
+__device__ __forceinline__ uint32_t span_bits(int lo, int hi, int base) {
+  int a = lo - base, b = hi - base;
+  if (b < 0 || a > 31 || b < a) return 0u;
+  a = max(a, 0);
+  b = min(b, 31);
+  return ((2u << b) - 1u) & (0xffffffffu << a);
+}
+
+// The allowed columns of a 128-key tile as four 32-bit words (bit c of word c/32).
+__device__ __forceinline__ void row_mask(const RowPredicate& p, uint32_t (&w)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w[k] = span_bits(p.lo, p.hi, 32 * k) | (p.bits[k] & span_bits(0, p.hb, 32 * k));
+}
+
 __device__ __forceinline__ bool pred_allowed(const RowPredicate& p, int c) {
   const bool in_band = c >= p.lo && c <= p.hi;
   const bool in_cols = ((p.bits[c >> 5] >> (c & 31)) & 1u) && c <= p.hb;

@@ -507,7 +507,7 @@ spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   a.mask = p->mask_dev();
   a.walk = p->walk_enabled ? p->d_walk : nullptr;
   a.err = p->d_err;
-  a.wait_budget_ns = p->wait_budget_ns;
+  a.wait_budget_cycles = p->wait_budget_cycles;
   const spattn::Schedule& s = p->sched[dtype == SPATTN_BF16 ? 0 : 1];
   a.items = s.d_items;
   a.entries = s.d_entries;
