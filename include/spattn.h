@@ -188,6 +188,26 @@ spattn_status spattn_fwd_host(const spattn_plan* plan, int32_t B, int32_t H,
                               void* Q_dev, void* K_dev, void* V_dev, void* O_dev,
                               float* LSE_dev, void* cuda_stream);
 
+/*
+ * The forward pass of spattn_fwd for callers that cannot allocate device memory
+ * (a process whose GPU memory is owned by another allocator, or a loop that must
+ * never pay for a cudaMalloc after start-up).  The method on the pages has no
+ * counterpart: this is a memory-management variant only.  Same arguments, layouts,
+ * results and errors as spattn_fwd, but the packing scratch (packed strided /
+ * global key columns and gathered global query rows) comes from one fixed 16 MiB
+ * array in the library's device memory, held by every GPU that loads the library
+ * until the process exits, so the call allocates nothing.  The scratch needed is
+ * B*H*(2*n_columns + n_global)*d*element_size bytes; above 16 MiB the call returns
+ * SPATTN_ERR_SHAPE and launches nothing.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  All calls share the array:
+ * calls that may overlap on the GPU (unordered streams) race and give wrong results.
+ */
+spattn_status spattn_fwd_static_scratch(const spattn_plan* plan, int32_t B, int32_t H,
+                                        spattn_dtype dtype, const void* Q, const void* K,
+                                        const void* V, float scale, void* O, float* LSE,
+                                        void* cuda_stream);
+
 /* Synchronise `cuda_stream` and report (then clear) the plan's device error word:
  * SPATTN_OK, SPATTN_ERR_TIMEOUT or SPATTN_ERR_CUDA. */
 spattn_status spattn_plan_check_device(const spattn_plan* plan, void* cuda_stream);

@@ -28,7 +28,7 @@ BF16, FP32 = 0, 1
 EXPORTS = ("spattn_mask_validate", "spattn_plan_create", "spattn_plan_info",
            "spattn_plan_copy_tiles", "spattn_plan_copy_columns", "spattn_plan_copy_schedule",
            "spattn_plan_set_walk_counter", "spattn_plan_walk_count", "spattn_fwd",
-           "spattn_fwd_host", "spattn_plan_check_device", "spattn_plan_destroy",
+           "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_check_device", "spattn_plan_destroy",
            "spattn_last_error", "spattn_version")
 
 
@@ -79,6 +79,7 @@ def lib():
             L.spattn_fwd_host.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, _vp,
                                           _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]
+            L.spattn_fwd_static_scratch.argtypes = L.spattn_fwd.argtypes
             L.spattn_plan_check_device.argtypes = [_vp, _vp]
             L.spattn_plan_destroy.argtypes = [_vp]
             L.spattn_plan_destroy.restype = None
@@ -230,6 +231,26 @@ def fwd(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None, want
                             v.data_ptr(), float(scale), out.data_ptr(),
                             lse.data_ptr() if lse is not None else None,
                             _stream_handle(stream)))
+    return out, lse
+
+
+def fwd_static_scratch(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None):
+    """fwd() through spattn_fwd_static_scratch: the packing scratch comes from the
+    library's fixed 16 MiB device array, so the call allocates no device memory
+    (out / lse are allocated here only when not given)."""
+    import torch
+    B, H, T, d = q.shape
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, H, T, d):
+            raise ValueError("q, k, v must be contiguous CUDA tensors of equal shape")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    _check(lib().spattn_fwd_static_scratch(plan.handle, B, H, _dtype_code(q), q.data_ptr(),
+                                           k.data_ptr(), v.data_ptr(), float(scale),
+                                           out.data_ptr(), lse.data_ptr(),
+                                           _stream_handle(stream)))
     return out, lse
 
 

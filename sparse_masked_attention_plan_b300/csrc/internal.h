@@ -150,4 +150,7 @@ cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** 
 // fwd_simt.cu (fp32 forward)
 cudaError_t launch_fwd_simt(int d, const TcArgs& a, cudaStream_t st);
 
+// spattn_api.cu: set the calling thread's spattn_last_error() message.
+void set_last_error(const char* msg);
+
 }  // namespace spattn

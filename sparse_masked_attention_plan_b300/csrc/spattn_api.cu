@@ -212,6 +212,8 @@ spattn_status check_ptr(const void* p, const char* name) {
 
 }  // namespace
 
+void spattn::set_last_error(const char* msg) { g_last_error = msg; }
+
 extern "C" {
 
 const char* spattn_last_error(void) { return g_last_error.c_str(); }
