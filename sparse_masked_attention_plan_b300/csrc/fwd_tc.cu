@@ -165,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64,
                       item.x + t * kTile, bh);
       int issued = 0;
+      int4 e_next = ents[0];
       for (int n = 0; n < n_ent; ++n) {
-        const int4 e = ents[n];
+        const int4 e = e_next;
+        if (n + 1 < n_ent) e_next = ents[n + 1];
         const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
         bool ok = true;
 #pragma unroll
@@ -206,8 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pph[2] = {0u, 0u};
         bool oinit[2] = {false, false};
         bool ok = true;
+        int4 e_next = ents[0];
         for (int n = 0; n < n_ent && ok; ++n) {
-          const int4 e = ents[n];
+          const int4 e = e_next;
+          if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: global latency off the issue path
           const bool a0 = (e.y & kActive0) != 0, a1 = (e.y & kActive1) != 0;
           const int kit = 2 * n, vit = 2 * n + 1;
           const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
@@ -288,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float mrow = -INFINITY, lrow = 0.f;
     uint32_t sph = 0;
     int n_done = 0;
+    int4 e_next = ents[0];
     for (int n = 0; n < n_ent; ++n) {
-      const int4 e = ents[n];
+      const int4 e = e_next;
+      if (n + 1 < n_ent) e_next = ents[n + 1];
       if (!(e.y & (kActive0 << wg))) continue;
       const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -309,9 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) mx8[j] = __uint_as_float(sr[j]);
 #pragma unroll
-      for (int c = 8; c < kTile; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 8; c + 16 <= kTile; c += 16)  // columns 8..119, two per instruction
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          mx8[j] = fmax3(mx8[j], __uint_as_float(sr[c + j]), __uint_as_float(sr[c + 8 + j]));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], __uint_as_float(sr[kTile - 8 + j]));
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float mcand = fmaxf(mrow, mx * c2);
       const bool need = mcand > mrow + kRescaleThreshold;
       float corr = 1.f;
@@ -321,22 +332,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         lrow *= corr;
       }
       const float msub = (mrow == -INFINITY) ? 0.f : mrow;
-      // P = 2^(s * scale * log2 e - m), stored as bf16 over the first half of S
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(s * scale * log2 e - m), stored as bf16 over the first half of S;
+      // the scale-and-shift and the row sum run two columns per instruction
+      const uint64_t c2x2 = f32x2(c2, c2), nmx2 = f32x2(-msub, -msub);
+      uint64_t acc2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int b = 0; b < 16; ++b) {
           const int c0 = 32 * q + 2 * b;
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c0]), c2, -msub));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c0 + 1]), c2, -msub));
-          sum4[b & 3] += p0 + p1;
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), c2x2,
+                                nmx2),
+                      x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          acc2[b & 1] = add_f32x2(acc2[b & 1], f32x2(p0, p1));
           pk[b] = pack_bf16x2(p0, p1);
         }
         tmem_st16(lane_base + colS + 16 * q, pk);
       }
-      const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      float s0, s1, s2, s3;
+      f32x2_split(acc2[0], s0, s1);
+      f32x2_split(acc2[1], s2, s3);
+      const float sum = (s0 + s1) + (s2 + s3);
       lrow += sum;
       if (n_done > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
