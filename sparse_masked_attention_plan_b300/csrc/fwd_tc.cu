@@ -79,26 +79,27 @@ struct KParams {
   uint64_t budget;
 };
 
+// Descriptors are built once per operand base; a k-step only adds its byte offset
+// / 16 to the start-address field (bits 0-13), which cannot carry out because
+// shared-memory addresses stay below 2^18.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = TcCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc_sw128(a_smem + off, 16, 1024), smem_desc_sw128(b_smem + off, 16, 1024),
-           C::kIdescQK, kk > 0 ? 1u : 0u);
+    const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, q_desc + off16, k_desc + off16, C::kIdescQK, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
   using C = TcCfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 16 * 128, C::kChunkBytes, 1024),
-           C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_ts(d_tmem, p_tmem + kk * 8, v_desc + ((kk * 16 * 128) >> 4), C::kIdescPV,
+           (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -201,6 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       unsigned long long walked = 0;
+      const uint64_t q0_desc = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t q1_desc = smem_desc_sw128(sQ + C::kTileBytes, 16, 1024);
+      const uint64_t kv_kdesc = smem_desc_sw128(sKV, 16, 1024);  // slot 0 as a K operand
+      const uint64_t kv_vdesc = smem_desc_sw128(sKV, C::kChunkBytes, 1024);  // slot 0 as V
+      constexpr uint32_t kSlot16 = C::kTileBytes >> 4;
       if (mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout)) {
         tc_fence_after();
         int pend1 = -1;
@@ -218,9 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1, p.budget, p.err,
                          kErrTimeout)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t k_smem = sKV + ks * C::kTileBytes;
+          const uint64_t k_desc = kv_kdesc + ks * kSlot16;
           if (a0) {
-            issue_qk<D>(tmem + C::kColS0, sQ, k_smem);
+            issue_qk<D>(tmem + C::kColS0, q0_desc, k_desc);
             mma_commit(BAR(C::kBarS + 0));
             ++walked;
           }
@@ -228,13 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout)) { ok = false; break; }
             pph[1] ^= 1u;
             tc_fence_after();
-            issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, sKV + pend_vs * C::kTileBytes, oinit[1]);
+            issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, kv_vdesc + pend_vs * kSlot16, oinit[1]);
             oinit[1] = true;
             mma_commit(BAR(C::kBarEmpty + pend_vs));
             pend1 = -1;
           }
           if (a1) {
-            issue_qk<D>(tmem + C::kColS1, sQ + C::kTileBytes, k_smem);
+            issue_qk<D>(tmem + C::kColS1, q1_desc, k_desc);
             mma_commit(BAR(C::kBarS + 1));
             ++walked;
           }
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(BAR(C::kBarP + 0), pph[0], p.budget, p.err, kErrTimeout)) { ok = false; break; }
             pph[0] ^= 1u;
             tc_fence_after();
-            issue_pv<D>(tmem + C::kColO0, tmem + C::kColS0, sKV + vs * C::kTileBytes, oinit[0]);
+            issue_pv<D>(tmem + C::kColO0, tmem + C::kColS0, kv_vdesc + vs * kSlot16, oinit[0]);
             oinit[0] = true;
           }
           if (a1) {
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && pend1 >= 0) {
           if (mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout)) {
             tc_fence_after();
-            issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, sKV + pend_vs * C::kTileBytes, oinit[1]);
+            issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, kv_vdesc + pend_vs * kSlot16, oinit[1]);
             mma_commit(BAR(C::kBarEmpty + pend_vs));
           }
         }
