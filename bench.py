@@ -39,8 +39,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the tensor-core forward kernel on the
 # 32K / W=4096 workload, from the ncu capture summarised in
-# profiles/fwd_tc_t32k_w4096.md, valid for the kernel source with this hash.
-TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+# profiles/fwd_tc_t32k_w4096.md (captured with H=8, 250.8 MB, scaled by 32/8 heads),
+# valid only for the kernel source with this hash; any other source reports null.
+TRAFFIC = {"kernel_sha": "990f6a680e699149", "bytes_per_launch": 1003.1e6, "workload": "t32k_w4096"}
 
 
 def kernel_sha() -> str:
@@ -305,7 +306,8 @@ def run_ours(args, cfg, p):
     if rank == 0:
         achieved = flops_step / (kernel_ms / 1e3) / 1e12 if kernel_ms else value / world
         traffic = (TRAFFIC["bytes_per_launch"]
-                   if TRAFFIC["kernel_sha"] == kernel_sha() else None)
+                   if TRAFFIC["kernel_sha"] == kernel_sha() and
+                   TRAFFIC["workload"] == args.workload and not args.heads else None)
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             rate, pairs_done, nrows, secs, threads = oracle_sample_rate(cfg, p, Qh, Kh, Vh,
