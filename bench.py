@@ -121,14 +121,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """(world, rank, local_rank) from the torchrun environment; joins the process
+    group when world > 1 (NCCL for the GPU arm, gloo for CPU-only use)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl"
-        dist.init_process_group(backend=backend)
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
     return world, rank, local
 
 
@@ -139,13 +141,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The maximum of x over all ranks (x itself when world == 1)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(total_ms: float, steps: int, flops_per_step_per_rank: float, world: int):
+    """(ms_per_step, TFLOP/s) of the whole job: the slowest rank's time, every rank's work."""
+    ms = max_over_ranks(total_ms, world) / steps
+    return ms, world * flops_per_step_per_rank / (ms / 1e3) / 1e12
 
 
 # ----------------------------------------------------------------- CPU oracle arm
@@ -281,10 +291,7 @@ def run_ours(args, cfg, p):
         barrier(world)
     plan.check_device(stream)
     per = [ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    total_ms = max_over_ranks(total_ms, world)
-    ms_per_step = total_ms / args.steps
-    value = world * flops_step / (ms_per_step / 1e3) / 1e12
+    ms_per_step, value = aggregate(ev[0].elapsed_time(ev[-1]), args.steps, flops_step, world)
 
     # end to end through the host-buffer C-ABI entry: H2D of q, k, v, the forward,
     # D2H of O and LSE, every step

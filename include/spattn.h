@@ -208,6 +208,20 @@ spattn_status spattn_fwd_static_scratch(const spattn_plan* plan, int32_t B, int3
                                         const void* V, float scale, void* O, float* LSE,
                                         void* cuda_stream);
 
+/* Time budget, in SM clock cycles, of every device-side wait of the bf16 forward
+ * kernel (default 8e9, about 4 s at 2 GHz).  A wait that runs out records
+ * SPATTN_ERR_TIMEOUT in the plan's device error word; the kernel then drains its
+ * in-flight copies and products, frees its tensor memory and returns, so the CUDA
+ * context stays usable.  Errors: NULL, SHAPE (cycles == 0). */
+spattn_status spattn_plan_set_wait_budget(spattn_plan* plan, uint64_t cycles);
+
+/* Test hook for the failure path above: while enabled, the bf16 forward kernel's
+ * MMA warp first waits on a barrier that nothing signals, so that wait runs out of
+ * its budget (set a short one first) and the call's error word reports
+ * SPATTN_ERR_TIMEOUT through spattn_plan_check_device.  No fault, trap or unbounded
+ * wait is involved.  The outputs of such a call are unspecified. */
+spattn_status spattn_plan_test_wait_timeout(spattn_plan* plan, int32_t enable);
+
 /* Synchronise `cuda_stream` and report (then clear) the plan's device error word:
  * SPATTN_OK, SPATTN_ERR_TIMEOUT or SPATTN_ERR_CUDA. */
 spattn_status spattn_plan_check_device(const spattn_plan* plan, void* cuda_stream);

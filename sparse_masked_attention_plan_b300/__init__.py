@@ -28,7 +28,8 @@ BF16, FP32 = 0, 1
 EXPORTS = ("spattn_mask_validate", "spattn_plan_create", "spattn_plan_info",
            "spattn_plan_copy_tiles", "spattn_plan_copy_columns", "spattn_plan_copy_schedule",
            "spattn_plan_set_walk_counter", "spattn_plan_walk_count", "spattn_fwd",
-           "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_check_device", "spattn_plan_destroy",
+           "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
+           "spattn_plan_test_wait_timeout", "spattn_plan_check_device", "spattn_plan_destroy",
            "spattn_last_error", "spattn_version")
 
 
@@ -80,6 +81,8 @@ def lib():
                                           _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]
             L.spattn_fwd_static_scratch.argtypes = L.spattn_fwd.argtypes
+            L.spattn_plan_set_wait_budget.argtypes = [_vp, ctypes.c_uint64]
+            L.spattn_plan_test_wait_timeout.argtypes = [_vp, ctypes.c_int32]
             L.spattn_plan_check_device.argtypes = [_vp, _vp]
             L.spattn_plan_destroy.argtypes = [_vp]
             L.spattn_plan_destroy.restype = None
@@ -199,6 +202,12 @@ class Plan:
         v = ctypes.c_int64()
         _check(lib().spattn_plan_walk_count(self._h, ctypes.byref(v)))
         return v.value
+
+    def set_wait_budget(self, cycles: int):
+        _check(lib().spattn_plan_set_wait_budget(self._h, int(cycles)))
+
+    def test_wait_timeout(self, enable=True):
+        _check(lib().spattn_plan_test_wait_timeout(self._h, 1 if enable else 0))
 
     def check_device(self, stream=None):
         _check(lib().spattn_plan_check_device(self._h, _stream_handle(stream)))

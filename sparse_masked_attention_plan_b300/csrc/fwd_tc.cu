@@ -55,10 +55,12 @@ struct TcCfg {
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
-  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_final
+  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_final, and one that
+  // nothing ever arrives on (the wait-timeout test waits on it)
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
                        kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
-                       kBarO = 2 * kStages + 5, kNumBars = 2 * kStages + 6;
+                       kBarO = 2 * kStages + 5, kBarNever = 2 * kStages + 6,
+                       kNumBars = 2 * kStages + 7;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
@@ -77,6 +79,7 @@ struct KParams {
   unsigned long long* walk;
   int* err;
   uint64_t budget;
+  int inject_timeout;  // test hook: the MMA warp first waits on a barrier nobody signals
 };
 
 // Descriptors are built once per operand base; a k-step only adds its byte offset
@@ -138,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::kBarP + 0), 128);
     mbar_init(BAR(C::kBarP + 1), 128);
     mbar_init(BAR(C::kBarO), 1);
+    mbar_init(BAR(C::kBarNever), 1);
     fence_barrier_init();
   }
   if (warp == kLoadWarp && lane == 0) {
@@ -197,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
         mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
                   kErrTimeout);
+      mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);  // the Q tiles too
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -207,7 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kv_kdesc = smem_desc_sw128(sKV, 16, 1024);  // slot 0 as a K operand
       const uint64_t kv_vdesc = smem_desc_sw128(sKV, C::kChunkBytes, 1024);  // slot 0 as V
       constexpr uint32_t kSlot16 = C::kTileBytes >> 4;
-      if (mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout)) {
+      const bool started =
+          !p.inject_timeout || mbar_wait(BAR(C::kBarNever), 0, p.budget, p.err, kErrTimeout);
+      if (started && mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout)) {
         tc_fence_after();
         int pend1 = -1;
         uint32_t pend_vs = 0;
@@ -485,6 +492,7 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
   kp.walk = a.walk;
   kp.err = a.err;
   kp.budget = a.wait_budget_cycles;
+  kp.inject_timeout = a.inject_timeout;
   dim3 grid(a.n_items, a.BH);
   fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(mQ, mK, mV, mQg, mKc, mVc, kp);
   return cudaGetLastError();

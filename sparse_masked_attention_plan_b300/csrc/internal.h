@@ -81,6 +81,7 @@ struct spattn_plan {
   int32_t walk_enabled = 0;
   int* d_err = nullptr;
   uint64_t wait_budget_cycles = 8000000000ull;  // ~4 s at the maximum SM clock
+  int32_t inject_timeout = 0;                     // test hook, see spattn_plan_test_wait_timeout
 
   spattn::MaskDev mask_dev() const {
     spattn::MaskDev m;
@@ -144,6 +145,7 @@ struct TcArgs {
   unsigned long long* walk;
   int* err;
   uint64_t wait_budget_cycles;
+  int32_t inject_timeout = 0;
 };
 cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why);
 

@@ -510,6 +510,7 @@ spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   a.walk = p->walk_enabled ? p->d_walk : nullptr;
   a.err = p->d_err;
   a.wait_budget_cycles = p->wait_budget_cycles;
+  a.inject_timeout = p->inject_timeout;
   const spattn::Schedule& s = p->sched[dtype == SPATTN_BF16 ? 0 : 1];
   a.items = s.d_items;
   a.entries = s.d_entries;
@@ -551,6 +552,19 @@ spattn_status spattn_fwd_host(const spattn_plan* p, int32_t B, int32_t H, spattn
   CUDA_TRY(cudaMemcpyAsync(Oh, Od, bytes, cudaMemcpyDeviceToHost, stream));
   if (LSEh) CUDA_TRY(cudaMemcpyAsync(LSEh, LSEd, rows * 4, cudaMemcpyDeviceToHost, stream));
   CUDA_TRY(cudaStreamSynchronize(stream));
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_set_wait_budget(spattn_plan* p, uint64_t cycles) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  if (cycles == 0) return fail(SPATTN_ERR_SHAPE, "the wait budget must be positive");
+  p->wait_budget_cycles = cycles;
+  return SPATTN_OK;
+}
+
+spattn_status spattn_plan_test_wait_timeout(spattn_plan* p, int32_t enable) {
+  if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  p->inject_timeout = enable ? 1 : 0;
   return SPATTN_OK;
 }
 
