@@ -117,6 +117,7 @@ extern "C" spattn_status spattn_fwd_static_scratch(const spattn_plan* p, int32_t
   a.items = s.d_items;
   a.entries = s.d_entries;
   a.n_items = static_cast<int32_t>(s.items.size() / 4);
+  a.n_major = s.n_major;
   cudaError_t e;
   if (dtype == SPATTN_BF16) {
     const char* why = "";

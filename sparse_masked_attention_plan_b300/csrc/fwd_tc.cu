@@ -80,6 +80,9 @@ struct KParams {
   int* err;
   uint64_t budget;
   int inject_timeout;  // test hook: the MMA warp first waits on a barrier nobody signals
+  int BH;
+  int n_items;
+  int n_major;  // leading (longest) items launched for every head before the rest
 };
 
 // Descriptors are built once per operand base; a k-step only adds its byte offset
@@ -123,8 +126,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define BAR(k) (bar0 + 8u * static_cast<uint32_t>(k))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int4 item = p.items[blockIdx.x];
-  const int bh = blockIdx.y;
+  // Launch order: the n_major longest items for every (batch, head) first (rank-major,
+  // longest first), then the rest head by head (neighbouring query groups of one head
+  // share K/V tiles in L2).
+  int rank, bh;
+  {
+    const int u = blockIdx.x, nm = p.n_major * p.BH;
+    if (u < nm) {
+      rank = u / p.BH;
+      bh = u % p.BH;
+    } else {
+      const int rest = p.n_items - p.n_major;
+      bh = (u - nm) / rest;
+      rank = p.n_major + (u - nm) % rest;
+    }
+  }
+  const int4 item = p.items[rank];
   const int n_ent = item.z;
   const int4* ents = p.entries + item.y;
   const bool gathered = (item.w & kItemGathered) != 0;
@@ -160,8 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const void* mapQ = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
+    // The whole warp runs the loop (its values stay warp-uniform); one lane issues.
+    const void* mapQ = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
+    if (elect_one()) {
       mbar_arrive_expect_tx(BAR(C::kBarQ), 2 * C::kTileBytes);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
@@ -169,120 +187,143 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64,
                       item.x + t * kTile, bh);
-      int issued = 0;
-      int4 e_next = ents[0];
-      for (int n = 0; n < n_ent; ++n) {
-        const int4 e = e_next;
-        if (n + 1 < n_ent) e_next = ents[n + 1];
-        const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
-        bool ok = true;
+    }
+    __syncwarp();
+    int issued = 0;
+    bool ok = true;
+    int4 e_next = ents[0];
+    for (int n = 0; n < n_ent && ok; ++n) {
+      const int4 e = e_next;
+      if (n + 1 < n_ent) e_next = ents[n + 1];
+      const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = 2 * n + kv;
-          const int s = it % C::kStages;
-          const uint32_t ph = (it / C::kStages) & 1;
-          if (!mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout)) {
-            ok = false;
-            break;
-          }
-          const void* map = kv ? (packed ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV))
-                               : (packed ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK));
+      for (int kv = 0; kv < 2; ++kv) {
+        const int it = 2 * n + kv;
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout))) {
+          ok = false;
+          break;
+        }
+        const void* map = kv ? (packed ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV))
+                             : (packed ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK));
+        if (elect_one()) {
           mbar_arrive_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
                         c * 64, e.x, bh);
-          ++issued;
         }
-        if (!ok) break;
+        __syncwarp();
+        ++issued;
       }
-      // Drain: wait until the last load issued into each slot has landed, so no
-      // copy is still writing this CTA's shared memory when it exits.
-      for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
-        mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
-                  kErrTimeout);
-      mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);  // the Q tiles too
     }
+    // Drain: wait until the last load issued into each slot has landed, so no
+    // copy is still writing this CTA's shared memory when it exits.
+    for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+      mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
+                kErrTimeout);
+    mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);  // the Q tiles too
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      unsigned long long walked = 0;
-      const uint64_t q0_desc = smem_desc_sw128(sQ, 16, 1024);
-      const uint64_t q1_desc = smem_desc_sw128(sQ + C::kTileBytes, 16, 1024);
-      const uint64_t kv_kdesc = smem_desc_sw128(sKV, 16, 1024);  // slot 0 as a K operand
-      const uint64_t kv_vdesc = smem_desc_sw128(sKV, C::kChunkBytes, 1024);  // slot 0 as V
-      constexpr uint32_t kSlot16 = C::kTileBytes >> 4;
-      const bool started =
-          !p.inject_timeout || mbar_wait(BAR(C::kBarNever), 0, p.budget, p.err, kErrTimeout);
-      if (started && mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout)) {
+    // The whole warp runs the loop and waits; one elected lane (always lane 0 of the
+    // converged warp, so commits track its own products) issues MMAs and commits.
+    unsigned long long walked = 0;
+    const uint64_t q0_desc = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t q1_desc = smem_desc_sw128(sQ + C::kTileBytes, 16, 1024);
+    const uint64_t kv_kdesc = smem_desc_sw128(sKV, 16, 1024);  // slot 0 as a K operand
+    const uint64_t kv_vdesc = smem_desc_sw128(sKV, C::kChunkBytes, 1024);  // slot 0 as V
+    constexpr uint32_t kSlot16 = C::kTileBytes >> 4;
+    bool ok = __all_sync(0xffffffffu, !p.inject_timeout ||
+                                          mbar_wait(BAR(C::kBarNever), 0, p.budget, p.err, kErrTimeout));
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout));
+    if (ok) {
+      tc_fence_after();
+      int pend1 = -1;
+      uint32_t pend_vs = 0;
+      uint32_t pph[2] = {0u, 0u};
+      bool oinit[2] = {false, false};
+      int4 e_next = ents[0];
+      for (int n = 0; n < n_ent; ++n) {
+        const int4 e = e_next;
+        if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: global latency off the issue path
+        const bool a0 = (e.y & kActive0) != 0, a1 = (e.y & kActive1) != 0;
+        const int kit = 2 * n, vit = 2 * n + 1;
+        const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1,
+                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
         tc_fence_after();
-        int pend1 = -1;
-        uint32_t pend_vs = 0;
-        uint32_t pph[2] = {0u, 0u};
-        bool oinit[2] = {false, false};
-        bool ok = true;
-        int4 e_next = ents[0];
-        for (int n = 0; n < n_ent && ok; ++n) {
-          const int4 e = e_next;
-          if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: global latency off the issue path
-          const bool a0 = (e.y & kActive0) != 0, a1 = (e.y & kActive1) != 0;
-          const int kit = 2 * n, vit = 2 * n + 1;
-          const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
-          if (!mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1, p.budget, p.err,
-                         kErrTimeout)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t k_desc = kv_kdesc + ks * kSlot16;
-          if (a0) {
+        const uint64_t k_desc = kv_kdesc + ks * kSlot16;
+        if (a0) {
+          if (elect_one()) {
             issue_qk<D>(tmem + C::kColS0, q0_desc, k_desc);
             mma_commit(BAR(C::kBarS + 0));
-            ++walked;
           }
-          if (pend1 >= 0) {
-            if (!mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout)) { ok = false; break; }
-            pph[1] ^= 1u;
-            tc_fence_after();
+          __syncwarp();
+          ++walked;
+        }
+        if (pend1 >= 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err,
+                                                 kErrTimeout))) { ok = false; break; }
+          pph[1] ^= 1u;
+          tc_fence_after();
+          if (elect_one()) {
             issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, kv_vdesc + pend_vs * kSlot16, oinit[1]);
-            oinit[1] = true;
             mma_commit(BAR(C::kBarEmpty + pend_vs));
-            pend1 = -1;
           }
-          if (a1) {
+          __syncwarp();
+          oinit[1] = true;
+          pend1 = -1;
+        }
+        if (a1) {
+          if (elect_one()) {
             issue_qk<D>(tmem + C::kColS1, q1_desc, k_desc);
             mma_commit(BAR(C::kBarS + 1));
-            ++walked;
           }
-          mma_commit(BAR(C::kBarEmpty + ks));
-          if (!mbar_wait(BAR(C::kBarFull + vs), (vit / C::kStages) & 1, p.budget, p.err,
-                         kErrTimeout)) { ok = false; break; }
-          tc_fence_after();
-          if (a0) {
-            if (!mbar_wait(BAR(C::kBarP + 0), pph[0], p.budget, p.err, kErrTimeout)) { ok = false; break; }
-            pph[0] ^= 1u;
-            tc_fence_after();
-            issue_pv<D>(tmem + C::kColO0, tmem + C::kColS0, kv_vdesc + vs * kSlot16, oinit[0]);
-            oinit[0] = true;
-          }
-          if (a1) {
-            pend1 = n;
-            pend_vs = vs;
-          } else {
-            mma_commit(BAR(C::kBarEmpty + vs));
-          }
+          __syncwarp();
+          ++walked;
         }
-        if (ok && pend1 >= 0) {
-          if (mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout)) {
-            tc_fence_after();
+        if (elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + vs), (vit / C::kStages) & 1,
+                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
+        tc_fence_after();
+        if (a0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + 0), pph[0], p.budget, p.err,
+                                                 kErrTimeout))) { ok = false; break; }
+          pph[0] ^= 1u;
+          tc_fence_after();
+          if (elect_one()) issue_pv<D>(tmem + C::kColO0, tmem + C::kColS0, kv_vdesc + vs * kSlot16, oinit[0]);
+          __syncwarp();
+          oinit[0] = true;
+        }
+        if (a1) {
+          pend1 = n;
+          pend_vs = vs;
+        } else {
+          if (elect_one()) mma_commit(BAR(C::kBarEmpty + vs));
+          __syncwarp();
+        }
+      }
+      if (ok && pend1 >= 0) {
+        if (__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + 1), pph[1], p.budget, p.err, kErrTimeout))) {
+          tc_fence_after();
+          if (elect_one()) {
             issue_pv<D>(tmem + C::kColO1, tmem + C::kColS1, kv_vdesc + pend_vs * kSlot16, oinit[1]);
             mma_commit(BAR(C::kBarEmpty + pend_vs));
           }
+          __syncwarp();
         }
       }
-      // Arrives when every product issued above has completed; the epilogue reads
-      // O after it, and waiting here keeps TMEM allocated until no product runs.
-      mma_commit(BAR(C::kBarO));
-      mbar_wait(BAR(C::kBarO), 0, p.budget, p.err, kErrTimeout);
-      if (p.walk && walked) atomicAdd(p.walk, walked);
     }
+    // Arrives when every product issued above has completed; the epilogue reads
+    // O after it, and waiting here keeps TMEM allocated until no product runs.
+    if (elect_one()) mma_commit(BAR(C::kBarO));
+    __syncwarp();
+    mbar_wait(BAR(C::kBarO), 0, p.budget, p.err, kErrTimeout);
+    if (lane == 0 && p.walk && walked) atomicAdd(p.walk, walked);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -493,8 +534,16 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
   kp.err = a.err;
   kp.budget = a.wait_budget_cycles;
   kp.inject_timeout = a.inject_timeout;
-  dim3 grid(a.n_items, a.BH);
-  fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(mQ, mK, mV, mQg, mKc, mVc, kp);
+  kp.BH = a.BH;
+  kp.n_items = a.n_items;
+  kp.n_major = a.n_major;
+  const long long ctas = static_cast<long long>(a.n_items) * a.BH;
+  if (ctas > 0x7fffffffLL) {
+    *why = "too many work items";
+    return cudaErrorInvalidValue;
+  }
+  fwd_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, st>>>(mQ, mK, mV, mQg,
+                                                                                  mKc, mVc, kp);
   return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@ struct Schedule {
   int4* d_items = nullptr;
   int4* d_entries = nullptr;
   int64_t tile_products = 0;  // (query tile x key tile) products per (batch, head)
+  int32_t n_major = 0;        // leading items (>= 1.5x the median length) launched first
 };
 
 }  // namespace spattn
@@ -146,6 +147,7 @@ struct TcArgs {
   int* err;
   uint64_t wait_budget_cycles;
   int32_t inject_timeout = 0;
+  int32_t n_major = 0;
 };
 cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why);
 

@@ -191,6 +191,15 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
     std::stable_sort(items.begin(), items.end(),
                      [](const Item& x, const Item& y) { return x.cnt > y.cnt; });
   for (const Item& it : items) s->items.insert(s->items.end(), {it.q0, it.off, it.cnt, it.flags});
+  // items much longer than the median (e.g. gathered global rows that read every key)
+  // are launched first for every head, so they do not end up in the last wave
+  s->n_major = 0;
+  if (longest_first && !items.empty()) {
+    const int32_t median = items[items.size() / 2].cnt;
+    while (s->n_major < static_cast<int32_t>(items.size()) &&
+           2 * items[s->n_major].cnt >= 3 * median && items[s->n_major].cnt > median)
+      ++s->n_major;
+  }
 }
 
 spattn_status upload_schedule(spattn::Schedule* s) {
@@ -515,6 +524,7 @@ spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   a.items = s.d_items;
   a.entries = s.d_entries;
   a.n_items = static_cast<int32_t>(s.items.size() / 4);
+  a.n_major = s.n_major;
   if (dtype == SPATTN_BF16) {
     const char* why = "";
     cudaError_t e = spattn::launch_fwd_tc(p->d, a, stream, &why);
