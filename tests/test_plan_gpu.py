@@ -109,35 +109,41 @@ def covered_keys(plan_sched, cols, T, group_rows, qtile_rows, i, grow, p):
             rows = p["global_pos_sorted"][q0:q0 + group_rows]
             if i not in rows:
                 continue
-            t = int(np.nonzero(rows == i)[0][0]) // qtile_rows
+            # split items: both query tiles hold these rows, key tiles alternate
+            tiles = (0, 1) if fl & 2 else (int(np.nonzero(rows == i)[0][0]) // qtile_rows,)
         else:
             if grow or not (q0 <= i < q0 + group_rows):
                 continue
-            t = (i - q0) // qtile_rows
+            tiles = ((i - q0) // qtile_rows,)
         for (src, f, kb, lim) in ents[off:off + cnt]:
-            if not (f & (1 << t)):
-                continue
-            kind = (f >> 4) & 3
-            full = bool(f & (4 << t))  # the kernels skip the predicate: the whole tile counts
-            if kind == 1:
-                keys += [int(c) for c in (cols[src:src + 128] if full else cols[src:lim])]
-                continue
-            for j in range(src, src + 128):
-                if full:
-                    ok = True
-                elif j >= T:
-                    ok = False
-                elif kind == 2:
-                    ok = (j <= i) if causal else True
-                elif causal:
-                    w = p.get("window", 0)
-                    ok = j <= i and ((w == 0 or i - j < w) or j in colset)
-                else:
-                    r = p.get("radius", -1)
-                    ok = (r < 0 or abs(i - j) <= r) or j in colset
-                if ok:
-                    keys.append(j)
+            for t in tiles:
+                if f & (1 << t):
+                    keys += entry_keys(src, f, lim, t, i, T, cols, colset, causal, p)
     return keys
+
+
+def entry_keys(src, f, lim, t, i, T, cols, colset, causal, p):
+    kind = (f >> 4) & 3
+    full = bool(f & (4 << t))  # the kernels skip the predicate: the whole tile counts
+    if kind == 1:
+        return [int(c) for c in (cols[src:src + 128] if full else cols[src:lim])]
+    out = []
+    for j in range(src, src + 128):
+        if full:
+            ok = True
+        elif j >= T:
+            ok = False
+        elif kind == 2:
+            ok = (j <= i) if causal else True
+        elif causal:
+            w = p.get("window", 0)
+            ok = j <= i and ((w == 0 or i - j < w) or j in colset)
+        else:
+            r = p.get("radius", -1)
+            ok = (r < 0 or abs(i - j) <= r) or j in colset
+        if ok:
+            out.append(j)
+    return out
 
 
 @pytest.mark.parametrize("k", range(len(EDGE_SPECS)))
