@@ -54,10 +54,10 @@ typedef enum {
 typedef enum { SPATTN_BF16 = 0, SPATTN_FP32 = 1 } spattn_dtype;
 
 /*
- * Mask specification.  Allowed pairs (i, j), 0 <= i, j < T:
- *   causal = 1:  j <= i and (0 <= i-j < window  or  window == 0 (no window)
+ * Mask specification.  Allowed pairs (i, j), 0 <= i, j < T, with d = dilation:
+ *   causal = 1:  j <= i and ((i-j) % d == 0 and (i-j < window*d or window == 0)
  *                 or j strided or j global or i global)
- *   causal = 0:  |i-j| <= radius  (radius == -1: no limit)
+ *   causal = 0:  (|i-j| % d == 0 and (|i-j| <= radius*d or radius == -1))
  *                 or j strided or j global or i global
  * where "j strided" means stride > 0 and j % stride == stride_offset, and
  * "global" means a member of global_pos.
@@ -70,11 +70,16 @@ typedef enum { SPATTN_BF16 = 0, SPATTN_FP32 = 1 } spattn_dtype;
  * variants", section 3, "local radius 2": query 12 reads 10..14); global rows
  * read every key and global columns are read by every query, and both stay
  * causal in a causal mask (with_global and the look-ahead warning after it).
+ * A dilation d > 1 keeps every d-th key of the local window, so a causal window
+ * reads i, i-d, ..., i-(window-1)d ("Attention variants", section 6, the
+ * dilated(n, w, d) exercise: gap >= 0, gap % d == 0, gap < w d); d = 0 or 1 is the
+ * contiguous window.
  * Domains: causal in {0,1}; causal: window >= 0 and radius == -1; bidirectional:
  * radius >= -1 and window == 0; stride >= 0; 0 <= stride_offset < stride (or 0
  * when stride == 0); 0 <= n_global <= T; global_pos is a HOST array of n_global
  * distinct positions in [0, T), any order (it is copied; the caller keeps
- * ownership).  Anything else is SPATTN_ERR_INVALID_SPEC.
+ * ownership); 0 <= dilation <= 2^31, and with dilation > 1 window and radius at
+ * most 2^31.  Anything else is SPATTN_ERR_INVALID_SPEC.
  */
 typedef struct {
   int32_t causal;
@@ -84,6 +89,7 @@ typedef struct {
   int64_t stride_offset;
   int32_t n_global;
   const int32_t* global_pos;
+  int64_t dilation;
 } spattn_mask_spec;
 
 typedef struct spattn_plan spattn_plan; /* opaque, owned by the library */

@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY: imported by the tests, by ``__graft_entry__.smoke`` an
 the benchmark's CPU-baseline / reference leg.  The CUDA library never imports it.
 
 Every function takes the mask as plain fields (causal, window, radius, stride,
-offset, global_pos) and calls the C code compiled from ``oracle.c`` with gcc.
+offset, global_pos, dilation) and calls the C code compiled from ``oracle.c`` with gcc.
 """
 from __future__ import annotations
 
@@ -38,7 +38,7 @@ def build(force: bool = False) -> str:
 
 
 def _configure(lib):
-    spec = [ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i32p, _i64]
+    spec = [ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64, _i32p, _i64]
     lib.oracle_validate.argtypes = spec
     lib.oracle_validate.restype = ctypes.c_int
     lib.oracle_allowed.argtypes = spec + [_i64, _i64]
@@ -90,14 +90,16 @@ class use_library:
 
 
 class Mask:
-    """A mask rule: causal window / bidirectional radius, strided columns, globals."""
+    """A mask rule: causal window / bidirectional radius (optionally dilated), strided
+    columns, globals."""
 
     def __init__(self, T, causal=1, window=0, radius=-1, stride=0, offset=0,
-                 global_pos=()):
+                 global_pos=(), dilation=1):
         self.T = int(T)
         self.causal = int(causal)
         self.window = int(window)
         self.radius = int(radius)
+        self.dilation = int(dilation)
         self.stride = int(stride)
         self.offset = int(offset)
         self.gpos = np.ascontiguousarray(np.asarray(global_pos, dtype=np.int32))
@@ -105,10 +107,10 @@ class Mask:
     @classmethod
     def from_params(cls, T, p):
         return cls(T, p["causal"], p["window"], p["radius"], p["stride"], p["offset"],
-                   p.get("global_pos", ()))
+                   p.get("global_pos", ()), p.get("dilation", 1))
 
     def _args(self):
-        return (self.causal, self.window, self.radius, self.stride, self.offset,
+        return (self.causal, self.window, self.radius, self.dilation, self.stride, self.offset,
                 len(self.gpos), self.gpos.ctypes.data_as(_i32p), self.T)
 
     def validate(self) -> int:

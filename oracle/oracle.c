@@ -18,6 +18,10 @@
  *       (octlm "Sparse attention", §One mask function for every pattern).
  *     - bidirectional local radius r: |i-j| <= r ("Attention variants" §3 worked
  *       example, "local radius 2": query 12 reads 10..14).  r = -1: no limit.
+ *     - dilation d >= 1 of the local window: only keys whose distance is a multiple
+ *       of d, and w (or r) counts those keys, so the causal window reads i, i-d, ...,
+ *       i-(w-1)d: 0 <= i-j < w d with (i-j) % d == 0 ("Attention variants" §6,
+ *       the dilated(n, w, d) exercise).  d = 1 is the contiguous window.
  *     - strided columns: key j with j % s == o is readable by every query (causal:
  *       every later query).  o = 0 is the octlm convention (columns % stride == 0),
  *       o = s-1 the "Attention variants" local_strided convention.
@@ -48,6 +52,7 @@ typedef struct {
   int causal;      /* 1: j <= i only */
   int64_t window;  /* causal local width, 0 = unbounded */
   int64_t radius;  /* bidirectional radius, -1 = unbounded */
+  int64_t dilation; /* local keys every dilation-th position, >= 1 */
   int64_t stride;  /* 0 = none */
   int64_t offset;  /* strided columns: j % stride == offset */
   int64_t n_global;
@@ -58,12 +63,16 @@ typedef struct {
 /* ---- spec checks: the readings every valid mask obeys ------------------------- */
 
 /* Returns 0 for a valid mask, a negative code naming the first violated rule. */
-int oracle_validate(int causal, int64_t window, int64_t radius, int64_t stride,
+int oracle_validate(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                     int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T) {
   if (T <= 0) return -1;
   if (causal != 0 && causal != 1) return -2;
   if (causal == 1 && (window < 0 || radius != -1)) return -3;
   if (causal == 0 && (radius < -1 || window != 0)) return -4;
+  /* products of a width and the dilation must stay far inside int64 */
+  if (dilation < 1 || dilation > ((int64_t)1 << 31) || window > ((int64_t)1 << 31) ||
+      radius > ((int64_t)1 << 31))
+    return -10;
   if (stride < 0) return -5;
   if (stride == 0 && offset != 0) return -6;
   if (stride > 0 && (offset < 0 || offset >= stride)) return -6;
@@ -88,14 +97,16 @@ static int allowed(const omask* m, int64_t i, int64_t j) {
   if (in_global(m, i)) return 1;                /* a global row reads every key */
   if (in_global(m, j)) return 1;                /* every query reads a global column */
   if (m->stride > 0 && j % m->stride == m->offset) return 1; /* strided column */
-  if (m->causal) return m->window == 0 || (i - j) < m->window; /* 0 <= i-j < w */
-  return m->radius < 0 || llabs(i - j) <= m->radius;            /* |i-j| <= r */
+  const int64_t gap = i - j;
+  if (llabs(gap) % m->dilation != 0) return 0;                  /* every d-th key only */
+  if (m->causal) return m->window == 0 || gap < m->window * m->dilation; /* 0 <= i-j < w d */
+  return m->radius < 0 || llabs(gap) <= m->radius * m->dilation;         /* |i-j| <= r d */
 }
 
-int oracle_allowed(int causal, int64_t window, int64_t radius, int64_t stride,
+int oracle_allowed(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                    int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
                    int64_t i, int64_t j) {
-  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
   return allowed(&m, i, j);
 }
 
@@ -122,20 +133,20 @@ static int64_t row_set_union(const omask* m, int64_t i, int32_t* out) {
     for (int64_t j = 0; j <= jmax; j++) out[n++] = (int32_t)j;
     return n;
   }
-  int64_t lo, hi; /* local interval */
+  int64_t lo, hi; /* local span; the local keys are its j with (i - j) % dilation == 0 */
   if (m->causal) {
-    lo = (m->window == 0) ? 0 : i - m->window + 1;
+    lo = (m->window == 0) ? 0 : i - (m->window - 1) * m->dilation;
     hi = i;
   } else {
-    lo = (m->radius < 0) ? 0 : i - m->radius;
-    hi = (m->radius < 0) ? T - 1 : i + m->radius;
+    lo = (m->radius < 0) ? 0 : i - m->radius * m->dilation;
+    hi = (m->radius < 0) ? T - 1 : i + m->radius * m->dilation;
   }
   if (lo < 0) lo = 0;
   if (hi > jmax) hi = jmax;
   /* three ascending streams: strided progression, global columns, local interval */
   int64_t js = (m->stride > 0) ? m->offset : T; /* next strided column */
   int64_t ag = 0;                                /* next global index */
-  int64_t jl = lo;                               /* next local column */
+  int64_t jl = lo + (i - lo) % m->dilation;       /* next local column (lo <= i) */
   int64_t last = -1;
   for (;;) {
     int64_t cs = (js <= jmax) ? js : INT64_MAX;
@@ -149,25 +160,25 @@ static int64_t row_set_union(const omask* m, int64_t i, int32_t* out) {
     last = c;
     if (c == cs) js += m->stride;
     if (c == cg) ag++;
-    if (c == cl) jl++;
+    if (c == cl) jl += m->dilation;
   }
   return n;
 }
 
 /* Allowed set of one query, ascending.  method 0: union of rule sets, 1: full scan.
  * `out` must hold T entries.  Returns |S_i|. */
-int64_t oracle_row_set(int causal, int64_t window, int64_t radius, int64_t stride,
+int64_t oracle_row_set(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                        int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
                        int64_t i, int method, int32_t* out) {
-  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
   return method ? row_set_scan(&m, i, out) : row_set_union(&m, i, out);
 }
 
 /* Number of allowed (i, j) pairs: the sum of |S_i| (the glossary's edge count E). */
-int64_t oracle_count_pairs(int causal, int64_t window, int64_t radius, int64_t stride,
+int64_t oracle_count_pairs(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                            int64_t offset, int64_t n_global, const int32_t* gpos,
                            int64_t T) {
-  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
   int64_t total = 0;
 #pragma omp parallel
   {
@@ -181,10 +192,10 @@ int64_t oracle_count_pairs(int causal, int64_t window, int64_t radius, int64_t s
 
 /* Histogram of allowed pairs into BM x BN tiles: cnt[(i/BM) * nkb + (j/BN)].
  * `cnt` has ceil(T/BM) * ceil(T/BN) int32 entries and is overwritten. */
-void oracle_tile_counts(int causal, int64_t window, int64_t radius, int64_t stride,
+void oracle_tile_counts(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                         int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
                         int64_t BM, int64_t BN, int32_t* cnt) {
-  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
   const int64_t nqb = (T + BM - 1) / BM, nkb = (T + BN - 1) / BN;
   memset(cnt, 0, sizeof(int32_t) * (size_t)(nqb * nkb));
 #pragma omp parallel
@@ -216,13 +227,13 @@ static double load_elem(const void* p, int dtype, int64_t idx) {
 /* One head.  Q, K, V: [T][d] row-major, dtype 0 = fp32, 1 = bf16 bits.
  * rows: the query indices to evaluate (n_rows of them).
  * O: [n_rows][d] fp64, LSE: [n_rows] fp64 (natural log).  Returns total |S_i|. */
-int64_t oracle_attention_head(int causal, int64_t window, int64_t radius, int64_t stride,
+int64_t oracle_attention_head(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                               int64_t offset, int64_t n_global, const int32_t* gpos,
                               int64_t T, int64_t d, int dtype, const void* Q,
                               const void* K, const void* V, double scale,
                               const int64_t* rows, int64_t n_rows, double* O,
                               double* LSE) {
-  omask m = {causal, window, radius, stride, offset, n_global, gpos, T};
+  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
   int64_t total = 0;
 #pragma omp parallel
   {

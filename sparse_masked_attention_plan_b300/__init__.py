@@ -43,7 +43,7 @@ class MaskSpec(ctypes.Structure):
     _fields_ = [("causal", ctypes.c_int32), ("window", ctypes.c_int64),
                 ("radius", ctypes.c_int64), ("stride", ctypes.c_int64),
                 ("stride_offset", ctypes.c_int64), ("n_global", ctypes.c_int32),
-                ("global_pos", ctypes.POINTER(ctypes.c_int32))]
+                ("global_pos", ctypes.POINTER(ctypes.c_int32)), ("dilation", ctypes.c_int64)]
 
 
 _lib = None
@@ -100,11 +100,11 @@ def _check(status: int):
         raise SpattnError(status, lib().spattn_last_error().decode())
 
 
-def make_spec(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=()):
+def make_spec(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=(), dilation=1):
     """(MaskSpec, keepalive array) for the mask fields (see include/spattn.h)."""
     g = np.ascontiguousarray(np.asarray(global_pos, dtype=np.int32))
     spec = MaskSpec(int(causal), int(window), int(radius), int(stride), int(offset), len(g),
-                    g.ctypes.data_as(_i32p) if len(g) else None)
+                    g.ctypes.data_as(_i32p) if len(g) else None, int(dilation))
     return spec, g
 
 
@@ -125,13 +125,14 @@ class Plan:
     """Block-sparse plan of one mask for sequence length T (owns device memory)."""
 
     def __init__(self, T, head_dim, causal=1, window=0, radius=-1, stride=0, offset=0,
-                 global_pos=(), stream=None):
+                 global_pos=(), dilation=1, stream=None):
         self.T = int(T)
         self.head_dim = int(head_dim)
         self.mask = dict(causal=int(causal), window=int(window), radius=int(radius),
                          stride=int(stride), offset=int(offset),
-                         global_pos=np.asarray(global_pos, dtype=np.int32))
-        spec, keep = make_spec(causal, window, radius, stride, offset, global_pos)
+                         global_pos=np.asarray(global_pos, dtype=np.int32),
+                         dilation=int(dilation))
+        spec, keep = make_spec(causal, window, radius, stride, offset, global_pos, dilation)
         h = _vp()
         _check(lib().spattn_plan_create(ctypes.byref(spec), self.T, self.head_dim,
                                         _stream_handle(stream), ctypes.byref(h)))

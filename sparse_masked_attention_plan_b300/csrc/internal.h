@@ -25,6 +25,7 @@ struct MaskDev {
   int32_t causal;
   int32_t window;  // causal local width, 0 = none
   int32_t radius;  // bidirectional radius, -1 = none
+  int32_t dilation;  // local keys every dilation-th position (1 = contiguous)
   int32_t stride;  // 0 = none
   int32_t offset;
   int32_t n_global;
@@ -51,7 +52,7 @@ struct Schedule {
 struct spattn_plan {
   // normalised spec
   int32_t causal = 1;
-  int64_t window = 0, radius = -1, stride = 0, offset = 0;
+  int64_t window = 0, radius = -1, stride = 0, offset = 0, dilation = 1;
   int64_t T = 0;
   int32_t d = 0;
   int device = 0;
@@ -90,6 +91,7 @@ struct spattn_plan {
     m.causal = causal;
     m.window = static_cast<int32_t>(window);
     m.radius = static_cast<int32_t>(radius);
+    m.dilation = static_cast<int32_t>(dilation);
     m.stride = static_cast<int32_t>(stride);
     m.offset = static_cast<int32_t>(offset);
     m.n_global = static_cast<int32_t>(gpos.size());

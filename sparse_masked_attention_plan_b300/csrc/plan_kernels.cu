@@ -45,35 +45,99 @@ __device__ __forceinline__ int gns_count(const MaskDev& m, int x, int y) {
   return lower_bound(m.gpos_ns, m.n_gns, y + 1) - lower_bound(m.gpos_ns, m.n_gns, x);
 }
 
+// #{j in [x, y] : j % d == r}  (0 <= r < d)
+__device__ __forceinline__ int mod_count(int x, int y, int r, int d) {
+  if (y < x) return 0;
+  return floordiv(y - r, d) - floordiv(x - 1 - r, d);
+}
+
+// Inverse of a modulo m (gcd(a, m) == 1, m >= 1), by the extended Euclidean algorithm.
+__device__ long long inv_mod(long long a, long long m) {
+  long long g = m, x = 0, x1 = 1, a1 = ((a % m) + m) % m;
+  while (a1 != 0) {
+    const long long q = g / a1;
+    long long t = g - q * a1;
+    g = a1;
+    a1 = t;
+    t = x - q * x1;
+    x = x1;
+    x1 = t;
+  }
+  return ((x % m) + m) % m;
+}
+
+__device__ __forceinline__ long long floordiv64(long long u, long long v) {  // v > 0
+  return u >= 0 ? u / v : -((-u + v - 1) / v);
+}
+
+// #{j in [x, y] : j % m1 == r1 and j % m2 == r2}, by the Chinese remainder theorem.
+__device__ int crt_count(int x, int y, int r1, int m1, int r2, int m2) {
+  if (y < x) return 0;
+  long long a = m1, b = m2;
+  while (b) {
+    const long long t = a % b;
+    a = b;
+    b = t;
+  }
+  const long long g = a;
+  if (((static_cast<long long>(r2) - r1) % g + g) % g != 0) return 0;
+  const long long mg = m2 / g;  // solve m1 t == r2 - r1 (mod m2)
+  const long long rhs = (((static_cast<long long>(r2) - r1) / g) % mg + mg) % mg;
+  const long long t = mg == 1 ? 0 : (rhs * inv_mod((m1 / g) % mg, mg)) % mg;
+  const long long L = static_cast<long long>(m1) / g * m2;
+  const long long j0 = r1 + static_cast<long long>(m1) * t;  // the residue modulo L
+  return static_cast<int>(floordiv64(y - j0, L) - floordiv64(x - 1 - j0, L));
+}
+
+// Non-strided global columns in [x, y] on the dilation grid (j % d == r).
+__device__ int gns_count_grid(const MaskDev& m, int x, int y, int r, int d) {
+  if (m.n_gns == 0 || y < x) return 0;
+  int c = 0;
+  for (int k = lower_bound(m.gpos_ns, m.n_gns, x); k < m.n_gns && m.gpos_ns[k] <= y; ++k)
+    c += (m.gpos_ns[k] % d) == r;
+  return c;
+}
+
 // Allowed keys j in [a, b] for query row i (closed form; a <= b inside [0, T)).
+// The local keys are the j of the local span with (i - j) % dilation == 0.
 __device__ int row_count(const MaskDev& m, int i, int a, int b) {
   const int jmax = m.causal ? i : m.T - 1;
   if (b > jmax) b = jmax;
   if (b < a) return 0;
   if (m.rowglobal[i]) return b - a + 1;  // a global row reads every permitted key
+  const int d = m.dilation;
   int lo, hi;
   if (m.causal) {
-    lo = m.window ? i - m.window + 1 : 0;
+    lo = m.window ? i - (m.window - 1) * d : 0;
     hi = i;
   } else {
-    lo = m.radius >= 0 ? i - m.radius : 0;
-    hi = m.radius >= 0 ? i + m.radius : m.T - 1;
+    lo = m.radius >= 0 ? i - m.radius * d : 0;
+    hi = m.radius >= 0 ? i + m.radius * d : m.T - 1;
   }
   const int la = max(a, lo), lb = min(b, hi);
-  const int nl = lb >= la ? lb - la + 1 : 0;
-  const int ns = ap_count(m, a, b) - (nl ? ap_count(m, la, lb) : 0);
-  const int ng = gns_count(m, a, b) - (nl ? gns_count(m, la, lb) : 0);
+  if (d == 1) {
+    const int nl = lb >= la ? lb - la + 1 : 0;
+    const int ns = ap_count(m, a, b) - (nl ? ap_count(m, la, lb) : 0);
+    const int ng = gns_count(m, a, b) - (nl ? gns_count(m, la, lb) : 0);
+    return nl + ns + ng;
+  }
+  const int res = i % d;
+  const int nl = mod_count(la, lb, res, d);
+  const int ns = ap_count(m, a, b) -
+                 (nl && m.stride > 0 ? crt_count(la, lb, m.offset, m.stride, res, d) : 0);
+  const int ng = gns_count(m, a, b) - (nl ? gns_count_grid(m, la, lb, res, d) : 0);
   return nl + ns + ng;
 }
 
-// Can any (i in [q0,q1], j in [k0,k1]) be allowed by the local rule?
+// Can any (i in [q0,q1], j in [k0,k1]) be allowed by the local rule?  Conservative
+// (the local span only, ignoring the dilation grid): it only gates a fast skip.
 __device__ __forceinline__ bool local_meets(const MaskDev& m, int q0, int q1, int k0, int k1) {
   if (m.causal) {
     if (k0 > q1) return false;
-    return m.window == 0 || max(0, q0 - k1) < m.window;
+    return m.window == 0 || max(0, q0 - k1) <= (m.window - 1) * m.dilation;
   }
   if (m.radius < 0) return true;
-  return max(0, max(k0 - q1, q0 - k1)) <= m.radius;
+  return max(0, max(k0 - q1, q0 - k1)) <= m.radius * m.dilation;
 }
 
 __global__ void k_strided_flags(MaskDev m, uint8_t* flags, uint8_t* rowglobal) {

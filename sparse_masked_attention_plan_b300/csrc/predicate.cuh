@@ -25,6 +25,7 @@ namespace spattn {
 
 struct RowPredicate {
   int lo, hi, hb;
+  int dil, res;  // band columns also need c % dil == res (a dilated local window)
   uint32_t bits[4];
 };
 
@@ -35,17 +36,22 @@ __device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const u
   const int k0 = e.x;
   p.bits[0] = p.bits[1] = p.bits[2] = p.bits[3] = 0u;
   p.hb = -1;
+  p.dil = 1;
+  p.res = 0;
   if (kind == kKindBand) {
     int lo, hi, hb;
+    const int d = m.dilation;
     if (m.causal) {
-      lo = m.window ? i - m.window + 1 : 0;
+      lo = m.window ? i - (m.window - 1) * d : 0;
       hi = i;
       hb = i;
     } else {
-      lo = m.radius >= 0 ? i - m.radius : 0;
-      hi = m.radius >= 0 ? i + m.radius : m.T - 1;
+      lo = m.radius >= 0 ? i - m.radius * d : 0;
+      hi = m.radius >= 0 ? i + m.radius * d : m.T - 1;
       hb = m.T - 1;
     }
+    p.dil = d;
+    p.res = ((i - k0) % d + d) % d;  // column c = key k0 + c is on the grid iff c % d == res
     hi = min(hi, m.T - 1);
     hb = min(hb, m.T - 1);
     p.lo = lo - k0;
@@ -77,13 +83,23 @@ __device__ __forceinline__ uint32_t span_bits(int lo, int hi, int base) {
 
 // The allowed columns of a 128-key tile as four 32-bit words (bit c of word c/32).
 __device__ __forceinline__ void row_mask(const RowPredicate& p, uint32_t (&w)[4]) {
+  if (p.dil == 1) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    w[k] = span_bits(p.lo, p.hi, 32 * k) | (p.bits[k] & span_bits(0, p.hb, 32 * k));
+    for (int k = 0; k < 4; ++k)
+      w[k] = span_bits(p.lo, p.hi, 32 * k) | (p.bits[k] & span_bits(0, p.hb, 32 * k));
+    return;
+  }
+  // dilated window: every dil-th column of [lo, hi] starting on the row's residue
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = p.bits[k] & span_bits(0, p.hb, 32 * k);
+  int c = max(p.lo, 0);
+  c += ((p.res - c) % p.dil + p.dil) % p.dil;
+  const int last = min(p.hi, kTile - 1);
+  for (; c <= last; c += p.dil) w[c >> 5] |= 1u << (c & 31);
 }
 
 __device__ __forceinline__ bool pred_allowed(const RowPredicate& p, int c) {
-  const bool in_band = c >= p.lo && c <= p.hi;
+  const bool in_band = c >= p.lo && c <= p.hi && (p.dil == 1 || c % p.dil == p.res);
   const bool in_cols = ((p.bits[c >> 5] >> (c & 31)) & 1u) && c <= p.hb;
   return in_band || in_cols;
 }

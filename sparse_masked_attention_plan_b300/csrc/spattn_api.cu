@@ -71,17 +71,31 @@ struct Sched {
     return std::upper_bound(p->cols.begin(), p->cols.end(), static_cast<int32_t>(
                                 std::min<int64_t>(v, INT32_MAX))) - p->cols.begin();
   }
-  // Any (i in [a,b], j in [k0,k1]) allowed by the local rule?
-  bool local_meets(int64_t a, int64_t b, int64_t k0, int64_t k1) const {
-    if (p->causal) {
-      if (k0 > b) return false;
-      return p->window == 0 || std::max<int64_t>(0, a - k1) < p->window;
-    }
-    if (p->radius < 0) return true;
-    return std::max<int64_t>(0, std::max(k0 - b, a - k1)) <= p->radius;
+  static int64_t floor_div(int64_t x, int64_t d) { return x >= 0 ? x / d : -((-x + d - 1) / d); }
+  // Is a multiple of the dilation inside [lo, hi]?
+  bool grid_in(int64_t lo, int64_t hi) const {
+    if (lo > hi) return false;
+    const int64_t d = p->dilation;
+    return (floor_div(lo + d - 1, d)) * d <= hi;
   }
-  // Every (i in [a,b], j in [k0,k1]) allowed by the local rule?
+  // Any (i in [a,b], j in [k0,k1]) allowed by the local rule?  (The distances i - j
+  // of such pairs fill [a - k1, b - k0]; the rule wants one on the dilation grid.)
+  bool local_meets(int64_t a, int64_t b, int64_t k0, int64_t k1) const {
+    const int64_t d = p->dilation;
+    if (p->causal) {
+      const int64_t hi = p->window ? std::min(b - k0, (p->window - 1) * d) : b - k0;
+      return grid_in(std::max<int64_t>(0, a - k1), hi);
+    }
+    int64_t lo = a - k1, hi = b - k0;
+    if (p->radius >= 0) {
+      lo = std::max(lo, -p->radius * d);
+      hi = std::min(hi, p->radius * d);
+    }
+    return grid_in(lo, hi);
+  }
+  // Every (i in [a,b], j in [k0,k1]) allowed by the local rule?  (never with a dilation)
   bool local_covers(int64_t a, int64_t b, int64_t k0, int64_t k1) const {
+    if (p->dilation > 1) return false;
     if (p->causal) return k1 <= a && (p->window == 0 || b - k0 < p->window);
     if (p->radius < 0) return true;
     return b - k0 <= p->radius && k1 - a <= p->radius;
@@ -111,12 +125,13 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
   for (int64_t g = 0; g < n_groups; ++g) {
     const int64_t r0 = g * group_rows, r1 = std::min<int64_t>(r0 + group_rows, T) - 1;
     int64_t jlo, jhi;
+    const int64_t d = p->dilation;
     if (p->causal) {
-      jlo = p->window ? std::max<int64_t>(0, r0 - p->window + 1) : 0;
+      jlo = p->window ? std::max<int64_t>(0, r0 - (p->window - 1) * d) : 0;
       jhi = r1;
     } else {
-      jlo = p->radius >= 0 ? std::max<int64_t>(0, r0 - p->radius) : 0;
-      jhi = p->radius >= 0 ? std::min<int64_t>(T - 1, r1 + p->radius) : T - 1;
+      jlo = p->radius >= 0 ? std::max<int64_t>(0, r0 - p->radius * d) : 0;
+      jhi = p->radius >= 0 ? std::min<int64_t>(T - 1, r1 + p->radius * d) : T - 1;
     }
     const int64_t kb_lo = jlo / kTile, kb_hi = jhi / kTile;
     const int32_t off = static_cast<int32_t>(s->entries.size() / 4);
@@ -241,6 +256,10 @@ spattn_status spattn_mask_validate(const spattn_mask_spec* spec, int64_t T) {
     if (spec->radius < -1) return fail(SPATTN_ERR_INVALID_SPEC, "radius must be >= -1");
     if (spec->window != 0) return fail(SPATTN_ERR_INVALID_SPEC, "bidirectional mask takes window = 0");
   }
+  if (spec->dilation < 0 || spec->dilation > (int64_t(1) << 31))
+    return fail(SPATTN_ERR_INVALID_SPEC, "dilation must lie in [0, 2^31]");
+  if (spec->dilation > 1 && (spec->window > (int64_t(1) << 31) || spec->radius > (int64_t(1) << 31)))
+    return fail(SPATTN_ERR_INVALID_SPEC, "with a dilation, window and radius must be <= 2^31");
   if (spec->stride < 0) return fail(SPATTN_ERR_INVALID_SPEC, "stride must be >= 0");
   if (spec->stride == 0 && spec->stride_offset != 0)
     return fail(SPATTN_ERR_INVALID_SPEC, "stride_offset must be 0 without a stride");
@@ -282,6 +301,15 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
   p->causal = spec->causal;
   p->window = std::min<int64_t>(spec->window, T);
   p->radius = spec->radius < 0 ? -1 : std::min<int64_t>(spec->radius, T);
+  p->dilation = spec->dilation < 1 ? 1 : spec->dilation;
+  if (p->dilation >= T) {  // only distance 0 is a multiple of d below T: each row reads itself
+    if (p->causal) p->window = 1; else p->radius = 0;
+    p->dilation = 1;
+  }
+  if (p->dilation > 1) {  // spans reaching past the sequence are the unbounded window
+    if (p->causal && p->window > 0 && (p->window - 1) * p->dilation >= T) p->window = 0;
+    if (!p->causal && p->radius >= 0 && p->radius * p->dilation >= T) p->radius = -1;
+  }
   p->stride = spec->stride;
   p->offset = spec->stride_offset;
   if (p->stride > T) {  // at most one strided column, j == offset

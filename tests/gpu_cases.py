@@ -71,7 +71,8 @@ def run_and_compare(B, H, T, d, mask, dtype="bf16", seed=0, heads=None, rows=Non
     O = o.float().cpu().numpy()
     L = lse.cpu().numpy()
     m = oracle.Mask(T, mask.get("causal", 1), mask.get("window", 0), mask.get("radius", -1),
-                    mask.get("stride", 0), mask.get("offset", 0), mask.get("global_pos", ()))
+                    mask.get("stride", 0), mask.get("offset", 0), mask.get("global_pos", ()),
+                    mask.get("dilation", 1))
     heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     tol = TOL[dtype]
     worst = dict(max_abs=0.0, rel_l2=0.0, lse=0.0)

@@ -32,19 +32,23 @@ GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
 def mask_of(e) -> oracle.Mask:
     return oracle.Mask(e["T"], e.get("causal", 1), e.get("window", 0),
                        e.get("radius", -1), e.get("stride", 0), e.get("offset", 0),
-                       e.get("global_pos", []))
+                       e.get("global_pos", []), e.get("dilation", 1))
 
 
 # ---------------------------------------------------------------- independent rules
 
-def np_dense_mask(T, causal, window, radius, stride, offset, gpos) -> np.ndarray:
-    """Dense boolean mask, True = may attend, from index grids (independent of oracle.c)."""
+def np_dense_mask(T, causal, window, radius, stride, offset, gpos, dilation=1) -> np.ndarray:
+    """Dense boolean mask, True = may attend, from index grids (independent of oracle.c).
+    The dilated local rule is the "Attention variants" exercise's dilated(n, w, d):
+    gap >= 0, gap % d == 0, gap < w d (bidirectional: |gap| <= r d, |gap| % d == 0)."""
     i, j = np.indices((T, T))
     past = j <= i
+    gap = i - j
+    on_grid = (np.abs(gap) % dilation) == 0
     if causal:
-        local = past & ((i - j < window) if window > 0 else np.ones_like(past))
+        local = past & on_grid & ((gap < window * dilation) if window > 0 else True)
     else:
-        local = (np.abs(i - j) <= radius) if radius >= 0 else np.ones_like(past)
+        local = on_grid & ((np.abs(gap) <= radius * dilation) if radius >= 0 else True)
     m = local.copy()
     if stride > 0:
         col = (j % stride == offset)
@@ -58,8 +62,13 @@ def np_dense_mask(T, causal, window, radius, stride, offset, gpos) -> np.ndarray
     return m
 
 
-def closed_form_pairs(T, causal, window, radius, stride, offset, gpos) -> int:
-    """Pair count by inclusion-exclusion per row: |L| + |S minus L| + |G minus (L u S)|."""
+def closed_form_pairs(T, causal, window, radius, stride, offset, gpos, dilation=1) -> int:
+    """Pair count by inclusion-exclusion per row: |L| + |S minus L| + |G minus (L u S)|.
+    With a dilation d > 1 the row terms are counted by brute force over each row's
+    local span (still independent of oracle.c)."""
+    if dilation > 1:
+        D = np_dense_mask(T, causal, window, radius, stride, offset, gpos, dilation)
+        return int(D.sum())
     i = np.arange(T, dtype=np.int64)
     jmax = i if causal else np.full(T, T - 1, dtype=np.int64)
     if causal:
@@ -122,8 +131,9 @@ def small_specs(seed=0, n=60):
         offset = int(rng.integers(0, stride)) if stride else 0
         g = int(rng.choice([0, 0, 1, 3, 5]))
         gpos = np.sort(rng.choice(T, size=min(g, T), replace=False)).tolist()
+        dilation = int(rng.choice([1, 1, 1, 2, 3, 5]))
         out.append(dict(T=T, causal=causal, window=window, radius=radius, stride=stride,
-                        offset=offset, global_pos=gpos))
+                        offset=offset, global_pos=gpos, dilation=dilation))
     return out
 
 
@@ -195,6 +205,33 @@ def check_edge_formula():
     return bad
 
 
+def check_dilated_counts():
+    """The dilated causal window of the "Attention variants" exercise (section 6,
+    dilated(n, w, d)): row i reads i, i-d, ..., i-(w-1)d, those >= 0, so its count is
+    min(w, floor(i/d) + 1).  The exercise asks for n=16, w=4, d=2 (not printed: the
+    closed form gives 52)."""
+    bad = []
+    for n, w, d in [(16, 4, 2), (30, 5, 3), (64, 8, 7), (20, 1, 4), (33, 40, 2), (50, 0, 3)]:
+        cap = w if w else n  # window 0: no limit
+        want = sum(min(cap, i // d + 1) for i in range(n))
+        got = oracle.Mask(n, 1, w, dilation=d).count_pairs()
+        if got != want:
+            bad.append(f"dilated count n={n} w={w} d={d}: {got} != {want}")
+    if oracle.Mask(16, 1, 4, dilation=2).count_pairs() != 52:
+        bad.append("dilated(16, 4, 2) != 52")
+    if oracle.Mask(16, 1, 4, dilation=2).row_set(15).tolist() != [9, 11, 13, 15]:
+        bad.append("dilated(16, 4, 2): query 15 does not read 9, 11, 13, 15")
+    # bidirectional radius r on the dilation grid: 2r+1 keys away from the ends
+    m = oracle.Mask(40, 0, 0, 3, dilation=4)
+    if m.row_set(20).tolist() != [8, 12, 16, 20, 24, 28, 32]:
+        bad.append("bidirectional r=3 d=4 row 20")
+    # dilation 1 is the contiguous window
+    for T, w in [(30, 7), (17, 1)]:
+        if oracle.Mask(T, 1, w, dilation=1).count_pairs() != oracle.Mask(T, 1, w).count_pairs():
+            bad.append("dilation 1 differs from the plain window")
+    return bad
+
+
 def check_causal_equivalences():
     bad = []
     for T in [1, 2, 5, 16, 33]:
@@ -220,7 +257,7 @@ def check_against_numpy_rules(seed=0):
             bad.append(f"valid spec rejected: {e}")
             continue
         D = np_dense_mask(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
-                          e["offset"], e["global_pos"])
+                          e["offset"], e["global_pos"], e["dilation"])
         for i in range(e["T"]):
             u = m.row_set(i, "union").tolist()
             s = m.row_set(i, "scan").tolist()
@@ -231,7 +268,7 @@ def check_against_numpy_rules(seed=0):
         if m.count_pairs() != int(D.sum()):
             bad.append(f"count of {e}")
         if closed_form_pairs(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
-                             e["offset"], e["global_pos"]) != int(D.sum()):
+                             e["offset"], e["global_pos"], e["dilation"]) != int(D.sum()):
             bad.append(f"closed form of {e}")
         for BM, BN in [(4, 4), (8, 16), (128, 128)]:
             cnt = m.tile_counts(BM, BN)
@@ -253,7 +290,7 @@ def check_rejects_invalid():
         dict(T=8, causal=0, window=3, radius=1), dict(T=8, stride=-1),
         dict(T=8, stride=4, offset=4), dict(T=8, stride=0, offset=1),
         dict(T=8, global_pos=[8]), dict(T=8, global_pos=[-1]),
-        dict(T=8, global_pos=[3, 3]),
+        dict(T=8, global_pos=[3, 3]), dict(T=8, dilation=0),
     ]
     for c in cases:
         if mask_of(c).validate() == 0:
@@ -308,7 +345,8 @@ def check_sdpa_masked(seed=5):
         Q, K, V = _rand(T, d, 100 + n)
         sc = 0.7 / math.sqrt(d)
         D = torch.from_numpy(np_dense_mask(T, e["causal"], e["window"], e["radius"],
-                                           e["stride"], e["offset"], e["global_pos"]))
+                                           e["stride"], e["offset"], e["global_pos"],
+                                           e["dilation"]))
         q, k, v = (x.double()[None, None] for x in (Q, K, V))
         ref = torch.nn.functional.scaled_dot_product_attention(
             q, k, v, attn_mask=D[None, None], scale=sc)[0, 0].numpy()
@@ -380,6 +418,6 @@ def check_special_values():
 
 
 COUNT_CHECKS = [check_page_counts, check_row_sets, check_reach, check_edge_formula,
-                check_causal_equivalences, check_against_numpy_rules,
+                check_dilated_counts, check_causal_equivalences, check_against_numpy_rules,
                 check_rejects_invalid]
 ATTENTION_CHECKS = [check_sdpa_dense, check_sdpa_masked, check_special_values]

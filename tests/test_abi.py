@@ -58,10 +58,11 @@ def test_version(built):
 def test_validate_accepts_what_the_oracle_accepts(oracle_mod, built, seed):
     for e in small_specs(seed, n=60):
         m = oracle.Mask(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
-                        e["offset"], e["global_pos"])
+                        e["offset"], e["global_pos"], e["dilation"])
         assert m.validate() == 0
         st = sp.validate(e["T"], causal=e["causal"], window=e["window"], radius=e["radius"],
-                         stride=e["stride"], offset=e["offset"], global_pos=e["global_pos"])
+                         stride=e["stride"], offset=e["offset"], global_pos=e["global_pos"],
+                         dilation=e["dilation"])
         assert st == sp.OK, (e, built.spattn_last_error())
 
 
@@ -71,16 +72,17 @@ INVALID = [
     dict(T=8, causal=0, window=3, radius=1), dict(T=8, stride=-1),
     dict(T=8, stride=4, offset=4), dict(T=8, stride=0, offset=1),
     dict(T=8, global_pos=[8]), dict(T=8, global_pos=[-1]), dict(T=8, global_pos=[3, 3]),
+    dict(T=8, dilation=-1),
 ]
 
 
 @pytest.mark.parametrize("case", INVALID, ids=[str(c) for c in INVALID])
 def test_validate_rejects_what_the_oracle_rejects(oracle_mod, built, case):
-    c = dict(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=[])
+    c = dict(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=[], dilation=1)
     c.update(case)
     T = c.pop("T")
     m = oracle.Mask(T, c["causal"], c["window"], c["radius"], c["stride"], c["offset"],
-                    c["global_pos"])
+                    c["global_pos"], c["dilation"])
     assert m.validate() != 0
     assert sp.validate(T, **c) != sp.OK
 

@@ -41,6 +41,13 @@ SWEEP = [
                            global_pos=list(range(0, 1000, 97)))),
     (1, 2, 1100, 64, dict(causal=1, window=0, stride=64)),
     (1, 1, 1300, 128, dict(causal=0, radius=300, global_pos=list(range(5, 1300, 4)))),
+    # dilated local windows ("Attention variants" dilated(n, w, d)), alone and mixed
+    (1, 2, 1000, 64, dict(causal=1, window=64, dilation=2)),
+    (2, 1, 777, 128, dict(causal=1, window=50, dilation=5, stride=64, offset=3,
+                          global_pos=[1, 400])),
+    (1, 2, 900, 64, dict(causal=0, radius=30, dilation=4, stride=100, offset=0,
+                         global_pos=[17, 600])),
+    (1, 1, 513, 128, dict(causal=1, window=0, dilation=3)),
 ]
 
 

@@ -16,14 +16,17 @@ from pins import ATTENTION_CHECKS, COUNT_CHECKS
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = {
-    "window_off_by_one_rule": ("(i - j) < m->window", "(i - j) <= m->window"),
-    "window_off_by_one_set": ("i - m->window + 1;", "i - m->window;"),
+    "window_off_by_one_rule": ("gap < m->window * m->dilation", "gap <= m->window * m->dilation"),
+    "window_off_by_one_set": ("i - (m->window - 1) * m->dilation;", "i - m->window * m->dilation;"),
+    "dilation_ignored_in_rule": ("if (llabs(gap) % m->dilation != 0) return 0;", ""),
+    "dilation_phase_ignored": ("lo + (i - lo) % m->dilation;", "lo;"),
+    "dilation_span_undilated": ("i - (m->window - 1) * m->dilation;", "i - (m->window - 1);"),
     "stride_phase_zero": ("j % m->stride == m->offset", "j % m->stride == 0"),
     "stride_start_zero": ("(m->stride > 0) ? m->offset : T", "(m->stride > 0) ? 0 : T"),
     "global_row_not_causal": ("const int64_t jmax = m->causal ? i : T - 1;",
                               "const int64_t jmax = T - 1;"),
-    "radius_exclusive": ("llabs(i - j) <= m->radius", "llabs(i - j) < m->radius"),
-    "radius_set_short": ("i + m->radius;", "i + m->radius - 1;"),
+    "radius_exclusive": ("llabs(gap) <= m->radius * m->dilation", "llabs(gap) < m->radius * m->dilation"),
+    "radius_set_short": ("i + m->radius * m->dilation;", "i + m->radius * m->dilation - 1;"),
     "global_col_ignored": ("if (in_global(m, j)) return 1;", ""),
     "dropped_scale": ("s[a] = scale * acc;", "s[a] = acc;"),
     "normaliser_unshifted": ("l += exp(s[a] - mx);", "l += exp(s[a]);"),

@@ -28,12 +28,19 @@ EDGE_SPECS = [
     dict(T=1024, causal=1, window=0, stride=64, offset=0),
     dict(T=600, causal=1, window=200, stride=1000, offset=3),
     dict(T=600, causal=1, window=200, stride=1000, offset=700),
+    dict(T=700, causal=1, window=37, dilation=3),
+    dict(T=900, causal=1, window=100, dilation=2, stride=64, offset=1, global_pos=[0, 7, 450]),
+    dict(T=640, causal=0, radius=20, dilation=5, stride=16, offset=3, global_pos=[2, 300]),
+    dict(T=500, causal=1, window=0, dilation=7),
+    dict(T=300, causal=1, window=40, dilation=301),
+    dict(T=1000, causal=0, radius=3, dilation=200),
 ]
 
 
 def oracle_mask(T, p):
     return oracle.Mask(T, p.get("causal", 1), p.get("window", 0), p.get("radius", -1),
-                       p.get("stride", 0), p.get("offset", 0), p.get("global_pos", ()))
+                       p.get("stride", 0), p.get("offset", 0), p.get("global_pos", ()),
+                       p.get("dilation", 1))
 
 
 def expected_columns(T, p):
@@ -92,7 +99,8 @@ def test_random_spec_plans_match_oracle(oracle_mod, seed):
         e = dict(causal=causal, window=int(rng.choice([0, 1, 50, 129, 700])) if causal else 0,
                  radius=-1 if causal else int(rng.choice([-1, 0, 20, 128, 400])),
                  stride=s, offset=int(rng.integers(0, s)) if s else 0,
-                 global_pos=np.sort(rng.choice(T, int(rng.choice([0, 1, 9])), replace=False)))
+                 global_pos=np.sort(rng.choice(T, int(rng.choice([0, 1, 9])), replace=False)),
+                 dilation=int(rng.choice([1, 1, 2, 3, 130])))
         check_plan(T, e)
 
 
@@ -136,11 +144,11 @@ def entry_keys(src, f, lim, t, i, T, cols, colset, causal, p):
         elif kind == 2:
             ok = (j <= i) if causal else True
         elif causal:
-            w = p.get("window", 0)
-            ok = j <= i and ((w == 0 or i - j < w) or j in colset)
+            w, dl = p.get("window", 0), p.get("dilation", 1)
+            ok = j <= i and (((w == 0 or i - j < w * dl) and (i - j) % dl == 0) or j in colset)
         else:
-            r = p.get("radius", -1)
-            ok = (r < 0 or abs(i - j) <= r) or j in colset
+            r, dl = p.get("radius", -1), p.get("dilation", 1)
+            ok = ((r < 0 or abs(i - j) <= r * dl) and abs(i - j) % dl == 0) or j in colset
         if ok:
             out.append(j)
     return out
