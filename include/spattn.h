@@ -139,7 +139,10 @@ spattn_status spattn_plan_copy_columns(const spattn_plan* plan, int32_t* cols, i
 /*
  * Execution schedule the forward kernels walk, copied to HOST arrays.
  * which = 0: the bf16 tensor-core kernel (groups of 256 query rows = two 128-row
- * query tiles); which = 1: the fp32 kernel (groups of 64 rows).
+ * query tiles); which = 1: the fp32 kernel (groups of 64 rows); which = 2: the bf16
+ * kernel's schedule over the residue classes of a dilated window (used instead of 0
+ * when dilation d > 1, there are no strided or global columns and d divides T: class
+ * r holds positions r, r+d, ..., where the window is contiguous; empty otherwise).
  * items:   4 int32 per work item  {q_row0, entry_offset, entry_count, flags}
  *          flags bit 0: rows are global rows gathered from global_pos.
  * entries: 4 int32 per entry {src_row, flags, kb, lim}

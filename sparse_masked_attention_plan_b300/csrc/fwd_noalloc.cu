@@ -106,18 +106,11 @@ extern "C" spattn_status spattn_fwd_static_scratch(const spattn_plan* p, int32_t
   a.O = O;
   a.LSE = LSE;
   a.BH = static_cast<int32_t>(BH);
-  a.n_cols = p->n_cols;
   a.scale = scale;
-  a.colmask = p->d_colmask;
-  a.mask = p->mask_dev();
   a.walk = p->walk_enabled ? p->d_walk : nullptr;
   a.err = p->d_err;
   a.wait_budget_cycles = p->wait_budget_cycles;
-  const spattn::Schedule& s = p->sched[dtype == SPATTN_BF16 ? 0 : 1];
-  a.items = s.d_items;
-  a.entries = s.d_entries;
-  a.n_items = static_cast<int32_t>(s.items.size() / 4);
-  a.n_major = s.n_major;
+  spattn::select_schedule(p, dtype == SPATTN_BF16, &a);
   cudaError_t e;
   if (dtype == SPATTN_BF16) {
     const char* why = "";

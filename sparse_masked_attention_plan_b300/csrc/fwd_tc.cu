@@ -80,9 +80,11 @@ struct KParams {
   int* err;
   uint64_t budget;
   int inject_timeout;  // test hook: the MMA warp first waits on a barrier nobody signals
-  int BH;
+  int BH;        // work units along the head axis: (batch, head) x residue classes
   int n_items;
   int n_major;  // leading (longest) items launched for every head before the rest
+  int dview;    // residue classes of a dilated view (1: rows are the sequence itself)
+  int T_out;    // sequence length of O and LSE (the mask's T times dview)
 };
 
 // Descriptors are built once per operand base; a k-step only adds its byte offset
@@ -141,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       rank = p.n_major + (u - nm) % rest;
     }
   }
+  // a unit along the head axis is a (batch, head) and, in a dilated view, a residue
+  // class r: its query / key row q is sequence position q * dview + r
+  const int res = bh % p.dview;
+  bh /= p.dview;
   const int4 item = p.items[rank];
   const int n_ent = item.z;
   const int4* ents = p.entries + item.y;
@@ -185,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64,
-                      item.x + t * kTile, bh);
+          tma_load_4d(sQ + t * C::kTileBytes + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64,
+                      res, item.x + t * kTile, bh);
     }
     __syncwarp();
     int issued = 0;
@@ -212,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
-                        c * 64, e.x, bh);
+            tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
+                        c * 64, packed ? 0 : res, e.x, bh);
         }
         __syncwarp();
         ++issued;
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool write = valid && (gathered || !m.rowglobal[i]);
         const float inv = (write && lrow > 0.f) ? 1.f / lrow : 0.f;
-        const size_t row = static_cast<size_t>(bh) * m.T + i;
+        const size_t row = static_cast<size_t>(bh) * p.T_out + static_cast<size_t>(i) * p.dview + res;
         uint4* dst = reinterpret_cast<uint4*>(p.O + row * D);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -485,18 +491,22 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [BH][rows][D] bf16, boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill.
-bool make_map(CUtensorMap* map, const void* base, int D, long long rows, long long BH) {
+// [BH][rows * dview][D] bf16 seen as {D, dview, rows, BH}: element (x, r, q, bh) is
+// row q * dview + r of head bh.  Boxes of 128 rows (q) x 64 columns, one residue r,
+// 128-byte swizzle, zero fill past `rows`.  dview = 1 is the plain [BH][rows][D].
+bool make_map(CUtensorMap* map, const void* base, int D, long long rows, long long BH,
+              long long dview = 1) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   if (rows < 1) rows = 1;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                           static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(dview),
+                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[3] = {row_bytes, row_bytes * static_cast<cuuint64_t>(dview),
+                           row_bytes * static_cast<cuuint64_t>(dview) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -511,10 +521,11 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
                                     C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const long long T = a.mask.T;
+  const long long T = a.mask.T;  // rows per residue class
+  const long long dv = a.dview;
   CUtensorMap mQ, mK, mV, mQg, mKc, mVc;
-  bool ok = make_map(&mQ, a.Q, D, T, a.BH) && make_map(&mK, a.K, D, T, a.BH) &&
-            make_map(&mV, a.V, D, T, a.BH);
+  bool ok = make_map(&mQ, a.Q, D, T, a.BH, dv) && make_map(&mK, a.K, D, T, a.BH, dv) &&
+            make_map(&mV, a.V, D, T, a.BH, dv);
   ok = ok && (a.n_cols > 0 ? make_map(&mKc, a.Kc, D, a.n_cols, a.BH) && make_map(&mVc, a.Vc, D, a.n_cols, a.BH)
                            : (mKc = mK, mVc = mV, true));
   ok = ok && (a.mask.n_global > 0 ? make_map(&mQg, a.Qg, D, a.mask.n_global, a.BH) : (mQg = mQ, true));
@@ -534,10 +545,12 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
   kp.err = a.err;
   kp.budget = a.wait_budget_cycles;
   kp.inject_timeout = a.inject_timeout;
-  kp.BH = a.BH;
   kp.n_items = a.n_items;
   kp.n_major = a.n_major;
-  const long long ctas = static_cast<long long>(a.n_items) * a.BH;
+  kp.dview = static_cast<int>(dv);
+  kp.T_out = static_cast<int>(T * dv);
+  kp.BH = a.BH * static_cast<int>(dv);
+  const long long ctas = static_cast<long long>(a.n_items) * a.BH * dv;
   if (ctas > 0x7fffffffLL) {
     *why = "too many work items";
     return cudaErrorInvalidValue;

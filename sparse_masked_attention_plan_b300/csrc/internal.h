@@ -73,8 +73,15 @@ struct spattn_plan {
   uint8_t* d_rowglobal = nullptr;
   int32_t* d_gpos = nullptr;
   int32_t* d_gpos_ns = nullptr;
-  // execution schedules: [0] tensor-core bf16 kernel, [1] fp32 kernel
-  spattn::Schedule sched[2];
+  // execution schedules: [0] tensor-core bf16 kernel, [1] fp32 kernel, [2] the
+  // tensor-core kernel on the residue classes of a dilated window (when dview > 1)
+  spattn::Schedule sched[3];
+  // Dilated view: with dilation d > 1, no strided or global columns and d | T, the
+  // window is d independent contiguous windows, one per residue class r of the rows
+  // (positions r, r + d, ...); the bf16 kernel then walks sched[2] over T / d rows.
+  int32_t dview = 1;
+  uint32_t* d_colmask_res = nullptr;  // all zero: no strided / global columns
+  uint8_t* d_rowzero = nullptr;       // no global rows
   // packing scratch (packed K, V of the sparse columns and gathered global-row Q)
   void* d_scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -99,6 +106,15 @@ struct spattn_plan {
     m.gpos = d_gpos;
     m.gpos_ns = d_gpos_ns;
     m.rowglobal = d_rowglobal;
+    return m;
+  }
+
+  // The mask as the bf16 kernel sees it in the dilated view: T / d rows, contiguous.
+  spattn::MaskDev mask_dev_res() const {
+    spattn::MaskDev m = mask_dev();
+    m.T = static_cast<int32_t>(T / dview);
+    m.dilation = 1;
+    m.rowglobal = d_rowzero;
     return m;
   }
 };
@@ -150,11 +166,15 @@ struct TcArgs {
   uint64_t wait_budget_cycles;
   int32_t inject_timeout = 0;
   int32_t n_major = 0;
+  int32_t dview = 1;  // residue classes of a dilated view (mask.T is then T / dview)
 };
 cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why);
 
 // fwd_simt.cu (fp32 forward)
 cudaError_t launch_fwd_simt(int d, const TcArgs& a, cudaStream_t st);
+
+// spattn_api.cu: schedule, mask view and column data a forward launch of `dtype` uses.
+void select_schedule(const spattn_plan* p, bool bf16, TcArgs* a);
 
 // spattn_api.cu: set the calling thread's spattn_last_error() message.
 void set_last_error(const char* msg);

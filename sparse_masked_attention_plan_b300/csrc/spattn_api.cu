@@ -47,7 +47,8 @@ void free_plan_memory(spattn_plan* p) {
   void* ptrs[] = {p->d_tile_qb, p->d_tile_kb, p->d_tile_cnt, p->d_tile_cls, p->d_cols,
                   p->d_colmask, p->d_rowglobal, p->d_gpos, p->d_gpos_ns, p->d_scratch,
                   p->d_walk, p->d_err, p->sched[0].d_items, p->sched[0].d_entries,
-                  p->sched[1].d_items, p->sched[1].d_entries};
+                  p->sched[1].d_items, p->sched[1].d_entries, p->sched[2].d_items,
+                  p->sched[2].d_entries, p->d_colmask_res, p->d_rowzero};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -238,6 +239,19 @@ spattn_status check_ptr(const void* p, const char* name) {
 
 void spattn::set_last_error(const char* msg) { g_last_error = msg; }
 
+void spattn::select_schedule(const spattn_plan* p, bool bf16, TcArgs* a) {
+  const bool view = bf16 && p->dview > 1;
+  const spattn::Schedule& s = p->sched[view ? 2 : (bf16 ? 0 : 1)];
+  a->items = s.d_items;
+  a->entries = s.d_entries;
+  a->n_items = static_cast<int32_t>(s.items.size() / 4);
+  a->n_major = s.n_major;
+  a->mask = view ? p->mask_dev_res() : p->mask_dev();
+  a->colmask = view ? p->d_colmask_res : p->d_colmask;
+  a->n_cols = view ? 0 : p->n_cols;
+  a->dview = view ? p->dview : 1;
+}
+
 extern "C" {
 
 const char* spattn_last_error(void) { return g_last_error.c_str(); }
@@ -410,6 +424,24 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
   // execution schedules
   build_schedule(p, &p->sched[0], 2 * kTile, kTile, 2, true);
   build_schedule(p, &p->sched[1], 64, 64, 1, true);
+  if (p->dilation > 1 && p->stride == 0 && p->gpos.empty() && T % p->dilation == 0) {
+    // dilated view: residue class r holds rows r, r + d, ...; there the dilated
+    // window is a contiguous window of the same width over T / d rows
+    spattn_plan v;
+    v.T = T / p->dilation;
+    v.causal = p->causal;
+    v.window = p->window;
+    v.radius = p->radius;
+    v.dilation = 1;
+    build_schedule(&v, &p->sched[2], 2 * kTile, kTile, 2, true);
+    p->dview = static_cast<int32_t>(p->dilation);
+    const int64_t nkb_res = (v.T + kTile - 1) / kTile;
+    cudaError_t e = dev_alloc(&p->d_colmask_res, size_t(nkb_res) * 4);
+    if (e == cudaSuccess) e = dev_alloc(&p->d_rowzero, v.T);
+    if (e == cudaSuccess) e = cudaMemset(p->d_colmask_res, 0, size_t(nkb_res) * 16);
+    if (e == cudaSuccess) e = cudaMemset(p->d_rowzero, 0, size_t(v.T));
+    if (e != cudaSuccess) return bail(fail(SPATTN_ERR_CUDA, "plan: %s", cudaGetErrorString(e)));
+  }
   for (auto& s : p->sched) {
     spattn_status us = upload_schedule(&s);
     if (us != SPATTN_OK) return bail(us);
@@ -460,12 +492,12 @@ spattn_status spattn_plan_copy_schedule(const spattn_plan* p, int32_t which, int
                                         int64_t entry_cap, int64_t* n_entries,
                                         int64_t* tile_products) {
   if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
-  if (which != 0 && which != 1) return fail(SPATTN_ERR_SHAPE, "which must be 0 or 1");
+  if (which < 0 || which > 2) return fail(SPATTN_ERR_SHAPE, "which must be 0, 1 or 2");
   const spattn::Schedule& s = p->sched[which];
   const int64_t ni = s.items.size() / 4, ne = s.entries.size() / 4;
   if (n_items) *n_items = ni;
   if (n_entries) *n_entries = ne;
-  if (tile_products) *tile_products = s.tile_products;
+  if (tile_products) *tile_products = s.tile_products * (which == 2 ? p->dview : 1);
   if ((items && item_cap < ni) || (entries && entry_cap < ne))
     return fail(SPATTN_ERR_SHAPE, "schedule arrays too small");
   if (items && ni) std::memcpy(items, s.items.data(), size_t(ni) * 16);
@@ -542,17 +574,11 @@ spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   a.BH = static_cast<int32_t>(BH);
   a.n_cols = p->n_cols;
   a.scale = scale;
-  a.colmask = p->d_colmask;
-  a.mask = p->mask_dev();
   a.walk = p->walk_enabled ? p->d_walk : nullptr;
   a.err = p->d_err;
   a.wait_budget_cycles = p->wait_budget_cycles;
   a.inject_timeout = p->inject_timeout;
-  const spattn::Schedule& s = p->sched[dtype == SPATTN_BF16 ? 0 : 1];
-  a.items = s.d_items;
-  a.entries = s.d_entries;
-  a.n_items = static_cast<int32_t>(s.items.size() / 4);
-  a.n_major = s.n_major;
+  spattn::select_schedule(p, dtype == SPATTN_BF16, &a);
   if (dtype == SPATTN_BF16) {
     const char* why = "";
     cudaError_t e = spattn::launch_fwd_tc(p->d, a, stream, &why);

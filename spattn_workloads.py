@@ -11,6 +11,8 @@ Workload shapes follow the pages' own examples:
     Mistral-style W=4096 at a 32K context, and the 128K context it compares against.
   * "Sparse Attention" (ai360xpert.com, §Combined complexity): N=16384, W=512,
     stride 16, 128 global tokens.
+  * "Sparse and sliding-window attention" (getnybble.com, §Dilated sliding window):
+    W=512 keys with dilation 2, here at the 32K context.
 Q, K and V are i.i.d. N(0, 1) drawn in fp32 from ``torch.Generator().manual_seed``;
 bf16 inputs are the round-to-nearest-even casts of those fp32 draws.
 """
@@ -48,6 +50,9 @@ WORKLOADS = {
                               radius=-1, stride=1024, offset=0, n_global=0),
     "t8k_full_causal": dict(B=1, H=32, T=8192, d=128, causal=1, window=0, radius=-1,
                             stride=0, offset=0, n_global=0),
+    # Longformer-style dilated window: 512 keys spaced 2 apart (a 1023-token span).
+    "t32k_w512_d2": dict(B=1, H=32, T=32768, d=128, causal=1, window=512, radius=-1,
+                         stride=0, offset=0, n_global=0, dilation=2),
 }
 
 
@@ -65,7 +70,8 @@ def mask_params(name_or_cfg, seed_override=None) -> dict:
     gseed = cfg.get("global_seed", 0) if seed_override is None else seed_override
     return dict(causal=cfg["causal"], window=cfg["window"], radius=cfg["radius"],
                 stride=cfg["stride"], offset=cfg["offset"],
-                global_pos=global_positions(cfg["T"], cfg["n_global"], gseed))
+                global_pos=global_positions(cfg["T"], cfg["n_global"], gseed),
+                dilation=cfg.get("dilation", 1))
 
 
 def qkv(B: int, H: int, T: int, d: int, seed: int, dtype=torch.bfloat16):

@@ -67,6 +67,15 @@ def closed_form_pairs(T, causal, window, radius, stride, offset, gpos, dilation=
     With a dilation d > 1 the row terms are counted by brute force over each row's
     local span (still independent of oracle.c)."""
     if dilation > 1:
+        if stride == 0 and len(gpos) == 0:  # local keys only: i - k d for k in the window
+            i = np.arange(T, dtype=np.int64)
+            if causal:
+                back = i // dilation
+                return int((np.minimum(back, window - 1) + 1 if window else back + 1).sum())
+            back, fwd = i // dilation, (T - 1 - i) // dilation
+            if radius >= 0:
+                back, fwd = np.minimum(back, radius), np.minimum(fwd, radius)
+            return int((back + fwd + 1).sum())
         D = np_dense_mask(T, causal, window, radius, stride, offset, gpos, dilation)
         return int(D.sum())
     i = np.arange(T, dtype=np.int64)

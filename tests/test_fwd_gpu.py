@@ -48,7 +48,24 @@ SWEEP = [
     (1, 2, 900, 64, dict(causal=0, radius=30, dilation=4, stride=100, offset=0,
                          global_pos=[17, 600])),
     (1, 1, 513, 128, dict(causal=1, window=0, dilation=3)),
+    (1, 2, 1024, 128, dict(causal=0, radius=50, dilation=4)),
+    (2, 1, 600, 64, dict(causal=1, window=70, dilation=6)),
 ]
+
+
+@pytest.mark.parametrize("mask,T,views", [
+    (dict(causal=1, window=64, dilation=2), 1000, True),
+    (dict(causal=0, radius=50, dilation=4), 1024, True),
+    (dict(causal=1, window=64, dilation=3), 1000, False),          # 3 does not divide T
+    (dict(causal=1, window=64, dilation=2, stride=16), 1000, False),  # strided columns
+])
+def test_dilated_view_is_used_exactly_when_it_applies(mask, T, views):
+    plan = sp.Plan(T, 64, **mask)
+    items, _, products = plan.schedule(2)
+    assert (len(items) > 0) == views
+    if views:  # the residue classes partition the rows: same pair count, fewer products
+        _, _, plain = plan.schedule(0)
+        assert products <= plain
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])

@@ -21,7 +21,7 @@ def test_workload_pair_counts_closed_form(oracle_mod, name):
     m = oracle.Mask.from_params(cfg["T"], p)
     assert m.validate() == 0
     cf = closed_form_pairs(cfg["T"], p["causal"], p["window"], p["radius"], p["stride"],
-                           p["offset"], p["global_pos"])
+                           p["offset"], p["global_pos"], p["dilation"])
     assert m.count_pairs() == cf
 
 
