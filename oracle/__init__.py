@@ -54,6 +54,11 @@ def _configure(lib):
         ctypes.POINTER(ctypes.c_int64), _i64,
         ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     lib.oracle_attention_head.restype = _i64
+    lib.oracle_attention_bwd_head.argtypes = spec + [
+        _i64, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_double,
+        ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+        ctypes.POINTER(ctypes.c_double)]
+    lib.oracle_attention_bwd_head.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -188,6 +193,30 @@ def attention(mask: Mask, Q, K, V, scale: float, rows=None):
         O.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
         L.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return O, L
+
+
+def attention_bwd(mask: Mask, Q, K, V, dO, scale: float):
+    """fp64 gradients (dQ, dK, dV) [T, d] of the masked attention of one head, given
+    dO.  Inputs as for attention(): float32 arrays or uint16 bf16 bit patterns."""
+    T, d = Q.shape
+    assert T == mask.T and K.shape == (T, d) and V.shape == (T, d) and dO.shape == (T, d)
+    if Q.dtype == np.float32:
+        dt = 0
+    elif Q.dtype == np.uint16:
+        dt = 1
+    else:
+        raise TypeError("inputs must be float32 or uint16 (bf16 bits)")
+    assert K.dtype == V.dtype == dO.dtype == Q.dtype
+    Q, K, V, dO = (np.ascontiguousarray(x) for x in (Q, K, V, dO))
+    dQ = np.zeros((T, d), np.float64)
+    dK = np.zeros((T, d), np.float64)
+    dV = np.zeros((T, d), np.float64)
+    pd = ctypes.POINTER(ctypes.c_double)
+    _load().oracle_attention_bwd_head(
+        *mask._args(), int(d), dt, Q.ctypes.data, K.ctypes.data, V.ctypes.data,
+        dO.ctypes.data, float(scale), dQ.ctypes.data_as(pd), dK.ctypes.data_as(pd),
+        dV.ctypes.data_as(pd))
+    return dQ, dK, dV
 
 
 def num_threads() -> int:

@@ -426,6 +426,105 @@ def check_special_values():
     return bad
 
 
+# ---------------------------------------------------------------- gradient pins
+
+def _oracle_bwd(m, Q, K, V, dO, scale):
+    return oracle.attention_bwd(m, Q.numpy(), K.numpy(), V.numpy(), dO.numpy(), scale)
+
+
+def check_bwd_autograd(seed=21):
+    """Gradients against torch's fp64 autograd through SDPA with the independent numpy
+    boolean mask (a library routine): one dense, one causal and the sweep masks."""
+    bad = []
+    specs = [dict(T=33, causal=0, window=0, radius=-1, stride=0, offset=0, global_pos=[],
+                  dilation=1),
+             dict(T=40, causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=[],
+                  dilation=1)] + small_specs(seed, n=16)
+    for n, e in enumerate(specs):
+        T = e["T"]
+        d = 8 + 8 * (n % 2)
+        g = torch.Generator().manual_seed(300 + n)
+        Q, K, V, dO = (torch.randn(T, d, generator=g) for _ in range(4))
+        sc = 0.6 / math.sqrt(d)
+        D = torch.from_numpy(np_dense_mask(T, e["causal"], e["window"], e["radius"],
+                                           e["stride"], e["offset"], e["global_pos"],
+                                           e["dilation"]))
+        q, k, v = (x.double().requires_grad_(True) for x in (Q, K, V))
+        y = torch.nn.functional.scaled_dot_product_attention(
+            q[None, None], k[None, None], v[None, None], attn_mask=D[None, None],
+            scale=sc)[0, 0]
+        y.backward(dO.double())
+        got = _oracle_bwd(mask_of(e), Q, K, V, dO, sc)
+        for name, a, b in zip("QKV", got, (q.grad, k.grad, v.grad)):
+            if not np.allclose(a, b.numpy(), rtol=0, atol=1e-11):
+                bad.append(f"d{name} vs autograd for {e}: {np.abs(a - b.numpy()).max():.3g}")
+    return bad
+
+
+def check_bwd_finite_differences():
+    """Central differences of the forward oracle's loss L = sum(y * dO) for sampled
+    entries of Q, K and V (fp32 inputs; the step actually taken is the fp32 one)."""
+    bad = []
+    T, d = 24, 8
+    m = oracle.Mask(T, 1, 6, -1, 5, 3, [2, 17])
+    g = torch.Generator().manual_seed(41)
+    X = [torch.randn(T, d, generator=g) for _ in range(3)]
+    dO = torch.randn(T, d, generator=g)
+    sc = 0.5
+    grads = _oracle_bwd(m, *X, dO, sc)
+    W = dO.double().numpy()
+
+    def loss(Xs):
+        O, _ = oracle.attention(m, *(x.numpy() for x in Xs), sc)
+        return float((O * W).sum())
+
+    rng = np.random.default_rng(7)
+    for which in range(3):
+        for _ in range(12):
+            i, k = int(rng.integers(T)), int(rng.integers(d))
+            base = X[which][i, k].item()
+            hp = np.float32(base + 1e-2)
+            hm = np.float32(base - 1e-2)
+            Xp = [x.clone() for x in X]
+            Xm = [x.clone() for x in X]
+            Xp[which][i, k] = float(hp)
+            Xm[which][i, k] = float(hm)
+            fd = (loss(Xp) - loss(Xm)) / (float(hp) - float(hm))
+            if not math.isclose(fd, grads[which][i, k], rel_tol=1e-3, abs_tol=1e-5):
+                bad.append(f"d{'QKV'[which]}[{i},{k}] = {grads[which][i, k]:.6g}, "
+                           f"central difference {fd:.6g}")
+    return bad
+
+
+def check_bwd_invariants():
+    """Identities of the softmax over S_i: sum_j dV_j = sum_i dO_i (weights sum to 1);
+    sum_j dK_j = 0 (each row's ds sums to 0); with w = 1 (S_i = {i}) dV = dO and
+    dQ = dK = 0; with Q = 0 and dO = 0 everything is 0."""
+    bad = []
+    for e in small_specs(33, n=10):
+        T = e["T"]
+        d = 8
+        g = torch.Generator().manual_seed(500 + T)
+        Q, K, V, dO = (torch.randn(T, d, generator=g) for _ in range(4))
+        dQ, dK, dV = _oracle_bwd(mask_of(e), Q, K, V, dO, 0.4)
+        if not np.allclose(dV.sum(0), dO.double().numpy().sum(0), rtol=0, atol=1e-10):
+            bad.append(f"sum dV != sum dO for {e}")
+        if not np.allclose(dK.sum(0), 0.0, rtol=0, atol=1e-10):
+            bad.append(f"sum dK != 0 for {e}")
+    T, d = 30, 8
+    g = torch.Generator().manual_seed(77)
+    Q, K, V, dO = (torch.randn(T, d, generator=g) for _ in range(4))
+    dQ, dK, dV = _oracle_bwd(oracle.Mask(T, 1, 1), Q, K, V, dO, 0.4)
+    if not (np.array_equal(dV, dO.double().numpy()) and not dQ.any() and not dK.any()):
+        bad.append("w=1 gradients")
+    dQ, dK, dV = _oracle_bwd(oracle.Mask(T, 0, 0, 4), Q, K, V, torch.zeros(T, d), 0.4)
+    if dQ.any() or dK.any() or dV.any():
+        bad.append("dO = 0 gives nonzero gradients")
+    return bad
+
+
+BWD_CHECKS = [check_bwd_autograd, check_bwd_finite_differences, check_bwd_invariants]
+
 COUNT_CHECKS = [check_page_counts, check_row_sets, check_reach, check_edge_formula,
                 check_dilated_counts, check_causal_equivalences, check_against_numpy_rules,
                 check_rejects_invalid]

@@ -11,7 +11,7 @@ import subprocess
 import pytest
 
 import oracle
-from pins import ATTENTION_CHECKS, COUNT_CHECKS
+from pins import ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -35,6 +35,46 @@ MUTANTS = {
     "key_transposed": ("load_elem(K, dtype, j * d + k)", "load_elem(K, dtype, k * d + j % d)"),
     "first_key_skipped": ("for (int64_t a = 0; a < n; a++) l +=", "for (int64_t a = 1; a < n; a++) l +="),
 }
+
+# Slips in the gradient function, checked against the gradient pins only.
+BWD_MUTANTS = {
+    "bwd_softmax_jacobian_no_D": ("const double ds = a[t] * (da[t] - D);",
+                                  "const double ds = a[t] * da[t];"),
+    "bwd_D_unweighted": ("D += a[t] * acc;", "D += acc;"),
+    "bwd_dV_unweighted": ("dV[j * d + k] += a[t] * load_elem(dO",
+                          "dV[j * d + k] += load_elem(dO"),
+    "bwd_dQ_no_scale": ("dQ[i * d + k] += scale * ds", "dQ[i * d + k] += ds"),
+    "bwd_dK_uses_key": ("dK[j * d + k] += scale * ds * load_elem(Q, dtype, i * d + k);",
+                        "dK[j * d + k] += scale * ds * load_elem(K, dtype, i * d + k);"),
+    "bwd_dalpha_uses_key": ("acc += load_elem(dO, dtype, i * d + k) * load_elem(V, dtype, set[t] * d + k);",
+                            "acc += load_elem(dO, dtype, i * d + k) * load_elem(K, dtype, set[t] * d + k);"),
+    "bwd_logit_unscaled": ("      a[t] = scale * acc;\n      if (a[t] > mx)",
+                           "      a[t] = acc;\n      if (a[t] > mx)"),
+    "bwd_dV_to_query_row": ("dV[j * d + k] +=", "dV[i * d + k] +="),
+}
+
+
+def _build_mutant(tmp_path, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site not found: {old!r}"
+    c = tmp_path / "mut.c"
+    so = tmp_path / "libmut.so"
+    c.write_text(src.replace(old, new))
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                           str(c), "-lm"])
+    return str(so)
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_gradient_mutant_is_caught(oracle_mod, tmp_path, name):
+    so = _build_mutant(tmp_path, *BWD_MUTANTS[name])
+    failures = []
+    with oracle.use_library(so):
+        for check in BWD_CHECKS:
+            failures += check()
+            if failures:
+                break
+    assert failures, f"mutant {name} passed every gradient pin"
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
