@@ -39,9 +39,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the tensor-core forward kernel on the
 # 32K / W=4096 workload, from the ncu capture summarised in
-# profiles/fwd_tc_t32k_w4096.md (captured with H=8, 250.8 MB, scaled by 32/8 heads),
+# profiles/fwd_tc_t32k_w4096.md (captured with H=8, 251.0 MB, scaled by 32/8 heads),
 # valid only for the kernel source with this hash; any other source reports null.
-TRAFFIC = {"kernel_sha": "990f6a680e699149", "bytes_per_launch": 1003.1e6, "workload": "t32k_w4096"}
+TRAFFIC = {"kernel_sha": "a7b8bfe485cc9f3d", "bytes_per_launch": 1004.0e6, "workload": "t32k_w4096"}
 
 
 def kernel_sha() -> str:
@@ -167,8 +167,7 @@ def oracle_sample_rate(cfg, p, Q, K, V, budget_s: float, seed: int = 0):
     import oracle
     oracle.build()
     T, d = cfg["T"], cfg["d"]
-    m = oracle.Mask(T, p["causal"], p["window"], p["radius"], p["stride"], p["offset"],
-                    p["global_pos"])
+    m = oracle.Mask.from_params(T, p)
     q, k, v = (oracle.bf16_bits(x[0, 0]) for x in (Q, K, V))
     scale = 1.0 / math.sqrt(d)
     # calibrate on growing row counts, then size the sample to the budget
@@ -201,8 +200,7 @@ def run_reference(args, cfg, p):
     g = torch.Generator().manual_seed(0)
     # one head's inputs are all the oracle sample touches
     Q, K, V = (torch.randn(1, 1, T, d, generator=g).to(torch.bfloat16) for _ in range(3))
-    m = oracle.Mask(T, p["causal"], p["window"], p["radius"], p["stride"], p["offset"],
-                    p["global_pos"])
+    m = oracle.Mask.from_params(T, p)
     q, k, v = (oracle.bf16_bits(x[0, 0]) for x in (Q, K, V))
     scale = 1.0 / math.sqrt(d)
     step_budget = 2.0
@@ -358,6 +356,90 @@ def run_ours(args, cfg, p):
     return 0
 
 
+# ----------------------------------------------------------------- backward arm
+
+BWD_METRIC = "allowed-pair backward TFLOP/s (10·d·pairs/s), 1 GPU"
+# FP32 FMA peak of the backward's SIMT kernels: 148 SMs x 128 FP32 lanes x 2 flops
+# at the 2032 MHz maximum SM clock.
+FP32_FMA_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def run_ours_bwd(args, cfg, p):
+    """One step = one spattn_bwd over the whole batch (dQ, dK, dV of every head) with
+    q, k, v, O, LSE and dO resident in HBM.  value = 10 d B H pairs / t_step: per
+    allowed pair 2d flops each for the recomputed logit, dO.v, and the dV, dK and dQ
+    updates (the kernels execute 14 d: the query-major dQ pass recomputes the logit
+    and dO.v)."""
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    import sparse_masked_attention_plan_b300 as sp
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    Qh, Kh, Vh = W.qkv(B, H, T, d, seed=rank, dtype=torch.bfloat16)
+    dOh = W.grad_out(B, H, T, d, seed=rank, dtype=torch.bfloat16)
+    with torch.cuda.stream(stream):
+        q, k, v, do = (x.to(dev) for x in (Qh, Kh, Vh, dOh))
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    plan = sp.Plan(T, d, **p, stream=stream)
+    o, lse = sp.fwd(plan, q, k, v, scale, stream=stream)
+    stream.synchronize()
+    info = plan.info()
+    pairs_total = info["pairs_per_head"] * B * H
+    flops_step = 10.0 * d * pairs_total
+    n_packed_units = int((plan.schedule(3)[0][:, 3] & 1).sum())
+
+    def step():
+        sp.bwd(plan, q, k, v, o, lse, do, scale, dq, dk, dv, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for s in range(args.steps):
+            step()
+            ev[s + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    plan.check_device(stream)
+    per = [ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps)]
+    ms_per_step, value = aggregate(ev[0].elapsed_time(ev[-1]), args.steps, flops_step, world)
+    if rank == 0:
+        step_ms = statistics.mean(per)
+        achieved = flops_step / (step_ms / 1e3) / 1e12
+        line = {
+            "metric": BWD_METRIC, "pass": "bwd", "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in/out, fp32 arithmetic", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d,
+                       "mask": mask_desc(p), "pairs_per_head": info["pairs_per_head"],
+                       "l2": "inputs larger than L2" if 6 * q.numel() * 2 > 126e6
+                             else "inputs fit in L2"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_FMA_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / FP32_FMA_PEAK_TFLOPS,
+                         "traffic": None,
+                         "peak_source": "derived: 148 SMs x 128 FP32 FMA lanes x 2 x 2032 MHz",
+                         "kernel": "rowdot + dq + dkdv (whole step)",
+                         "kernel_ms": step_ms},
+            "e2e": None,
+            "gpu_launches": (3 + (1 if n_packed_units else 0)) * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,6 +450,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="time the forward (default, the headline) or the backward pass")
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (smaller profiling captures; the line then names it)")
     args = ap.parse_args()
@@ -379,6 +463,8 @@ def main():
     p = W.mask_params(args.workload)
     if args.impl == "reference":
         return run_reference(args, cfg, p)
+    if args.which == "bwd":
+        return run_ours_bwd(args, cfg, p)
     return run_ours(args, cfg, p)
 
 

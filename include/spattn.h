@@ -150,10 +150,18 @@ spattn_status spattn_plan_copy_columns(const spattn_plan* plan, int32_t* cols, i
  *          bits 2/3: the tile needs no predicate for query tile 0/1,
  *          bits 4-5: kind (0 band tile of the natural grid, 1 packed sparse
  *          columns [src_row, lim) of C, 2 dense causal walk for global rows).
+ * which = 3: the key-major schedule of spattn_bwd's dK/dV pass.  Its "items" are
+ *          64-key units {key0, entry_offset, entry_count, flags}; flags bit 0: the
+ *          unit is packed sparse columns C[key0 .. key0+63] (these come first),
+ *          else natural keys key0 .. key0+63.  Its entries are 64-row query groups
+ *          {q0, flags, a, b}: flags bits 4-5 kind as above, bit 0: q0 indexes
+ *          global_pos (rows gathered from the global list); a packed entry reads
+ *          packed columns [a, b) of its unit.  Rows that are global tokens take
+ *          part only in gathered entries.
  * *n_items / *n_entries receive the sizes; arrays shorter than that are an
  * error (SPATTN_ERR_SHAPE) and nothing is written.  items/entries may be NULL to
  * query the sizes.  *tile_products receives the number of (query tile, key tile)
- * products one (batch, head) computes.
+ * products one (batch, head) computes (which = 3: the number of entries).
  */
 spattn_status spattn_plan_copy_schedule(const spattn_plan* plan, int32_t which, int32_t* items,
                                         int64_t item_cap, int64_t* n_items, int32_t* entries,
@@ -182,6 +190,29 @@ spattn_status spattn_plan_walk_count(const spattn_plan* plan, int64_t* count);
 spattn_status spattn_fwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_dtype dtype,
                          const void* Q, const void* K, const void* V, float scale, void* O,
                          float* LSE, void* cuda_stream);
+
+/*
+ * Backward pass (gradients) on device buffers, asynchronous on `cuda_stream`.
+ * Given the forward's inputs Q, K, V, its output O and log-sum-exp LSE (as written
+ * by spattn_fwd with the same plan, dtype and scale) and the gradient dO of a loss
+ * with respect to O, writes dQ, dK, dV: the chain rule through the softmax over the
+ * allowed set S_i ("Sparse attention" glossary, section "Choose the available
+ * reads", differentiated):
+ *   alpha_ij = exp(scale q_i.k_j - LSE_i),  D_i = dO_i . O_i,
+ *   ds_ij = alpha_ij (dO_i . v_j - D_i)  for j in S_i (0 elsewhere),
+ *   dQ_i = scale sum_j ds_ij k_j,  dK_j = scale sum_i ds_ij q_i,  dV_j = sum_i alpha_ij dO_i.
+ * Q, K, V, O, dO, dQ, dK, dV: [B, H, T, d] of `dtype`, contiguous, 16-byte aligned;
+ * LSE: [B, H, T] fp32 (required).  dQ, dK, dV are overwritten (every row is
+ * written; nothing needs zeroing).  All products and sums run in fp32 on FP32 FMA
+ * units with no atomics, so the result is the same on every call; bf16 outputs
+ * are rounded once, to nearest even.  The first call for a given B*H may allocate
+ * the plan's backward scratch (row dots and packed-column partial sums).
+ * Errors: NULL, SHAPE, DTYPE, ALIGN, INVALID_SPEC (scale), CUDA.
+ */
+spattn_status spattn_bwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_dtype dtype,
+                         const void* Q, const void* K, const void* V, const void* O,
+                         const float* LSE, const void* dO, float scale, void* dQ, void* dK,
+                         void* dV, void* cuda_stream);
 
 /*
  * The same forward pass from HOST buffers: copies Q/K/V host -> device, runs

@@ -59,6 +59,10 @@ def _configure(lib):
         ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
         ctypes.POINTER(ctypes.c_double)]
     lib.oracle_attention_bwd_head.restype = None
+    lib.oracle_attention_bwd_dq_rows.argtypes = spec + [
+        _i64, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_double, _vp, _i64,
+        ctypes.POINTER(ctypes.c_double)]
+    lib.oracle_attention_bwd_dq_rows.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -217,6 +221,22 @@ def attention_bwd(mask: Mask, Q, K, V, dO, scale: float):
         dO.ctypes.data, float(scale), dQ.ctypes.data_as(pd), dK.ctypes.data_as(pd),
         dV.ctypes.data_as(pd))
     return dQ, dK, dV
+
+
+def attention_bwd_dq(mask: Mask, Q, K, V, dO, scale: float, rows):
+    """fp64 dQ [len(rows), d] of the listed rows only (each needs only its own set)."""
+    T, d = Q.shape
+    assert T == mask.T
+    dt = 0 if Q.dtype == np.float32 else 1
+    Q, K, V, dO = (np.ascontiguousarray(x) for x in (Q, K, V, dO))
+    rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert rr.size == 0 or (rr.min() >= 0 and rr.max() < T)
+    out = np.zeros((rr.size, d), np.float64)
+    _load().oracle_attention_bwd_dq_rows(
+        *mask._args(), int(d), dt, Q.ctypes.data, K.ctypes.data, V.ctypes.data,
+        dO.ctypes.data, float(scale), rr.ctypes.data, int(rr.size),
+        out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
 
 
 def num_threads() -> int:

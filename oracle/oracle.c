@@ -290,6 +290,53 @@ int64_t oracle_attention_head(int causal, int64_t window, int64_t radius, int64_
  * Every row is recomputed from its definition in fp64 (no saved forward state).
  * Q, K, V, dO: [T][d], dtype 0 = fp32, 1 = bf16 bits.  dQ, dK, dV: [T][d] fp64,
  * overwritten.  Sequential over rows (dK and dV gather from every row). */
+/* One row i of the gradient: recomputes alpha_ij over S_i, adds row i's share to
+ * dK and dV (when they are not NULL) and writes dQ_i to dq_row.  set, a, da: [T]. */
+static void bwd_row(const omask* m, int64_t i, int64_t d, int dtype, const void* Q,
+                    const void* K, const void* V, const void* dO, double scale, double* dq_row,
+                    double* dK, double* dV, int32_t* set, double* a, double* da) {
+  const int64_t n = row_set_union(m, i, set);
+  double mx = -INFINITY;
+  for (int64_t t = 0; t < n; t++) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < d; k++)
+      acc += load_elem(Q, dtype, i * d + k) * load_elem(K, dtype, set[t] * d + k);
+    a[t] = scale * acc;
+    if (a[t] > mx) mx = a[t];
+  }
+  double l = 0.0;
+  for (int64_t t = 0; t < n; t++) l += exp(a[t] - mx);
+  double D = 0.0;
+  for (int64_t t = 0; t < n; t++) {
+    a[t] = exp(a[t] - mx) / l; /* alpha_ij */
+    double acc = 0.0;
+    for (int64_t k = 0; k < d; k++)
+      acc += load_elem(dO, dtype, i * d + k) * load_elem(V, dtype, set[t] * d + k);
+    da[t] = acc;
+    D += a[t] * acc;
+  }
+  for (int64_t k = 0; k < d; k++) dq_row[k] = 0.0;
+  for (int64_t t = 0; t < n; t++) {
+    const int64_t j = set[t];
+    const double ds = a[t] * (da[t] - D);
+    for (int64_t k = 0; k < d; k++) {
+      dq_row[k] += scale * ds * load_elem(K, dtype, j * d + k);
+      if (dV) dV[j * d + k] += a[t] * load_elem(dO, dtype, i * d + k);
+      if (dK) dK[j * d + k] += scale * ds * load_elem(Q, dtype, i * d + k);
+    }
+  }
+}
+
+/* One head: given dO (the gradient of a loss with respect to y), the gradients with
+ * respect to Q, K and V of y_i = sum_{j in S_i} alpha_ij v_j, alpha_ij =
+ * softmax_{j in S_i}(scale q_i . k_j).  By the chain rule through the softmax over S_i:
+ *   dV_j = sum_{i : j in S_i} alpha_ij dO_i
+ *   dalpha_ij = dO_i . v_j,   D_i = sum_{j in S_i} alpha_ij dalpha_ij  (= dO_i . y_i)
+ *   ds_ij = alpha_ij (dalpha_ij - D_i)            (softmax Jacobian over S_i)
+ *   dQ_i = scale sum_{j in S_i} ds_ij k_j,   dK_j = scale sum_{i : j in S_i} ds_ij q_i
+ * Every row is recomputed from its definition in fp64 (no saved forward state).
+ * Q, K, V, dO: [T][d], dtype 0 = fp32, 1 = bf16 bits.  dQ, dK, dV: [T][d] fp64,
+ * overwritten.  Sequential over rows (dK and dV gather from every row). */
 void oracle_attention_bwd_head(int causal, int64_t window, int64_t radius, int64_t dilation,
                                int64_t stride, int64_t offset, int64_t n_global,
                                const int32_t* gpos, int64_t T, int64_t d, int dtype,
@@ -299,43 +346,38 @@ void oracle_attention_bwd_head(int causal, int64_t window, int64_t radius, int64
   int32_t* set = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
   double* a = (double*)malloc(sizeof(double) * (size_t)T);
   double* da = (double*)malloc(sizeof(double) * (size_t)T);
-  memset(dQ, 0, sizeof(double) * (size_t)(T * d));
   memset(dK, 0, sizeof(double) * (size_t)(T * d));
   memset(dV, 0, sizeof(double) * (size_t)(T * d));
-  for (int64_t i = 0; i < T; i++) {
-    const int64_t n = row_set_union(&m, i, set);
-    double mx = -INFINITY;
-    for (int64_t t = 0; t < n; t++) {
-      double acc = 0.0;
-      for (int64_t k = 0; k < d; k++)
-        acc += load_elem(Q, dtype, i * d + k) * load_elem(K, dtype, set[t] * d + k);
-      a[t] = scale * acc;
-      if (a[t] > mx) mx = a[t];
-    }
-    double l = 0.0;
-    for (int64_t t = 0; t < n; t++) l += exp(a[t] - mx);
-    double D = 0.0;
-    for (int64_t t = 0; t < n; t++) {
-      a[t] = exp(a[t] - mx) / l; /* alpha_ij */
-      double acc = 0.0;
-      for (int64_t k = 0; k < d; k++)
-        acc += load_elem(dO, dtype, i * d + k) * load_elem(V, dtype, set[t] * d + k);
-      da[t] = acc;
-      D += a[t] * acc;
-    }
-    for (int64_t t = 0; t < n; t++) {
-      const int64_t j = set[t];
-      const double ds = a[t] * (da[t] - D);
-      for (int64_t k = 0; k < d; k++) {
-        dV[j * d + k] += a[t] * load_elem(dO, dtype, i * d + k);
-        dQ[i * d + k] += scale * ds * load_elem(K, dtype, j * d + k);
-        dK[j * d + k] += scale * ds * load_elem(Q, dtype, i * d + k);
-      }
-    }
-  }
+  for (int64_t i = 0; i < T; i++)
+    bwd_row(&m, i, d, dtype, Q, K, V, dO, scale, dQ + i * d, dK, dV, set, a, da);
   free(set);
   free(a);
   free(da);
+}
+
+/* dQ alone for the listed rows (each row's dQ needs only its own set):
+ * dQ_rows[r][d] = dQ of row rows[r].  Rows are independent, so they run in
+ * parallel. */
+void oracle_attention_bwd_dq_rows(int causal, int64_t window, int64_t radius, int64_t dilation,
+                                  int64_t stride, int64_t offset, int64_t n_global,
+                                  const int32_t* gpos, int64_t T, int64_t d, int dtype,
+                                  const void* Q, const void* K, const void* V, const void* dO,
+                                  double scale, const int64_t* rows, int64_t n_rows,
+                                  double* dQ_rows) {
+  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+#pragma omp parallel
+  {
+    int32_t* set = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+    double* a = (double*)malloc(sizeof(double) * (size_t)T);
+    double* da = (double*)malloc(sizeof(double) * (size_t)T);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; r++)
+      bwd_row(&m, rows[r], d, dtype, Q, K, V, dO, scale, dQ_rows + r * d, NULL, NULL, set, a,
+              da);
+    free(set);
+    free(a);
+    free(da);
+  }
 }
 
 /* Number of OpenMP threads the oracle uses (1 when built without OpenMP). */

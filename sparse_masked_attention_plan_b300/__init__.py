@@ -28,7 +28,7 @@ BF16, FP32 = 0, 1
 EXPORTS = ("spattn_mask_validate", "spattn_plan_create", "spattn_plan_info",
            "spattn_plan_copy_tiles", "spattn_plan_copy_columns", "spattn_plan_copy_schedule",
            "spattn_plan_set_walk_counter", "spattn_plan_walk_count", "spattn_fwd",
-           "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
+           "spattn_bwd", "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
            "spattn_plan_test_wait_timeout", "spattn_plan_check_device", "spattn_plan_destroy",
            "spattn_last_error", "spattn_version")
 
@@ -81,6 +81,9 @@ def lib():
                                           _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]
             L.spattn_fwd_static_scratch.argtypes = L.spattn_fwd.argtypes
+            L.spattn_bwd.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, _vp,
+                                     _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
+                                     _vp]
             L.spattn_plan_set_wait_budget.argtypes = [_vp, ctypes.c_uint64]
             L.spattn_plan_test_wait_timeout.argtypes = [_vp, ctypes.c_int32]
             L.spattn_plan_check_device.argtypes = [_vp, _vp]
@@ -242,6 +245,31 @@ def fwd(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None, want
                             lse.data_ptr() if lse is not None else None,
                             _stream_handle(stream)))
     return out, lse
+
+
+def bwd(plan: Plan, q, k, v, o, lse, do, scale: float, dq=None, dk=None, dv=None,
+        stream=None):
+    """Gradients (dQ, dK, dV) of the masked attention given dO, from the forward's
+    inputs q, k, v, its output o and LSE (all [B, H, T, d] / [B, H, T] CUDA tensors,
+    contiguous, o and do of q's dtype).  Asynchronous on `stream`."""
+    import torch
+    B, H, T, d = q.shape
+    for t in (q, k, v, o, do):
+        if (not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, H, T, d)
+                or t.dtype != q.dtype):
+            raise ValueError("q, k, v, o, do must be contiguous CUDA tensors of equal shape "
+                             "and dtype")
+    if (not lse.is_cuda or not lse.is_contiguous() or lse.dtype != torch.float32
+            or tuple(lse.shape) != (B, H, T)):
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, H, T]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _check(lib().spattn_bwd(plan.handle, B, H, _dtype_code(q), q.data_ptr(), k.data_ptr(),
+                            v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                            float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def fwd_static_scratch(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None):

@@ -16,6 +16,15 @@ constexpr int kKindShift = 4;
 constexpr int kKindBand = 0, kKindPacked = 1, kKindDense = 2;
 constexpr int kItemGathered = 1;
 
+// Key-major (backward) schedule: a unit is 64 consecutive keys, either natural key
+// rows (k0 .. k0+63) or packed sparse columns (C[c0] .. C[c0+63]); its entries are
+// 64-row query groups {q0, flags, a, b} with the entry kind in the same bits as above
+// and kEntryGathered set when q0 indexes the global rows.  Packed entries read packed
+// columns [a, b) of the unit.
+constexpr int kBwdRows = 64, kBwdKeys = 64;
+constexpr int kUnitPacked = 1;
+constexpr int kEntryGathered = 1;
+
 // Device error word bits.
 constexpr int kErrTimeout = 1;
 
@@ -45,6 +54,7 @@ struct Schedule {
   int4* d_entries = nullptr;
   int64_t tile_products = 0;  // (query tile x key tile) products per (batch, head)
   int32_t n_major = 0;        // leading items (>= 1.5x the median length) launched first
+  int32_t n_packed_units = 0;  // key-major schedule: packed units come first
 };
 
 }  // namespace spattn
@@ -82,9 +92,16 @@ struct spattn_plan {
   int32_t dview = 1;
   uint32_t* d_colmask_res = nullptr;  // all zero: no strided / global columns
   uint8_t* d_rowzero = nullptr;       // no global rows
+  // key-major schedule of the backward pass and the packed index of every key
+  // (-1 where the key is not a sparse column)
+  spattn::Schedule bsched;
+  int32_t* d_colidx = nullptr;
   // packing scratch (packed K, V of the sparse columns and gathered global-row Q)
   void* d_scratch = nullptr;
   size_t scratch_bytes = 0;
+  // backward scratch: row dots D_i [BH][T] and packed-column dK, dV [BH][|C|][d], fp32
+  void* d_bscratch = nullptr;
+  size_t bscratch_bytes = 0;
   // debug walk counter and device error word
   unsigned long long* d_walk = nullptr;
   int32_t walk_enabled = 0;
@@ -172,6 +189,40 @@ cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** 
 
 // fwd_simt.cu (fp32 forward)
 cudaError_t launch_fwd_simt(int d, const TcArgs& a, cudaStream_t st);
+
+// bwd_simt.cu (backward on the FP32 FMA units, bf16 or fp32 inputs)
+struct BwdArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* O;
+  const float* LSE;
+  const void* dO;
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* Dvec;    // [BH][T] scratch
+  float* dKc;     // [BH][n_cols][d] scratch
+  float* dVc;
+  int32_t BH;
+  int32_t n_cols;
+  float scale;
+  int32_t bf16;
+  const int32_t* cols;
+  const int32_t* colidx;
+  const uint32_t* colmask;
+  MaskDev mask;
+  // query-major walk (dQ): the fp32 forward schedule
+  const int4* q_items;
+  const int4* q_entries;
+  int32_t n_q_items;
+  // key-major walk (dK, dV)
+  const int4* units;
+  const int4* u_entries;
+  int32_t n_packed_units;
+  int32_t n_units;
+};
+cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st);
 
 // spattn_api.cu: schedule, mask view and column data a forward launch of `dtype` uses.
 void select_schedule(const spattn_plan* p, bool bf16, TcArgs* a);

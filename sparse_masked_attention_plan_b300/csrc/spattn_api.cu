@@ -48,7 +48,8 @@ void free_plan_memory(spattn_plan* p) {
                   p->d_colmask, p->d_rowglobal, p->d_gpos, p->d_gpos_ns, p->d_scratch,
                   p->d_walk, p->d_err, p->sched[0].d_items, p->sched[0].d_entries,
                   p->sched[1].d_items, p->sched[1].d_entries, p->sched[2].d_items,
-                  p->sched[2].d_entries, p->d_colmask_res, p->d_rowzero};
+                  p->sched[2].d_entries, p->d_colmask_res, p->d_rowzero,
+                  p->bsched.d_items, p->bsched.d_entries, p->d_colidx, p->d_bscratch};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -216,6 +217,76 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
            2 * items[s->n_major].cnt >= 3 * median && items[s->n_major].cnt > median)
       ++s->n_major;
   }
+}
+
+// Key-major schedule of the backward pass: the same decomposition of every row's
+// allowed set as the forward schedule with 64-row groups (band keys of the natural
+// grid inside the group's band range, packed sparse columns outside it, dense walks
+// for global rows), listed per 64-key unit instead of per query group, so that the
+// gradient of every key is summed inside one CTA.
+void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s) {
+  using namespace spattn;
+  Sched h{p};
+  const int64_t T = p->T;
+  const int64_t nc = p->n_cols;
+  const int64_t nu_nat = (T + kBwdKeys - 1) / kBwdKeys, nu_pk = (nc + kBwdKeys - 1) / kBwdKeys;
+  std::vector<std::vector<int32_t>> nat(nu_nat), pk(nu_pk);
+  auto add = [](std::vector<int32_t>& v, int64_t q0, int32_t flags, int64_t a, int64_t b) {
+    v.insert(v.end(), {static_cast<int32_t>(q0), flags, static_cast<int32_t>(a),
+                       static_cast<int32_t>(b)});
+  };
+  const int64_t d = p->dilation;
+  for (int64_t r0 = 0; r0 < T; r0 += kBwdRows) {
+    const int64_t r1 = std::min<int64_t>(r0 + kBwdRows, T) - 1;
+    int64_t jlo, jhi;
+    if (p->causal) {
+      jlo = p->window ? std::max<int64_t>(0, r0 - (p->window - 1) * d) : 0;
+      jhi = r1;
+    } else {
+      jlo = p->radius >= 0 ? std::max<int64_t>(0, r0 - p->radius * d) : 0;
+      jhi = p->radius >= 0 ? std::min<int64_t>(T - 1, r1 + p->radius * d) : T - 1;
+    }
+    const int64_t kb_lo = jlo / kTile, kb_hi = jhi / kTile;
+    const int64_t u_hi = std::min<int64_t>(nu_nat - 1, (kb_hi + 1) * (kTile / kBwdKeys) - 1);
+    for (int64_t u = kb_lo * (kTile / kBwdKeys); u <= u_hi; ++u) {
+      const int64_t k0 = u * kBwdKeys, k1 = std::min<int64_t>(k0 + kBwdKeys, T) - 1;
+      if (h.local_meets(r0, r1, k0, k1) || h.cols_in(k0, p->causal ? std::min(k1, r1) : k1))
+        add(nat[u], r0, kKindBand << kKindShift, 0, 0);
+    }
+    if (nc > 0) {
+      const int64_t a_idx = h.lower(kb_lo * kTile), b_idx = h.lower((kb_hi + 1) * kTile);
+      const int64_t e_idx = p->causal ? h.upper(r1) : nc;
+      const int64_t ranges[2][2] = {{0, std::min(a_idx, e_idx)}, {b_idx, e_idx}};
+      for (auto& rg : ranges)
+        for (int64_t u = rg[0] / kBwdKeys; rg[0] < rg[1] && u <= (rg[1] - 1) / kBwdKeys; ++u)
+          add(pk[u], r0, kKindPacked << kKindShift, std::max(rg[0], u * kBwdKeys),
+              std::min(rg[1], (u + 1) * kBwdKeys));
+    }
+  }
+  const int64_t ng = static_cast<int64_t>(p->gpos.size());
+  for (int64_t q0 = 0; q0 < ng; q0 += kBwdRows) {
+    const int64_t last = p->gpos[std::min<int64_t>(q0 + kBwdRows, ng) - 1];
+    const int64_t u_hi = (p->causal ? last : T - 1) / kBwdKeys;
+    for (int64_t u = 0; u <= u_hi; ++u)
+      add(nat[u], q0, (kKindDense << kKindShift) | kEntryGathered, 0, 0);
+  }
+  s->group_rows = kBwdRows;
+  s->qtile_rows = kBwdRows;
+  s->n_qtiles = 1;
+  s->items.clear();
+  s->entries.clear();
+  s->tile_products = 0;
+  s->n_major = 0;
+  s->n_packed_units = static_cast<int32_t>(nu_pk);
+  auto emit = [&](std::vector<int32_t>& v, int64_t key0, int32_t flags) {
+    const int32_t off = static_cast<int32_t>(s->entries.size() / 4);
+    const int32_t cnt = static_cast<int32_t>(v.size() / 4);
+    s->items.insert(s->items.end(), {static_cast<int32_t>(key0), off, cnt, flags});
+    s->entries.insert(s->entries.end(), v.begin(), v.end());
+    s->tile_products += cnt;
+  };
+  for (int64_t u = 0; u < nu_pk; ++u) emit(pk[u], u * kBwdKeys, kUnitPacked);
+  for (int64_t u = 0; u < nu_nat; ++u) emit(nat[u], u * kBwdKeys, 0);
 }
 
 spattn_status upload_schedule(spattn::Schedule* s) {
@@ -442,9 +513,20 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
     if (e == cudaSuccess) e = cudaMemset(p->d_rowzero, 0, size_t(v.T));
     if (e != cudaSuccess) return bail(fail(SPATTN_ERR_CUDA, "plan: %s", cudaGetErrorString(e)));
   }
+  build_bwd_schedule(p, &p->bsched);
   for (auto& s : p->sched) {
     spattn_status us = upload_schedule(&s);
     if (us != SPATTN_OK) return bail(us);
+  }
+  {
+    spattn_status us = upload_schedule(&p->bsched);
+    if (us != SPATTN_OK) return bail(us);
+    std::vector<int32_t> colidx(size_t(T), -1);
+    for (int32_t c = 0; c < p->n_cols; ++c) colidx[p->cols[c]] = c;
+    cudaError_t e = dev_alloc(&p->d_colidx, size_t(T));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(p->d_colidx, colidx.data(), size_t(T) * 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return bail(fail(SPATTN_ERR_CUDA, "plan: %s", cudaGetErrorString(e)));
   }
   *out = p;
   return SPATTN_OK;
@@ -492,8 +574,8 @@ spattn_status spattn_plan_copy_schedule(const spattn_plan* p, int32_t which, int
                                         int64_t entry_cap, int64_t* n_entries,
                                         int64_t* tile_products) {
   if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
-  if (which < 0 || which > 2) return fail(SPATTN_ERR_SHAPE, "which must be 0, 1 or 2");
-  const spattn::Schedule& s = p->sched[which];
+  if (which < 0 || which > 3) return fail(SPATTN_ERR_SHAPE, "which must be 0, 1, 2 or 3");
+  const spattn::Schedule& s = which == 3 ? p->bsched : p->sched[which];
   const int64_t ni = s.items.size() / 4, ne = s.entries.size() / 4;
   if (n_items) *n_items = ni;
   if (n_entries) *n_entries = ne;
@@ -588,6 +670,71 @@ spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
     cudaError_t e = spattn::launch_fwd_simt(p->d, a, stream);
     if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "fp32 forward launch: %s", cudaGetErrorString(e));
   }
+  return SPATTN_OK;
+}
+
+spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dtype dtype,
+                         const void* Q, const void* K, const void* V, const void* O,
+                         const float* LSE, const void* dO, float scale, void* dQ, void* dK,
+                         void* dV, void* cuda_stream) {
+  if (!cp) return fail(SPATTN_ERR_NULL, "plan is NULL");
+  spattn_plan* p = const_cast<spattn_plan*>(cp);  // owns mutable scratch
+  spattn_status st;
+  if ((st = check_ptr(Q, "Q")) || (st = check_ptr(K, "K")) || (st = check_ptr(V, "V")) ||
+      (st = check_ptr(O, "O")) || (st = check_ptr(LSE, "LSE")) || (st = check_ptr(dO, "dO")) ||
+      (st = check_ptr(dQ, "dQ")) || (st = check_ptr(dK, "dK")) || (st = check_ptr(dV, "dV")))
+    return st;
+  if (B < 1 || H < 1) return fail(SPATTN_ERR_SHAPE, "B and H must be >= 1");
+  const int64_t BH = int64_t(B) * H;
+  if (BH > 65535) return fail(SPATTN_ERR_SHAPE, "B*H = %lld exceeds 65535", (long long)BH);
+  if (dtype != SPATTN_BF16 && dtype != SPATTN_FP32) return fail(SPATTN_ERR_DTYPE, "unknown dtype");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(SPATTN_ERR_INVALID_SPEC, "scale must be positive and finite");
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const size_t dvec_bytes = (size_t(BH) * p->T * 4 + 255) / 256 * 256;
+  const size_t kc_bytes = size_t(BH) * p->n_cols * p->d * 4;
+  const size_t need = dvec_bytes + 2 * kc_bytes;
+  if (need > p->bscratch_bytes) {
+    if (p->d_bscratch) {
+      CUDA_TRY(cudaStreamSynchronize(stream));
+      CUDA_TRY(cudaFree(p->d_bscratch));
+      p->d_bscratch = nullptr;
+      p->bscratch_bytes = 0;
+    }
+    CUDA_TRY(cudaMalloc(&p->d_bscratch, need));
+    p->bscratch_bytes = need;
+  }
+  uint8_t* base = static_cast<uint8_t*>(p->d_bscratch);
+  spattn::BwdArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.LSE = LSE;
+  a.dO = dO;
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.Dvec = reinterpret_cast<float*>(base);
+  a.dKc = reinterpret_cast<float*>(base + dvec_bytes);
+  a.dVc = reinterpret_cast<float*>(base + dvec_bytes + kc_bytes);
+  a.BH = static_cast<int32_t>(BH);
+  a.n_cols = p->n_cols;
+  a.scale = scale;
+  a.bf16 = dtype == SPATTN_BF16;
+  a.cols = p->d_cols;
+  a.colidx = p->d_colidx;
+  a.colmask = p->d_colmask;
+  a.mask = p->mask_dev();
+  a.q_items = p->sched[1].d_items;
+  a.q_entries = p->sched[1].d_entries;
+  a.n_q_items = static_cast<int32_t>(p->sched[1].items.size() / 4);
+  a.units = p->bsched.d_items;
+  a.u_entries = p->bsched.d_entries;
+  a.n_packed_units = p->bsched.n_packed_units;
+  a.n_units = static_cast<int32_t>(p->bsched.items.size() / 4);
+  cudaError_t e = spattn::launch_bwd_simt(p->d, a, stream);
+  if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return SPATTN_OK;
 }
 

@@ -84,6 +84,13 @@ def qkv(B: int, H: int, T: int, d: int, seed: int, dtype=torch.bfloat16):
     return tuple(out)
 
 
+def grad_out(B: int, H: int, T: int, d: int, seed: int, dtype=torch.bfloat16):
+    """dO of shape [B, H, T, d] (contiguous, CPU), i.i.d. N(0,1), drawn from a stream
+    of its own (seed + 104729) so that it is independent of Q, K, V."""
+    g = torch.Generator().manual_seed(int(seed) + 104729)
+    return torch.randn(B, H, T, d, generator=g, dtype=torch.float32).to(dtype).contiguous()
+
+
 def sample_rows(T: int, n: int, seed: int, must=()) -> np.ndarray:
     """Sorted distinct query rows: `must` (clipped to [0,T)) plus seeded uniform picks."""
     rng = np.random.default_rng(seed + 7919)

@@ -520,6 +520,13 @@ def check_bwd_invariants():
     dQ, dK, dV = _oracle_bwd(oracle.Mask(T, 0, 0, 4), Q, K, V, torch.zeros(T, d), 0.4)
     if dQ.any() or dK.any() or dV.any():
         bad.append("dO = 0 gives nonzero gradients")
+    # the row-subset dQ equals the full evaluation's rows
+    m = oracle.Mask(T, 1, 5, -1, 4, 1, [3, 20])
+    dQ, _, _ = _oracle_bwd(m, Q, K, V, dO, 0.4)
+    rows = np.array([29, 0, 3, 20, 11], dtype=np.int64)
+    sub = oracle.attention_bwd_dq(m, Q.numpy(), K.numpy(), V.numpy(), dO.numpy(), 0.4, rows)
+    if not np.array_equal(sub, dQ[rows]):
+        bad.append("row-subset dQ differs from the full evaluation")
     return bad
 
 

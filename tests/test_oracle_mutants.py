@@ -43,14 +43,15 @@ BWD_MUTANTS = {
     "bwd_D_unweighted": ("D += a[t] * acc;", "D += acc;"),
     "bwd_dV_unweighted": ("dV[j * d + k] += a[t] * load_elem(dO",
                           "dV[j * d + k] += load_elem(dO"),
-    "bwd_dQ_no_scale": ("dQ[i * d + k] += scale * ds", "dQ[i * d + k] += ds"),
+    "bwd_dQ_no_scale": ("dq_row[k] += scale * ds", "dq_row[k] += ds"),
     "bwd_dK_uses_key": ("dK[j * d + k] += scale * ds * load_elem(Q, dtype, i * d + k);",
                         "dK[j * d + k] += scale * ds * load_elem(K, dtype, i * d + k);"),
     "bwd_dalpha_uses_key": ("acc += load_elem(dO, dtype, i * d + k) * load_elem(V, dtype, set[t] * d + k);",
                             "acc += load_elem(dO, dtype, i * d + k) * load_elem(K, dtype, set[t] * d + k);"),
-    "bwd_logit_unscaled": ("      a[t] = scale * acc;\n      if (a[t] > mx)",
-                           "      a[t] = acc;\n      if (a[t] > mx)"),
+    "bwd_logit_unscaled": ("    a[t] = scale * acc;\n    if (a[t] > mx)",
+                           "    a[t] = acc;\n    if (a[t] > mx)"),
     "bwd_dV_to_query_row": ("dV[j * d + k] +=", "dV[i * d + k] +="),
+    "bwd_rows_subset_shifted": ("bwd_row(&m, rows[r], d,", "bwd_row(&m, rows[r] / 2, d,"),
 }
 
 
