@@ -63,6 +63,10 @@ def _configure(lib):
         _i64, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_double, _vp, _i64,
         ctypes.POINTER(ctypes.c_double)]
     lib.oracle_attention_bwd_dq_rows.restype = None
+    lib.oracle_decode.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp,
+                                  ctypes.c_double, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]
+    lib.oracle_decode.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -237,6 +241,26 @@ def attention_bwd_dq(mask: Mask, Q, K, V, dO, scale: float, rows):
         dO.ctypes.data, float(scale), rr.ctypes.data, int(rr.size),
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return out
+
+
+def decode(q, Kc, Vc, t: int, window: int, scale: float):
+    """One decode step of one query head against a ring-buffer cache.
+
+    q: [d]; Kc, Vc: [cap, d] (float32, or uint16 bf16 bits); the token at position t
+    reads positions max(0, t-window+1) .. t, position p from slot p % cap.
+    Returns (out [d] fp64, lse)."""
+    cap, d = Kc.shape
+    assert Vc.shape == (cap, d) and q.shape == (d,) and 1 <= window <= cap
+    dt = 0 if q.dtype == np.float32 else 1
+    assert Kc.dtype == Vc.dtype == q.dtype
+    q, Kc, Vc = (np.ascontiguousarray(x) for x in (q, Kc, Vc))
+    out = np.zeros(d, np.float64)
+    lse = ctypes.c_double()
+    pd = ctypes.POINTER(ctypes.c_double)
+    _load().oracle_decode(int(cap), int(window), int(t), int(d), dt, q.ctypes.data,
+                          Kc.ctypes.data, Vc.ctypes.data, float(scale), out.ctypes.data_as(pd),
+                          ctypes.byref(lse))
+    return out, lse.value
 
 
 def num_threads() -> int:

@@ -42,6 +42,9 @@
  *
  *   Gradients.  oracle_attention_bwd_head: dQ, dK, dV of the same y given dO, by the
  *   chain rule through the softmax over S_i (see the function).
+ *
+ *   Decode.  oracle_decode: one new token against a ring-buffer KV cache that keeps
+ *   the last cap tokens (see the function).
  */
 #include <math.h>
 #include <stdint.h>
@@ -378,6 +381,46 @@ void oracle_attention_bwd_dq_rows(int causal, int64_t window, int64_t radius, in
     free(a);
     free(da);
   }
+}
+
+/* ---- decode with a capped KV cache ------------------------------------------------ */
+
+/* One decode step of one query head: the token at position t attends to positions
+ * max(0, t-w+1) .. t, the w most recent tokens including itself ("Sparse and
+ * sliding-window attention", getnybble, §Sliding window attention).  The cache keeps
+ * only the last cap >= w tokens ("Attention variants" §1, a sliding-window layer keeps
+ * the last w keys and values): position p lives in slot p % cap, so K/V of position
+ * p are Kc[p % cap], Vc[p % cap].  q: [d], Kc, Vc: [cap][d] (dtype 0 fp32, 1 bf16
+ * bits).  Writes out[d] (fp64) and *lse = ln sum exp(scale q.k).  t < 0: no keys,
+ * out = 0, *lse = -inf. */
+void oracle_decode(int64_t cap, int64_t w, int64_t t, int64_t d, int dtype, const void* q,
+                   const void* Kc, const void* Vc, double scale, double* out, double* lse) {
+  for (int64_t k = 0; k < d; k++) out[k] = 0.0;
+  if (t < 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  const int64_t p0 = t - w + 1 > 0 ? t - w + 1 : 0;
+  const int64_t n = t - p0 + 1;
+  double* s = (double*)malloc(sizeof(double) * (size_t)n);
+  double mx = -INFINITY;
+  for (int64_t a = 0; a < n; a++) {
+    const int64_t slot = (p0 + a) % cap;
+    double acc = 0.0;
+    for (int64_t k = 0; k < d; k++)
+      acc += load_elem(q, dtype, k) * load_elem(Kc, dtype, slot * d + k);
+    s[a] = scale * acc;
+    if (s[a] > mx) mx = s[a];
+  }
+  double l = 0.0;
+  for (int64_t a = 0; a < n; a++) l += exp(s[a] - mx);
+  for (int64_t a = 0; a < n; a++) {
+    const int64_t slot = (p0 + a) % cap;
+    const double wgt = exp(s[a] - mx) / l;
+    for (int64_t k = 0; k < d; k++) out[k] += wgt * load_elem(Vc, dtype, slot * d + k);
+  }
+  *lse = mx + log(l);
+  free(s);
 }
 
 /* Number of OpenMP threads the oracle uses (1 when built without OpenMP). */

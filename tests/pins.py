@@ -530,6 +530,64 @@ def check_bwd_invariants():
     return bad
 
 
+# ---------------------------------------------------------------- decode pins
+
+def ring_fill(K, t, cap):
+    """The cache after writing positions 0..t of K in order, position p to slot
+    p % cap (later positions overwrite earlier ones)."""
+    Kc = np.zeros((cap, K.shape[1]), K.dtype)
+    for p in range(t + 1):
+        Kc[p % cap] = K[p]
+    return Kc
+
+
+def check_decode_matches_sequence_rows():
+    """A decode step equals row t of the forward oracle on the whole sequence with the
+    causal window w, for a cache filled by the ring rule (t below, at and far above
+    the capacity; window below and equal to the capacity)."""
+    bad = []
+    T, d = 300, 16
+    g = torch.Generator().manual_seed(61)
+    Q, K, V = (torch.randn(T, d, generator=g).numpy() for _ in range(3))
+    for cap, w in [(64, 64), (64, 17), (100, 1), (37, 37)]:
+        m = oracle.Mask(T, 1, w)
+        for t in [0, 5, cap - 1, cap, cap + 3, 2 * cap + 7, T - 1]:
+            O, L = oracle.attention(m, Q, K, V, 0.3, np.array([t], dtype=np.int64))
+            out, lse = oracle.decode(Q[t], ring_fill(K, t, cap), ring_fill(V, t, cap), t, w, 0.3)
+            if not (np.allclose(out, O[0], rtol=0, atol=1e-12) and abs(lse - L[0]) < 1e-12):
+                bad.append(f"decode cap={cap} w={w} t={t} != sequence row")
+    return bad
+
+
+def check_decode_special():
+    """Against torch fp64 SDPA: with t < cap and w = cap the cache is the prefix and
+    the step is the causal attention row; the cache's slot order does not matter
+    (softmax over a set); a token before any key (t < 0) reads nothing."""
+    bad = []
+    cap, d = 50, 8
+    g = torch.Generator().manual_seed(62)
+    q, K, V = torch.randn(d, generator=g), torch.randn(cap, d, generator=g), torch.randn(cap, d, generator=g)
+    for t in [0, 1, 20, 49]:
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q.double()[None, None, None], K.double()[None, None, :t + 1],
+            V.double()[None, None, :t + 1], scale=0.5)[0, 0, 0].numpy()
+        out, _ = oracle.decode(q.numpy(), K.numpy(), V.numpy(), t, cap, 0.5)
+        if not np.allclose(out, ref, rtol=0, atol=1e-12):
+            bad.append(f"prefix decode t={t} vs SDPA")
+    # t >= cap - 1 with w = cap reads every slot: any permutation of the slots agrees
+    perm = np.random.default_rng(3).permutation(cap)
+    a, la = oracle.decode(q.numpy(), K.numpy(), V.numpy(), 1000, cap, 0.5)
+    b, lb = oracle.decode(q.numpy(), K.numpy()[perm], V.numpy()[perm], 1000, cap, 0.5)
+    if not (np.allclose(a, b, rtol=0, atol=1e-12) and abs(la - lb) < 1e-12):
+        bad.append("full-cache decode depends on slot order")
+    out, lse = oracle.decode(q.numpy(), K.numpy(), V.numpy(), -1, cap, 0.5)
+    if out.any() or lse != -math.inf:
+        bad.append("t < 0 is not empty")
+    return bad
+
+
+DECODE_CHECKS = [check_decode_matches_sequence_rows, check_decode_special]
+
 BWD_CHECKS = [check_bwd_autograd, check_bwd_finite_differences, check_bwd_invariants]
 
 COUNT_CHECKS = [check_page_counts, check_row_sets, check_reach, check_edge_formula,

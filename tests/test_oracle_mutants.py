@@ -11,7 +11,7 @@ import subprocess
 import pytest
 
 import oracle
-from pins import ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS
+from pins import ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS, DECODE_CHECKS
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -96,3 +96,26 @@ def test_mutant_is_caught(oracle_mod, tmp_path, name):
             if failures:
                 break
     assert failures, f"mutant {name} passed every pin"
+
+
+# Slips in the decode function, checked against the decode pins only.
+DECODE_MUTANTS = {
+    "decode_slot_is_position": ("const int64_t slot = (p0 + a) % cap;\n    double acc",
+                                "const int64_t slot = (p0 + a) % (cap + 1);\n    double acc"),
+    "decode_window_one_short": ("t - w + 1 > 0 ? t - w + 1 : 0", "t - w + 2 > 0 ? t - w + 2 : 0"),
+    "decode_value_slot_stale": ("const int64_t slot = (p0 + a) % cap;\n    const double wgt",
+                                "const int64_t slot = (p0 + a + 1) % cap;\n    const double wgt"),
+    "decode_unnormalised": ("exp(s[a] - mx) / l;", "exp(s[a] - mx);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_MUTANTS))
+def test_decode_mutant_is_caught(oracle_mod, tmp_path, name):
+    so = _build_mutant(tmp_path, *DECODE_MUTANTS[name])
+    failures = []
+    with oracle.use_library(so):
+        for check in DECODE_CHECKS:
+            failures += check()
+            if failures:
+                break
+    assert failures, f"mutant {name} passed every decode pin"

@@ -3,10 +3,10 @@ import pytest
 
 import oracle
 import spattn_workloads as W
-from pins import ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS, closed_form_pairs
+from pins import ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS, DECODE_CHECKS, closed_form_pairs
 
 
-@pytest.mark.parametrize("check", COUNT_CHECKS + ATTENTION_CHECKS + BWD_CHECKS,
+@pytest.mark.parametrize("check", COUNT_CHECKS + ATTENTION_CHECKS + BWD_CHECKS + DECODE_CHECKS,
                          ids=lambda f: f.__name__)
 def test_pin(oracle_mod, check):
     bad = check()
