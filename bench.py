@@ -440,6 +440,116 @@ def run_ours_bwd(args, cfg, p):
     return 0
 
 
+# ----------------------------------------------------------------- decode arm
+
+DECODE_METRIC = "decode KV-cache GB/s (bytes of cached K/V read per step / step time), 1 GPU"
+
+
+def run_decode(args):
+    """One step = one generation step of every sequence: spattn_kv_append of the
+    step's key/value rows, then spattn_decode of the step's queries against the
+    ring-buffer cache (the window of every sequence is full).  Algorithmic bytes per
+    step: the cached K and V rows read (B Hkv window d 2 2 bytes) plus q, the new rows
+    and the output."""
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    import sparse_masked_attention_plan_b300 as sp
+    cfg = W.DECODE_WORKLOADS[args.decode_workload]
+    B, Hq, Hkv, cap, w, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["cap"], cfg["window"], cfg["d"]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.Generator().manual_seed(rank)
+    with torch.cuda.stream(stream):
+        c = sp.DecodeCache(B, Hq, Hkv, cap, d, window=w, device=dev)
+        c.K.copy_(torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16))
+        c.V.copy_(torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16))
+    qh = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).pin_memory()
+    kh = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).pin_memory()
+    vh = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).pin_memory()
+    pos0 = torch.from_numpy(W.decode_positions(B, cap, rank))
+    q, kn, vn = (x.to(dev) for x in (qh, kh, vh))
+    out = torch.empty_like(q)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    steps_total = args.warmup + args.steps
+    pos_all = torch.stack([pos0 + s for s in range(steps_total)]).to(dev)  # [steps, B]
+    stream.synchronize()
+    kv_bytes = B * Hkv * w * d * 2 * 2
+    step_bytes = kv_bytes + (2 * q.numel() + 2 * kn.numel()) * 2 + lse.numel() * 4
+    scale = 1.0 / math.sqrt(d)
+
+    def step(s):
+        c.append(kn, vn, pos_all[s], stream=stream)
+        c.step(q, pos_all[s], scale, out=out, lse=lse, stream=stream)
+
+    for s in range(args.warmup):
+        step(s)
+    stream.synchronize()
+    c.check(stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for s in range(args.steps):
+            step(args.warmup + s)
+            ev[s + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    c.check(stream)
+    per = [ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps)]
+    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world) / args.steps
+    value = world * step_bytes / (ms / 1e3) / 1e9
+
+    # end to end: this step's q, k, v from pinned host memory, append + decode, the
+    # output back to the host, every step
+    oh = torch.empty_like(qh).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier(world)
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            q.copy_(qh, non_blocking=True)
+            kn.copy_(kh, non_blocking=True)
+            vn.copy_(vh, non_blocking=True)
+        step(s % steps_total)
+        with torch.cuda.stream(stream):
+            oh.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = world * step_bytes * e2e_steps / e2e_s / 1e9
+    if rank == 0:
+        peaks, src = load_peaks()
+        step_ms = statistics.mean(per)
+        achieved = step_bytes / (step_ms / 1e3) / 1e9
+        line = {
+            "metric": DECODE_METRIC, "pass": "decode", "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.decode_workload, **cfg,
+                       "tokens_per_step": B,
+                       "l2": f"cache larger than L2 ({kv_bytes / 1e6:.0f} MB of K/V)"},
+            "tokens_per_s": world * B / (ms / 1e3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"{src} hbm_gbs",
+                         "kernel": "kv_append + decode + combine (whole step)",
+                         "kernel_ms": step_ms},
+            "e2e": {"value": e2e, "unit": "GB/s",
+                    "h2d_bytes_per_step": (q.numel() + 2 * kn.numel()) * 2,
+                    "d2h_bytes_per_step": out.numel() * 2,
+                    "api": "DecodeCache.append/step with pinned host q/k/v and output"},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,8 +560,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
-                    help="time the forward (default, the headline) or the backward pass")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd", "decode"],
+                    help="time the forward (default, the headline), the backward pass, or "
+                         "one decode step")
+    ap.add_argument("--decode-workload", default="decode_b32_w4096",
+                    choices=sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (smaller profiling captures; the line then names it)")
     args = ap.parse_args()
@@ -465,6 +578,8 @@ def main():
         return run_reference(args, cfg, p)
     if args.which == "bwd":
         return run_ours_bwd(args, cfg, p)
+    if args.which == "decode":
+        return run_decode(args)
     return run_ours(args, cfg, p)
 
 

@@ -215,6 +215,61 @@ spattn_status spattn_bwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_d
                          void* dV, void* cuda_stream);
 
 /*
+ * ---- Decode: one generation step against a capped ring-buffer KV cache ----------
+ *
+ * The token at position t reads the w most recent positions max(0, t-w+1) .. t,
+ * itself included ("Sparse and sliding-window attention", section "Sliding window
+ * attention"); a sliding-window layer therefore keeps only the last cap >= w keys
+ * and values ("Attention variants", section 1), whatever the length of the
+ * generation.  Position p lives in slot p % cap of the cache.
+ *
+ * Layouts (device memory, contiguous, 16-byte aligned):
+ *   K_cache, V_cache: [B, Hkv, cap, d] of `dtype` (caller-owned; slots never written
+ *                     are never read while pos[b] < cap);
+ *   q, out:           [B, Hq, d] of `dtype`; lse: [B, Hq] fp32 natural log (or NULL);
+ *   k_new, v_new:     [B, Hkv, d] of `dtype`;
+ *   pos:              [B] int64, device memory: the position of the token each batch
+ *                     row is generating (rows may be at different positions).  A
+ *                     negative position means "no token": append skips the row and
+ *                     decode writes out = 0, lse = -inf.
+ * Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention); Hq must
+ * be a multiple of Hkv with Hq / Hkv <= 8.  head_dim 64 or 128; 1 <= cap <= 2^30.
+ */
+
+/* Write k_new, v_new of every (b, kv head) to slot pos[b] % cap.  Asynchronous on
+ * cuda_stream.  Errors: NULL, ALIGN, SHAPE, DTYPE, CUDA. */
+spattn_status spattn_kv_append(int32_t B, int32_t Hkv, int64_t cap, int32_t head_dim,
+                               spattn_dtype dtype, void* K_cache, void* V_cache,
+                               const void* k_new, const void* v_new, const int64_t* pos,
+                               void* cuda_stream);
+
+/* Bytes of device workspace spattn_decode needs for these sizes (caller-owned).  The
+ * first 4 bytes are the device error word: zero the workspace once (cudaMemset)
+ * before its first use; spattn_decode_check reads and clears the word. */
+spattn_status spattn_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap,
+                                            int32_t head_dim, size_t* bytes);
+
+/* One decode step: out[b, h] = sum over the allowed positions p of
+ * softmax_p(scale q[b,h] . k_p) v_p with k_p, v_p read from slot p % cap of key/value
+ * head h / (Hq/Hkv), the allowed positions being max(0, pos[b]-window+1) .. pos[b]
+ * (window = 0 means window = cap; 1 <= window <= cap).  The caller appends the
+ * step's own key and value (spattn_kv_append) before calling, as the token reads
+ * itself.  Asynchronous on cuda_stream; fp32 accumulation; bf16 out rounded once.
+ * Device-side waits are bounded: one that runs out sets the workspace's error word
+ * (reported by spattn_decode_check as SPATTN_ERR_TIMEOUT).
+ * Errors: NULL, ALIGN, SHAPE (also a workspace smaller than
+ * spattn_decode_workspace_bytes), INVALID_SPEC (window, scale), DTYPE, CUDA. */
+spattn_status spattn_decode(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap, int64_t window,
+                            int32_t head_dim, spattn_dtype dtype, const void* q,
+                            const void* K_cache, const void* V_cache, const int64_t* pos,
+                            float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* cuda_stream);
+
+/* Synchronise cuda_stream, then report (and clear) the decode workspace's error word:
+ * SPATTN_ERR_TIMEOUT if a device-side wait ran out, else SPATTN_OK. */
+spattn_status spattn_decode_check(void* workspace, void* cuda_stream);
+
+/*
  * The same forward pass from HOST buffers: copies Q/K/V host -> device, runs
  * spattn_fwd, copies O and LSE device -> host, all on `cuda_stream`, and returns
  * after the stream is synchronised.  Host buffers should be pinned for full copy

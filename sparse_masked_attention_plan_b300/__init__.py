@@ -28,7 +28,8 @@ BF16, FP32 = 0, 1
 EXPORTS = ("spattn_mask_validate", "spattn_plan_create", "spattn_plan_info",
            "spattn_plan_copy_tiles", "spattn_plan_copy_columns", "spattn_plan_copy_schedule",
            "spattn_plan_set_walk_counter", "spattn_plan_walk_count", "spattn_fwd",
-           "spattn_bwd", "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
+           "spattn_bwd", "spattn_kv_append", "spattn_decode_workspace_bytes",
+           "spattn_decode", "spattn_decode_check", "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
            "spattn_plan_test_wait_timeout", "spattn_plan_check_device", "spattn_plan_destroy",
            "spattn_last_error", "spattn_version")
 
@@ -81,6 +82,18 @@ def lib():
                                           _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]
             L.spattn_fwd_static_scratch.argtypes = L.spattn_fwd.argtypes
+            L.spattn_kv_append.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.c_int32, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                           _vp, _vp]
+            L.spattn_decode_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32,
+                                                        ctypes.c_int32, ctypes.c_int64,
+                                                        ctypes.c_int32,
+                                                        ctypes.POINTER(ctypes.c_size_t)]
+            L.spattn_decode.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                        _vp, _vp, ctypes.c_size_t, _vp]
+            L.spattn_decode_check.argtypes = [_vp, _vp]
             L.spattn_bwd.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, _vp,
                                      _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
                                      _vp]
@@ -270,6 +283,47 @@ def bwd(plan: Plan, q, k, v, o, lse, do, scale: float, dq=None, dk=None, dv=None
                             float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                             _stream_handle(stream)))
     return dq, dk, dv
+
+
+class DecodeCache:
+    """A ring-buffer KV cache of one sliding-window layer and its decode workspace.
+
+    K, V: [B, Hkv, cap, d] CUDA tensors (allocated here); position p lives in slot
+    p % cap.  append() writes a step's keys/values, step() runs one decode step."""
+
+    def __init__(self, B, Hq, Hkv, cap, head_dim, window=0, dtype=None, device="cuda"):
+        import torch
+        dtype = torch.bfloat16 if dtype is None else dtype
+        self.B, self.Hq, self.Hkv, self.cap, self.d = B, Hq, Hkv, cap, head_dim
+        self.window = window
+        self.K = torch.zeros(B, Hkv, cap, head_dim, dtype=dtype, device=device)
+        self.V = torch.zeros_like(self.K)
+        n = ctypes.c_size_t()
+        _check(lib().spattn_decode_workspace_bytes(B, Hq, Hkv, cap, head_dim, ctypes.byref(n)))
+        self.workspace = torch.zeros(n.value, dtype=torch.uint8, device=device)
+
+    def append(self, k_new, v_new, pos, stream=None):
+        """k_new, v_new: [B, Hkv, d]; pos: [B] int64 CUDA tensor."""
+        _check(lib().spattn_kv_append(self.B, self.Hkv, self.cap, self.d, _dtype_code(k_new),
+                                      self.K.data_ptr(), self.V.data_ptr(), k_new.data_ptr(),
+                                      v_new.data_ptr(), pos.data_ptr(), _stream_handle(stream)))
+
+    def step(self, q, pos, scale, out=None, lse=None, stream=None):
+        """q: [B, Hq, d]; pos: [B] int64 CUDA tensor.  Returns (out, lse)."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=q.device)
+        _check(lib().spattn_decode(self.B, self.Hq, self.Hkv, self.cap, self.window, self.d,
+                                   _dtype_code(q), q.data_ptr(), self.K.data_ptr(),
+                                   self.V.data_ptr(), pos.data_ptr(), float(scale),
+                                   out.data_ptr(), lse.data_ptr(), self.workspace.data_ptr(),
+                                   self.workspace.numel(), _stream_handle(stream)))
+        return out, lse
+
+    def check(self, stream=None):
+        _check(lib().spattn_decode_check(self.workspace.data_ptr(), _stream_handle(stream)))
 
 
 def fwd_static_scratch(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None):

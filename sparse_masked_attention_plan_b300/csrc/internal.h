@@ -224,6 +224,26 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st);
 
+// decode.cu (one generation step against a ring-buffer KV cache)
+struct DecodeArgs {
+  const void* q;
+  const void* Kc;
+  const void* Vc;
+  const int64_t* pos;
+  void* out;
+  float* lse;
+  float* part;  // [B*Hq][nsplit][d + 2] scratch
+  int* err;
+  int32_t B, Hq, Hkv, d, nsplit, bf16;
+  int64_t cap, window;
+  float scale;
+};
+int decode_splits(int64_t B, int64_t Hkv, int64_t cap);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_kv_append(bool bf16, void* Kc, void* Vc, const void* kn, const void* vn,
+                             const int64_t* pos, int32_t B, int32_t Hkv, int64_t cap, int32_t d,
+                             cudaStream_t st);
+
 // spattn_api.cu: schedule, mask view and column data a forward launch of `dtype` uses.
 void select_schedule(const spattn_plan* p, bool bf16, TcArgs* a);
 

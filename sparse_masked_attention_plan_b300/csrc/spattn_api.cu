@@ -738,6 +738,104 @@ spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   return SPATTN_OK;
 }
 
+// ---- decode ------------------------------------------------------------------------
+
+namespace {
+spattn_status decode_shape(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap, int64_t window,
+                           int32_t d, spattn_dtype dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1) return fail(SPATTN_ERR_SHAPE, "B, Hq and Hkv must be >= 1");
+  if (Hq % Hkv != 0 || Hq / Hkv > 8)
+    return fail(SPATTN_ERR_SHAPE, "Hq must be a multiple of Hkv with Hq / Hkv <= 8");
+  if (int64_t(B) * Hkv > (int64_t(1) << 24)) return fail(SPATTN_ERR_SHAPE, "B * Hkv too large");
+  if (cap < 1 || cap > (int64_t(1) << 30)) return fail(SPATTN_ERR_SHAPE, "cap must be in [1, 2^30]");
+  if (window < 0 || window > cap)
+    return fail(SPATTN_ERR_INVALID_SPEC, "window must be in [0, cap] (0 = cap)");
+  if (d != 64 && d != 128) return fail(SPATTN_ERR_SHAPE, "head_dim must be 64 or 128");
+  if (dtype != SPATTN_BF16 && dtype != SPATTN_FP32) return fail(SPATTN_ERR_DTYPE, "unknown dtype");
+  return SPATTN_OK;
+}
+constexpr size_t kDecodeHeader = 256;  // error word, padded
+}  // namespace
+
+spattn_status spattn_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap,
+                                            int32_t head_dim, size_t* bytes) {
+  if (!bytes) return fail(SPATTN_ERR_NULL, "bytes is NULL");
+  spattn_status st = decode_shape(B, Hq, Hkv, cap, 0, head_dim, SPATTN_BF16);
+  if (st != SPATTN_OK) return st;
+  const int ns = spattn::decode_splits(B, Hkv, cap);
+  *bytes = kDecodeHeader + size_t(B) * Hq * ns * (head_dim + 2) * 4;
+  return SPATTN_OK;
+}
+
+spattn_status spattn_kv_append(int32_t B, int32_t Hkv, int64_t cap, int32_t head_dim,
+                               spattn_dtype dtype, void* Kc, void* Vc, const void* k_new,
+                               const void* v_new, const int64_t* pos, void* cuda_stream) {
+  spattn_status st = decode_shape(B, Hkv, Hkv, cap, 0, head_dim, dtype);
+  if (st != SPATTN_OK) return st;
+  if ((st = check_ptr(Kc, "K_cache")) || (st = check_ptr(Vc, "V_cache")) ||
+      (st = check_ptr(k_new, "k_new")) || (st = check_ptr(v_new, "v_new")))
+    return st;
+  if (!pos) return fail(SPATTN_ERR_NULL, "pos is NULL");
+  if (reinterpret_cast<uintptr_t>(pos) % 8) return fail(SPATTN_ERR_ALIGN, "pos misaligned");
+  CUDA_TRY(spattn::launch_kv_append(dtype == SPATTN_BF16, Kc, Vc, k_new, v_new, pos, B, Hkv, cap,
+                                    head_dim, static_cast<cudaStream_t>(cuda_stream)));
+  return SPATTN_OK;
+}
+
+spattn_status spattn_decode(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap, int64_t window,
+                            int32_t head_dim, spattn_dtype dtype, const void* q, const void* Kc,
+                            const void* Vc, const int64_t* pos, float scale, void* out,
+                            float* lse, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream) {
+  spattn_status st = decode_shape(B, Hq, Hkv, cap, window, head_dim, dtype);
+  if (st != SPATTN_OK) return st;
+  if ((st = check_ptr(q, "q")) || (st = check_ptr(Kc, "K_cache")) ||
+      (st = check_ptr(Vc, "V_cache")) || (st = check_ptr(out, "out")) ||
+      (st = check_ptr(workspace, "workspace")))
+    return st;
+  if (!pos) return fail(SPATTN_ERR_NULL, "pos is NULL");
+  if (reinterpret_cast<uintptr_t>(pos) % 8) return fail(SPATTN_ERR_ALIGN, "pos misaligned");
+  if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return fail(SPATTN_ERR_ALIGN, "lse misaligned");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(SPATTN_ERR_INVALID_SPEC, "scale must be positive and finite");
+  size_t need = 0;
+  spattn_decode_workspace_bytes(B, Hq, Hkv, cap, head_dim, &need);
+  if (workspace_bytes < need)
+    return fail(SPATTN_ERR_SHAPE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  spattn::DecodeArgs a;
+  a.q = q;
+  a.Kc = Kc;
+  a.Vc = Vc;
+  a.pos = pos;
+  a.out = out;
+  a.lse = lse;
+  a.err = static_cast<int*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kDecodeHeader);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = head_dim;
+  a.nsplit = spattn::decode_splits(B, Hkv, cap);
+  a.bf16 = dtype == SPATTN_BF16;
+  a.cap = cap;
+  a.window = window ? window : cap;
+  a.scale = scale;
+  cudaError_t e = spattn::launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return SPATTN_OK;
+}
+
+spattn_status spattn_decode_check(void* workspace, void* cuda_stream) {
+  if (!workspace) return fail(SPATTN_ERR_NULL, "workspace is NULL");
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
+  int e = 0;
+  CUDA_TRY(cudaMemcpy(&e, workspace, sizeof e, cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(workspace, 0, sizeof(int)));
+  if (e & spattn::kErrTimeout)
+    return fail(SPATTN_ERR_TIMEOUT, "a device-side wait of the decode kernel ran out of time");
+  return SPATTN_OK;
+}
+
 spattn_status spattn_fwd_host(const spattn_plan* p, int32_t B, int32_t H, spattn_dtype dtype,
                               const void* Qh, const void* Kh, const void* Vh, float scale, void* Oh,
                               float* LSEh, void* Qd, void* Kd, void* Vd, void* Od, float* LSEd,

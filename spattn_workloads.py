@@ -56,6 +56,21 @@ WORKLOADS = {
 }
 
 
+# Decode workloads: one generation step of B sequences against a ring-buffer KV cache
+# of cap = W = 4096 slots (the Mistral 7B shape of "Sparse and sliding-window
+# attention": W = 4096, 32 query heads over 8 key/value heads, d = 128), every
+# sequence past the cap so the whole window is read.
+DECODE_WORKLOADS = {
+    "decode_b32_w4096": dict(B=32, Hq=32, Hkv=8, cap=4096, window=4096, d=128),
+    "decode_b8_w4096": dict(B=8, Hq=32, Hkv=8, cap=4096, window=4096, d=128),
+}
+
+
+def decode_positions(B: int, cap: int, seed: int) -> np.ndarray:
+    """Per-sequence positions, all past the cap (seeded uniform in [cap, 2^20))."""
+    return np.random.default_rng(seed + 31337).integers(cap, 1 << 20, size=B).astype(np.int64)
+
+
 def global_positions(T: int, g: int, seed: int) -> np.ndarray:
     """`g` distinct token positions in [0, T), sorted, drawn from numpy's PCG64."""
     if g == 0:

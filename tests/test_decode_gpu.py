@@ -1,0 +1,183 @@
+"""Decode parity: one generation step against a ring-buffer KV cache (spattn_kv_append +
+spattn_decode through the C ABI) against the fp64 oracle's decode step, and a whole
+generation loop against rows of the forward oracle on the full sequence."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_masked_attention_plan_b300 as sp
+from gpu_cases import TOL, host_view, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+POISON = 3000.0  # written to every slot a step must not read
+
+
+def _fill_cache(B, Hkv, cap, d, pos, window, dtype, g):
+    """Random N(0,1) rows in the slots each batch row's step reads, POISON elsewhere."""
+    K = torch.full((B, Hkv, cap, d), POISON)
+    V = torch.full((B, Hkv, cap, d), -POISON)
+    for b, t in enumerate(pos):
+        if t < 0:
+            continue
+        w = window or cap
+        for p in range(max(0, t - w + 1), t + 1):
+            K[b, :, p % cap] = torch.randn(Hkv, d, generator=g)
+            V[b, :, p % cap] = torch.randn(Hkv, d, generator=g)
+    return K.to(torch_dtype(dtype)), V.to(torch_dtype(dtype))
+
+
+def _compare(out, lse, q, K, V, pos, window, scale, dtype, G):
+    tol = TOL[dtype]
+    B, Hq, d = q.shape
+    cap = K.shape[2]
+    for b in range(B):
+        for h in range(Hq):
+            ref, ref_lse = oracle.decode(host_view(q[b, h]), host_view(K[b, h // G]),
+                                         host_view(V[b, h // G]), int(pos[b]), window or cap,
+                                         scale)
+            got = out[b, h].astype(np.float64)
+            err = np.abs(got - ref).max()
+            assert err <= tol["max_abs"], f"(b, h) = {(b, h)} t = {pos[b]}: max-abs {err:.3g}"
+            if tol["rel_l2"] is not None and np.linalg.norm(ref) > 0:
+                rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+                assert rel <= tol["rel_l2"], f"(b, h) = {(b, h)}: rel-L2 {rel:.3g}"
+            if ref_lse == -math.inf:
+                assert lse[b, h] == -math.inf and not got.any()
+            else:
+                assert abs(lse[b, h] - ref_lse) <= tol["lse"], f"(b, h) = {(b, h)} LSE"
+
+
+CASES = [
+    # (B, Hq, Hkv, cap, window, d, positions)
+    (3, 8, 2, 4096, 0, 128, [5, 4095, 100000]),
+    (2, 4, 4, 100, 37, 64, [36, 250]),
+    (1, 8, 1, 300, 300, 128, [1000]),
+    (2, 4, 2, 64, 1, 64, [0, 77]),
+    (2, 2, 1, 130, 65, 128, [-1, 129]),
+    (4, 16, 8, 1000, 999, 64, [998, 999, 1500, 3]),
+    (1, 2, 2, 5000, 4000, 128, [4999]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("k", range(len(CASES)))
+def test_decode_step(oracle_mod, k, dtype):
+    B, Hq, Hkv, cap, window, d, pos = CASES[k]
+    g = torch.Generator().manual_seed(500 + k)
+    K, V = _fill_cache(B, Hkv, cap, d, pos, window, dtype, g)
+    q = torch.randn(B, Hq, d, generator=g).to(torch_dtype(dtype))
+    scale = 1.0 / math.sqrt(d)
+    c = sp.DecodeCache(B, Hq, Hkv, cap, d, window=window, dtype=torch_dtype(dtype))
+    c.K.copy_(K.cuda())
+    c.V.copy_(V.cuda())
+    p = torch.tensor(pos, dtype=torch.int64, device="cuda")
+    out, lse = c.step(q.cuda(), p, scale)
+    c.check()
+    _compare(out.float().cpu().numpy(), lse.cpu().numpy(), q, K, V, pos, window, scale, dtype,
+             Hq // Hkv)
+
+
+def test_append_writes_the_ring_slot():
+    B, Hkv, cap, d = 3, 2, 50, 64
+    c = sp.DecodeCache(B, 4, Hkv, cap, d)
+    g = torch.Generator().manual_seed(1)
+    before = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16)
+    c.K.copy_(before.cuda())
+    c.V.copy_(before.cuda())
+    kn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16)
+    pos = [7, 149, -3]
+    c.append(kn.cuda(), vn.cuda(), torch.tensor(pos, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    want_k, want_v = before.clone(), before.clone()
+    for b, t in enumerate(pos):
+        if t >= 0:
+            want_k[b, :, t % cap] = kn[b]
+            want_v[b, :, t % cap] = vn[b]
+    assert torch.equal(c.K.cpu(), want_k) and torch.equal(c.V.cpu(), want_v)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_generation_loop_matches_sequence_rows(oracle_mod, dtype):
+    """Append + decode token by token with a cache smaller than the sequence; every
+    step must equal row t of the forward oracle over the whole sequence with the
+    causal window."""
+    T, Hq, Hkv, cap, window, d = 300, 4, 2, 64, 48, 64
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(9)
+    Q = torch.randn(Hq, T, d, generator=g).to(torch_dtype(dtype))
+    K = torch.randn(Hkv, T, d, generator=g).to(torch_dtype(dtype))
+    V = torch.randn(Hkv, T, d, generator=g).to(torch_dtype(dtype))
+    scale = 0.2
+    c = sp.DecodeCache(1, Hq, Hkv, cap, d, window=window, dtype=torch_dtype(dtype))
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    outs, lses = [], []
+    for t in range(T):
+        p = torch.tensor([t], dtype=torch.int64, device="cuda")
+        c.append(Kd[None, :, t].contiguous(), Vd[None, :, t].contiguous(), p)
+        o, l = c.step(Qd[None, :, t].contiguous(), p, scale)
+        outs.append(o[0].float().cpu())
+        lses.append(l[0].cpu())
+    c.check()
+    out = torch.stack(outs, 1).numpy()  # [Hq, T, d]
+    lse = torch.stack(lses, 1).numpy()
+    m = oracle.Mask(T, 1, window)
+    tol = TOL[dtype]
+    for h in range(Hq):
+        O, L = oracle.attention(m, host_view(Q[h]), host_view(K[h // G]), host_view(V[h // G]),
+                                scale)
+        err = np.abs(out[h] - O).max()
+        assert err <= tol["max_abs"], f"head {h}: max-abs {err:.3g}"
+        assert np.abs(lse[h] - L).max() <= tol["lse"], f"head {h}: LSE"
+
+
+def test_full_size_sampled_heads(oracle_mod):
+    """The benchmark's decode configuration (B=32, Hq=32, Hkv=8, cap=W=4096, d=128)
+    with every row past the cap at its own position; sampled (b, h) against the oracle."""
+    B, Hq, Hkv, cap, d = 32, 32, 8, 4096, 128
+    g = torch.Generator().manual_seed(17)
+    K = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16)
+    V = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16)
+    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16)
+    pos = np.random.default_rng(3).integers(cap, 10 ** 6, size=B)
+    c = sp.DecodeCache(B, Hq, Hkv, cap, d)
+    c.K.copy_(K.cuda())
+    c.V.copy_(V.cuda())
+    out, lse = c.step(q.cuda(), torch.tensor(pos, device="cuda"), 1 / math.sqrt(d))
+    c.check()
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b, h in [(0, 0), (5, 13), (31, 31), (17, 2)]:
+        ref, ref_lse = oracle.decode(host_view(q[b, h]), host_view(K[b, h // 4]),
+                                     host_view(V[b, h // 4]), int(pos[b]), cap, 1 / math.sqrt(d))
+        assert np.abs(out[b, h] - ref).max() <= 1e-2
+        assert abs(lse[b, h] - ref_lse) <= 1e-4
+
+
+def test_bad_arguments():
+    import ctypes
+    lib = sp.lib()
+    n = ctypes.c_size_t()
+    assert lib.spattn_decode_workspace_bytes(2, 6, 4, 100, 64, ctypes.byref(n)) == sp.ERR_SHAPE
+    assert lib.spattn_decode_workspace_bytes(2, 32, 2, 100, 64, ctypes.byref(n)) == sp.ERR_SHAPE
+    assert lib.spattn_decode_workspace_bytes(2, 8, 2, 100, 96, ctypes.byref(n)) == sp.ERR_SHAPE
+    assert lib.spattn_decode_workspace_bytes(2, 8, 2, 100, 64, ctypes.byref(n)) == sp.OK
+    c = sp.DecodeCache(2, 8, 2, 100, 64)
+    q = torch.zeros(2, 8, 64, dtype=torch.bfloat16, device="cuda")
+    p = torch.zeros(2, dtype=torch.int64, device="cuda")
+    out = torch.empty_like(q)
+    st = lib.spattn_decode(2, 8, 2, 100, 101, 64, 0, q.data_ptr(), c.K.data_ptr(), c.V.data_ptr(),
+                           p.data_ptr(), 0.1, out.data_ptr(), None, c.workspace.data_ptr(),
+                           c.workspace.numel(), None)
+    assert st == sp.ERR_INVALID_SPEC
+    st = lib.spattn_decode(2, 8, 2, 100, 0, 64, 0, q.data_ptr(), c.K.data_ptr(), c.V.data_ptr(),
+                           p.data_ptr(), 0.1, out.data_ptr(), None, c.workspace.data_ptr(),
+                           16, None)
+    assert st == sp.ERR_SHAPE
+    st = lib.spattn_decode(2, 8, 2, 100, 0, 64, 0, q.data_ptr(), c.K.data_ptr(), c.V.data_ptr(),
+                           None, 0.1, out.data_ptr(), None, c.workspace.data_ptr(),
+                           c.workspace.numel(), None)
+    assert st == sp.ERR_NULL
