@@ -232,8 +232,8 @@ spattn_status spattn_bwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_d
  *                     row is generating (rows may be at different positions).  A
  *                     negative position means "no token": append skips the row and
  *                     decode writes out = 0, lse = -inf.
- * Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention); Hq must
- * be a multiple of Hkv with Hq / Hkv <= 8.  head_dim 64 or 128; 1 <= cap <= 2^30.
+ * Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention); Hq / Hkv
+ * must be 1, 2, 4 or 8.  head_dim 64 or 128; 1 <= cap <= 2^30.
  */
 
 /* Write k_new, v_new of every (b, kv head) to slot pos[b] % cap.  Asynchronous on

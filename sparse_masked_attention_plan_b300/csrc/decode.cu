@@ -12,7 +12,7 @@
 // The step is HBM-bound: every cached key and value row is read once per step and
 // used by the G query heads of its group.  The slot range [0, cap) of each (batch,
 // key/value head) is split across CTAs; a CTA streams 64-slot sub-chunks of K and V
-// into shared memory with bulk asynchronous copies (two stages, an mbarrier per
+// into shared memory with bulk asynchronous copies (a ring of stages, an mbarrier per
 // stage), runs an online softmax over them for the G query heads, and leaves (max,
 // sum, unnormalised output) per head; a second kernel merges the splits.  The valid
 // slots of a step are one circular interval of slot space (up to two linear ones), so
@@ -34,43 +34,46 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kSub = 64;      // slots per sub-chunk
 constexpr int kMaxGroup = 8;  // query heads per key/value head
+constexpr int kStages = 2;    // sub-chunks (K and V rows) in flight per CTA
 constexpr uint64_t kWaitBudget = 8000000000ull;
 
-template <typename In, int D>
+template <typename In, int D, int G>
 struct DecCfg {
   static constexpr int kRowBytes = D * sizeof(In);
-  static constexpr int kStageBytes = kSub * kRowBytes;  // K or V of one sub-chunk
+  static constexpr int kStageBytes = kSub * kRowBytes;  // K or V rows of one sub-chunk
   static constexpr int kVecPerRow = kRowBytes / 16;     // uint4 per row
   static constexpr int kVecPerLane = kVecPerRow / 8;    // 8 lanes per row
   static constexpr int kElemsPerVec = 16 / sizeof(In);
-  // shared layout: K[2], V[2] stages | q [8][D] | s [8][kSub] | m, l, corr [8] | red | bars
-  static constexpr int kOffQ = 4 * kStageBytes;
-  static constexpr int kOffS = kOffQ + kMaxGroup * D * 4;
-  static constexpr int kOffStats = kOffS + kMaxGroup * kSub * 4;
-  static constexpr int kOffRed = kOffStats + 3 * kMaxGroup * 4;
-  static constexpr int kOffBar = kOffRed + kThreads * 4 * 4;
-  static constexpr int kSmemBytes = kOffBar + 16;
+  static constexpr int kFrag = kVecPerLane * kElemsPerVec;  // = D / 8 elements per lane
+  static constexpr int kPairs = D / 2;                      // column pairs of one head
+  static constexpr int kKeyGroups = kThreads / kPairs;      // PV threads per column pair
+  // shared layout: K [kStages], V [kStages] | scores [G][kSub] | weights [kSub][G] |
+  // m, l, corr [8] | barriers
+  static constexpr int kOffS = 2 * kStages * kStageBytes;
+  static constexpr int kOffP = kOffS + G * kSub * 4;
+  static constexpr int kOffStats = kOffP + G * kSub * 4;
+  static constexpr int kOffBar = kOffStats + 3 * kMaxGroup * 4;
+  static constexpr int kSmemBytes = kOffBar + 8 * kStages;
+  static_assert(kKeyGroups * G * D * 4 <= 2 * kStages * kStageBytes, "reduction fits the stages");
 };
 
-__device__ __forceinline__ void to_float(const uint4& v, float* out, const float*) {
-  const float* f = reinterpret_cast<const float*>(&v);
-  out[0] = f[0];
-  out[1] = f[1];
-  out[2] = f[2];
-  out[3] = f[3];
+// 16 bytes of In as kElemsPerVec floats, packed in pairs.
+__device__ __forceinline__ void unpack(const uint4& v, uint64_t* out, const float*) {
+  out[0] = (static_cast<uint64_t>(v.y) << 32) | v.x;
+  out[1] = (static_cast<uint64_t>(v.w) << 32) | v.z;
 }
-__device__ __forceinline__ void to_float(const uint4& v, float* out, const __nv_bfloat16*) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+__device__ __forceinline__ void unpack(const uint4& v, uint64_t* out, const __nv_bfloat16*) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 f = __bfloat1622float2(h[k]);
-    out[2 * k] = f.x;
-    out[2 * k + 1] = f.y;
-  }
+  for (int k = 0; k < 4; ++k)  // bf16 -> fp32 is a 16-bit shift of the bit pattern
+    out[k] = (static_cast<uint64_t>(w[k] & 0xffff0000u) << 32) | (w[k] << 16);
 }
-__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
-__device__ __forceinline__ float2 ld2(const __nv_bfloat16* p) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+__device__ __forceinline__ uint64_t ld2p(const float* p) {
+  return *reinterpret_cast<const uint64_t*>(p);
+}
+__device__ __forceinline__ uint64_t ld2p(const __nv_bfloat16* p) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+  return (static_cast<uint64_t>(w & 0xffff0000u) << 32) | (w << 16);
 }
 __device__ __forceinline__ float ld1(const float* p) { return *p; }
 __device__ __forceinline__ float ld1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -84,7 +87,7 @@ struct DecParams {
   const int64_t* pos;  // [B]
   void* out;        // [B][Hq][D]
   float* lse;       // [B][Hq] or null
-  float* part;      // [B*Hq][nsplit][D + 2]: unnormalised output, max, sum
+  float* part;      // [B*Hq][nsplit][D + 2]: unnormalised output, max (log2 units), sum
   int* err;
   int32_t B, Hq, Hkv, G, nsplit;
   int64_t cap, window, span;
@@ -132,25 +135,29 @@ __device__ __forceinline__ void sub_chunk(const Ranges& r, int o, int64_t& s0, i
   rows = static_cast<int>(min(static_cast<int64_t>(kSub), r.b[k] - s0));
 }
 
-template <typename In, int D>
+// Online softmax over the CTA's slots, one 64-slot sub-chunk (its K and V rows, one
+// copy each) at a time through a ring of kStages buffers.  Scores run in log2 units:
+// q is pre-multiplied by scale * log2(e), the weights are exp2 of the differences,
+// and the combine step converts the result back.
+template <typename In, int D, int G>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
-  using Cfg = DecCfg<In, D>;
+  using Cfg = DecCfg<In, D, G>;
+  constexpr int F2 = Cfg::kFrag / 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  In* sK = reinterpret_cast<In*>(smem);                       // [2][kSub][D]
-  In* sV = reinterpret_cast<In*>(smem + 2 * Cfg::kStageBytes);  // [2][kSub][D]
-  float* sq = reinterpret_cast<float*>(smem + Cfg::kOffQ);    // [8][D]
-  float* ss = reinterpret_cast<float*>(smem + Cfg::kOffS);    // [8][kSub]
+  In* sK = reinterpret_cast<In*>(smem);                                // [kStages][kSub][D]
+  In* sV = reinterpret_cast<In*>(smem + kStages * Cfg::kStageBytes);  // [kStages][kSub][D]
+  float* ss = reinterpret_cast<float*>(smem + Cfg::kOffS);             // [G][kSub] scores
+  float* sp = reinterpret_cast<float*>(smem + Cfg::kOffP);             // [kSub][G] weights
   float* sm_ = reinterpret_cast<float*>(smem + Cfg::kOffStats);
   float* sl = sm_ + kMaxGroup;
   float* scorr = sl + kMaxGroup;
-  float* sred = reinterpret_cast<float*>(smem + Cfg::kOffRed);
   const uint32_t bar0 = smem_addr(smem + Cfg::kOffBar);
 
   const int split = blockIdx.x % p.nsplit;
   const int bk = blockIdx.x / p.nsplit;  // b * Hkv + kv head
   const int b = bk / p.Hkv, hk = bk % p.Hkv;
-  const int G = p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gi = lane >> 3, li = lane & 7;
   const int64_t t = p.pos[b];
   const int64_t lo = static_cast<int64_t>(split) * p.span;
   const Ranges rg = valid_ranges(t, p.cap, p.window, lo, min(p.cap, lo + p.span));
@@ -159,53 +166,61 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
   const In* Kbase = static_cast<const In*>(p.Kc) + static_cast<int64_t>(bk) * p.cap * D;
   const In* Vbase = static_cast<const In*>(p.Vc) + static_cast<int64_t>(bk) * p.cap * D;
 
-  if (tid == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8, 1);
-    fence_barrier_init();
-  }
-  // the G query rows of this group, fp32
-  const In* qb = static_cast<const In*>(p.q) + (static_cast<int64_t>(b) * p.Hq + hk * G) * D;
-  for (int x = tid; x < G * D; x += kThreads) sq[x] = ld1(qb + x);
-  if (tid < kMaxGroup) {
-    sm_[tid] = -INFINITY;
-    sl[tid] = 0.f;
-  }
-  __syncthreads();
-
   auto issue = [&](int o) {
     int64_t s0;
     int rows;
     sub_chunk(rg, o, s0, rows);
     const uint32_t bytes = static_cast<uint32_t>(rows) * Cfg::kRowBytes;
-    const uint32_t bar = bar0 + 8 * (o & 1);
+    const int st = o % kStages;
+    const uint32_t bar = bar0 + 8 * st;
     mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_load(smem_addr(sK + (o & 1) * kSub * D), Kbase + s0 * D, bytes, bar);
-    bulk_load(smem_addr(sV + (o & 1) * kSub * D), Vbase + s0 * D, bytes, bar);
+    bulk_load(smem_addr(sK + st * kSub * D), Kbase + s0 * D, bytes, bar);
+    bulk_load(smem_addr(sV + st * kSub * D), Vbase + s0 * D, bytes, bar);
   };
   int issued = 0;
-  if (tid == 0) {
-    for (; issued < 2 && issued < n_sub; ++issued) issue(issued);
+  if (tid == 0) {  // the first copies start before anything else
+    for (int k = 0; k < kStages; ++k) mbar_init(bar0 + 8 * k, 1);
+    fence_barrier_init();
+    for (; issued < kStages && issued < n_sub; ++issued) issue(issued);
   }
+  if (tid < kMaxGroup) {
+    sm_[tid] = -INFINITY;
+    sl[tid] = 0.f;
+  }
+  // this lane's slice of the G query rows, scaled into log2 units
+  uint64_t qf[G][F2];
+  {
+    const In* qb = static_cast<const In*>(p.q) + (static_cast<int64_t>(b) * p.Hq + hk * G) * D;
+    const float qs = p.scale * 1.4426950408889634f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int u = 0; u < Cfg::kVecPerLane; ++u)
+#pragma unroll
+        for (int e = 0; e < Cfg::kElemsPerVec; e += 2) {
+          const In* src = qb + g * D + (li + 8 * u) * Cfg::kElemsPerVec + e;
+          qf[g][(u * Cfg::kElemsPerVec + e) / 2] = f32x2(ld1(src) * qs, ld1(src + 1) * qs);
+        }
+  }
+  __syncthreads();
 
-  // PV mapping: pairs of output columns (g, 2c .. 2c+1); with fewer pairs than
-  // threads the keys of a sub-chunk are split over `ks` groups of threads.
-  const int npairs = G * D / 2;
-  const int nact = min(npairs, kThreads);
-  const int ks = kThreads / nact;
-  const int kg = tid / nact, pi0 = tid % nact;
-  const int ppt = (npairs + kThreads - 1) / kThreads;  // 1 or 2
-  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  // weighted values: thread owns column pair cp of every head, for the keys
+  // kg, kg + kKeyGroups, ... of each sub-chunk
+  const int cp = tid % Cfg::kPairs, kg = tid / Cfg::kPairs;
+  uint64_t acc[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) acc[g] = 0ull;
 
   for (int o = 0; o < n_sub; ++o) {
-    const int st = o & 1;
-    bool ok = mbar_wait(bar0 + 8 * st, (o >> 1) & 1, kWaitBudget, p.err, kErrTimeout);
+    const int st = o % kStages;
+    bool ok = mbar_wait(bar0 + 8 * st, (o / kStages) & 1, kWaitBudget, p.err, kErrTimeout);
     ok = __syncthreads_and(ok);
     if (!ok) {
       // drain this CTA's copies still in flight (bounded), then leave
       if (tid == 0)
         for (int x = o; x < issued; ++x)
-          mbar_wait(bar0 + 8 * (x & 1), (x >> 1) & 1, kWaitBudget, p.err, kErrTimeout);
+          mbar_wait(bar0 + 8 * (x % kStages), (x / kStages) & 1, kWaitBudget, p.err,
+                    kErrTimeout);
       __syncthreads();
       return;
     }
@@ -214,31 +229,27 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
     sub_chunk(rg, o, s0, rows);
     const In* K = sK + st * kSub * D;
     const In* V = sV + st * kSub * D;
-    // scores: 8 lanes per row, 4 rows per warp, 32 rows per pass
-    {
-      const int gi = lane >> 3, li = lane & 7;
+    // scores: 8 lanes per key row, 4 rows per warp, 32 rows per pass
 #pragma unroll
-      for (int pass = 0; pass < kSub / 32; ++pass) {
-        const int r = pass * 32 + warp * 4 + gi;
-        float kv[Cfg::kVecPerLane * Cfg::kElemsPerVec];
+    for (int pass = 0; pass < kSub / 32; ++pass) {
+      const int r = pass * 32 + warp * 4 + gi;
+      uint64_t kf[F2];
 #pragma unroll
-        for (int u = 0; u < Cfg::kVecPerLane; ++u) {
-          const uint4 v = reinterpret_cast<const uint4*>(K + r * D)[li + 8 * u];
-          to_float(v, kv + u * Cfg::kElemsPerVec, static_cast<const In*>(nullptr));
-        }
-        for (int g = 0; g < G; ++g) {
-          float dot = 0.f;
+      for (int u = 0; u < Cfg::kVecPerLane; ++u)
+        unpack(reinterpret_cast<const uint4*>(K + r * D)[li + 8 * u],
+               kf + u * Cfg::kElemsPerVec / 2, static_cast<const In*>(nullptr));
 #pragma unroll
-          for (int u = 0; u < Cfg::kVecPerLane; ++u)
+      for (int g = 0; g < G; ++g) {
+        uint64_t a2 = 0ull;
 #pragma unroll
-            for (int e = 0; e < Cfg::kElemsPerVec; ++e)
-              dot = fmaf(sq[g * D + (li + 8 * u) * Cfg::kElemsPerVec + e],
-                         kv[u * Cfg::kElemsPerVec + e], dot);
-          dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-          dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-          dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-          if (li == 0) ss[g * kSub + r] = r < rows ? dot * p.scale : -INFINITY;
-        }
+        for (int x = 0; x < F2; ++x) a2 = fma_f32x2(qf[g][x], kf[x], a2);
+        float lo2, hi2;
+        f32x2_split(a2, lo2, hi2);
+        float dot = lo2 + hi2;
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+        if (li == 0) ss[g * kSub + r] = r < rows ? dot : -INFINITY;
       }
     }
     __syncthreads();
@@ -250,73 +261,65 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
       for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
       const float m_old = sm_[warp];
       const float m_new = fmaxf(m_old, mx);  // finite: row 0 of a sub-chunk is valid
-      const float pa = expf(s_a - m_new), pb = expf(s_b - m_new);
+      const float pa = exp2f(s_a - m_new), pb = exp2f(s_b - m_new);
       float sum = pa + pb;
 #pragma unroll
       for (int k = 16; k > 0; k >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, k);
-      ss[warp * kSub + lane] = pa;
-      ss[warp * kSub + lane + 32] = pb;
-      __syncwarp();
+      sp[lane * G + warp] = pa;
+      sp[(lane + 32) * G + warp] = pb;
       if (lane == 0) {
-        const float corr = expf(m_old - m_new);  // 0 on the first sub-chunk
+        const float corr = exp2f(m_old - m_new);  // 0 on the first sub-chunk
         scorr[warp] = corr;
         sl[warp] = sl[warp] * corr + sum;
         sm_[warp] = m_new;
       }
     }
     __syncthreads();
-    // weighted values
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (k >= ppt) break;
-      const int pi = pi0 + k * kThreads;
-      if (pi >= npairs) break;
-      const int g = pi / (D / 2), c = 2 * (pi % (D / 2));
-      const float corr = scorr[g];
-      float a0 = acc[k][0] * corr, a1 = acc[k][1] * corr;
-      for (int j = kg; j < rows; j += ks) {
-        const float pj = ss[g * kSub + j];
-        const float2 v = ld2(V + j * D + c);
-        a0 = fmaf(pj, v.x, a0);
-        a1 = fmaf(pj, v.y, a1);
+    for (int g = 0; g < G; ++g) {
+      const float c = scorr[g];
+      acc[g] = fma_f32x2(acc[g], f32x2(c, c), 0ull);
+    }
+    for (int j = kg; j < rows; j += Cfg::kKeyGroups) {
+      const uint64_t v2 = ld2p(V + j * D + 2 * cp);
+      float pw[G];
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int g = 0; g < G; g += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(sp + j * G + g);
+          pw[g] = x.x;
+          pw[g + 1] = x.y;
+          pw[g + 2] = x.z;
+          pw[g + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) pw[g] = sp[j * G + g];
       }
-      acc[k][0] = a0;
-      acc[k][1] = a1;
+#pragma unroll
+      for (int g = 0; g < G; ++g) acc[g] = fma_f32x2(f32x2(pw[g], pw[g]), v2, acc[g]);
     }
     __syncthreads();  // stage st is free again
     if (tid == 0 && issued < n_sub) issue(issued++);
   }
 
-  // combine the key groups and write this split's partial result
-  float* out = p.part + (static_cast<int64_t>(b) * p.Hq + hk * G) * p.nsplit * (D + 2);
+  // sum the key groups (in the now idle stage buffers) and write this split's partial
+  float* red = reinterpret_cast<float*>(smem);  // [kKeyGroups][G][D]
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    if (k >= ppt) break;
-    const int pi = pi0 + k * kThreads;
-    if (pi >= npairs) break;
-    if (ks > 1) {
-      sred[(kg * nact + pi0) * 2] = acc[k][0];
-      sred[(kg * nact + pi0) * 2 + 1] = acc[k][1];
-    }
+  for (int g = 0; g < G; ++g) {
+    float a0, a1;
+    f32x2_split(acc[g], a0, a1);
+    red[(kg * G + g) * D + 2 * cp] = a0;
+    red[(kg * G + g) * D + 2 * cp + 1] = a1;
   }
   __syncthreads();
+  float* out = p.part + (static_cast<int64_t>(b) * p.Hq + hk * G) * p.nsplit * (D + 2);
+  for (int x = tid; x < G * D; x += kThreads) {
+    const int g = x / D, c = x % D;
+    float a = 0.f;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    if (k >= ppt) break;
-    const int pi = pi0 + k * kThreads;
-    if (pi >= npairs || kg != 0) break;
-    float a0 = acc[k][0], a1 = acc[k][1];
-    if (ks > 1) {
-      a0 = a1 = 0.f;
-      for (int x = 0; x < ks; ++x) {
-        a0 += sred[(x * nact + pi0) * 2];
-        a1 += sred[(x * nact + pi0) * 2 + 1];
-      }
-    }
-    const int g = pi / (D / 2), c = 2 * (pi % (D / 2));
-    float* row = out + (static_cast<int64_t>(g) * p.nsplit + split) * (D + 2);
-    row[c] = a0;
-    row[c + 1] = a1;
+    for (int k = 0; k < Cfg::kKeyGroups; ++k) a += red[(k * G + g) * D + c];
+    out[(static_cast<int64_t>(g) * p.nsplit + split) * (D + 2) + c] = a;
   }
   if (tid < G) {
     float* row = out + (static_cast<int64_t>(tid) * p.nsplit + split) * (D + 2);
@@ -325,7 +328,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
   }
 }
 
-// Merge the splits of every (batch, query head): one warp each.
+// Merge the splits of every (batch, query head): one warp each.  Maxima are in log2
+// units; LSE is returned in natural-log units.
 template <typename In, int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecParams p) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecParams p) 
       const float* r = part + c * (D + 2);
       const float l = r[D + 1];
       if (!(l > 0.f)) continue;
-      const float w = expf(r[D] - M);
+      const float w = exp2f(r[D] - M);
       L = fmaf(l, w, L);
 #pragma unroll
       for (int x = 0; x < D / 32; ++x) acc[x] = fmaf(r[x * 32 + lane], w, acc[x]);
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecParams p) 
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
   for (int x = 0; x < D / 32; ++x) st1(o + x * 32 + lane, acc[x] * inv);
-  if (lane == 0 && p.lse) p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
+  if (lane == 0 && p.lse) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 // Ring-buffer append: slot pos[b] % cap of every (b, kv head) gets the new row.
@@ -370,31 +374,42 @@ __global__ void kv_append_kernel(In* Kc, In* Vc, const In* kn, const In* vn, con
   }
 }
 
-template <typename In, int D>
-cudaError_t launch_decode_typed(const DecParams& p, cudaStream_t st) {
-  using Cfg = DecCfg<In, D>;
+template <typename In, int D, int G>
+cudaError_t launch_decode_g(const DecParams& p, cudaStream_t st) {
+  using Cfg = DecCfg<In, D, G>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_kernel<In, D>,
+    attr_err = cudaFuncSetAttribute(decode_kernel<In, D, G>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t ctas = static_cast<int64_t>(p.B) * p.Hkv * p.nsplit;
-  decode_kernel<In, D><<<static_cast<unsigned>(ctas), kThreads, Cfg::kSmemBytes, st>>>(p);
+  decode_kernel<In, D, G><<<static_cast<unsigned>(ctas), kThreads, Cfg::kSmemBytes, st>>>(p);
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq;
   decode_combine_kernel<In, D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 
+template <typename In, int D>
+cudaError_t launch_decode_typed(const DecParams& p, cudaStream_t st) {
+  switch (p.G) {
+    case 1: return launch_decode_g<In, D, 1>(p, st);
+    case 2: return launch_decode_g<In, D, 2>(p, st);
+    case 4: return launch_decode_g<In, D, 4>(p, st);
+    case 8: return launch_decode_g<In, D, 8>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
 int decode_splits(int64_t B, int64_t Hkv, int64_t cap) {
-  // enough CTAs for ~6 per SM (3 resident x 2 waves), each at least one sub-chunk
+  // about 6 CTAs per SM over the launch, each at least one sub-chunk
   const int64_t target = 148 * 6;
   const int64_t per = (target + B * Hkv - 1) / (B * Hkv);
-  const int64_t max_split = (cap + kSub - 1) / kSub;
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(per, std::min<int64_t>(max_split, 64))));
+  const int64_t most = (cap + kSub - 1) / kSub;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(per, std::min<int64_t>(most, 64))));
 }
 
 int64_t decode_span(int64_t cap, int nsplit) {

@@ -744,8 +744,8 @@ namespace {
 spattn_status decode_shape(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap, int64_t window,
                            int32_t d, spattn_dtype dtype) {
   if (B < 1 || Hq < 1 || Hkv < 1) return fail(SPATTN_ERR_SHAPE, "B, Hq and Hkv must be >= 1");
-  if (Hq % Hkv != 0 || Hq / Hkv > 8)
-    return fail(SPATTN_ERR_SHAPE, "Hq must be a multiple of Hkv with Hq / Hkv <= 8");
+  if (Hq % Hkv != 0 || (Hq / Hkv != 1 && Hq / Hkv != 2 && Hq / Hkv != 4 && Hq / Hkv != 8))
+    return fail(SPATTN_ERR_SHAPE, "Hq / Hkv must be 1, 2, 4 or 8");
   if (int64_t(B) * Hkv > (int64_t(1) << 24)) return fail(SPATTN_ERR_SHAPE, "B * Hkv too large");
   if (cap < 1 || cap > (int64_t(1) << 30)) return fail(SPATTN_ERR_SHAPE, "cap must be in [1, 2^30]");
   if (window < 0 || window > cap)
