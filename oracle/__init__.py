@@ -38,7 +38,7 @@ def build(force: bool = False) -> str:
 
 
 def _configure(lib):
-    spec = [ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64, _i32p, _i64]
+    spec = [ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64, _i32p, _i64, _i64, _i64, _i32p]
     lib.oracle_validate.argtypes = spec
     lib.oracle_validate.restype = ctypes.c_int
     lib.oracle_allowed.argtypes = spec + [_i64, _i64]
@@ -107,7 +107,7 @@ class Mask:
     columns, globals."""
 
     def __init__(self, T, causal=1, window=0, radius=-1, stride=0, offset=0,
-                 global_pos=(), dilation=1):
+                 global_pos=(), dilation=1, rand_block=0, rand_pairs=()):
         self.T = int(T)
         self.causal = int(causal)
         self.window = int(window)
@@ -116,15 +116,20 @@ class Mask:
         self.stride = int(stride)
         self.offset = int(offset)
         self.gpos = np.ascontiguousarray(np.asarray(global_pos, dtype=np.int32))
+        self.rand_block = int(rand_block)
+        rp = np.asarray(rand_pairs, dtype=np.int32).reshape(-1, 2)
+        self.rand_pairs = np.ascontiguousarray(rp)
 
     @classmethod
     def from_params(cls, T, p):
         return cls(T, p["causal"], p["window"], p["radius"], p["stride"], p["offset"],
-                   p.get("global_pos", ()), p.get("dilation", 1))
+                   p.get("global_pos", ()), p.get("dilation", 1), p.get("rand_block", 0),
+                   p.get("rand_pairs", ()))
 
     def _args(self):
         return (self.causal, self.window, self.radius, self.dilation, self.stride, self.offset,
-                len(self.gpos), self.gpos.ctypes.data_as(_i32p), self.T)
+                len(self.gpos), self.gpos.ctypes.data_as(_i32p), self.T, self.rand_block,
+                len(self.rand_pairs), self.rand_pairs.ctypes.data_as(_i32p))
 
     def validate(self) -> int:
         return _load().oracle_validate(*self._args())

@@ -29,6 +29,11 @@
  *       query ("Attention variants" §4 with_global; ai360xpert "Sparse Attention",
  *       §Global tokens).  In a causal mask both stay causal ("Attention variants",
  *       the look-ahead warning after with_global).
+ *     - random blocks (BigBird, getnybble "Sparse and sliding-window attention",
+ *       §Block-sparse attention: BigBird): with block size b, a list of (query block,
+ *       key block) pairs; query i reads every key j with (i / b, j / b) in the list
+ *       (causal: j <= i).  Which blocks are random is an input (drawn by a seeded
+ *       generator outside), so the rule itself is deterministic.
  *
  *   Attention.  For each query i with allowed set S_i (never empty: j = i is always
  *   allowed),
@@ -64,13 +69,16 @@ typedef struct {
   int64_t n_global;
   const int32_t* global_pos; /* sorted ascending, distinct */
   int64_t T;
+  int64_t rand_block;        /* random-block size b (0 = no random blocks) */
+  int64_t n_rand;
+  const int32_t* rand_pairs; /* [n_rand][2] (query block, key block), sorted, distinct */
 } omask;
 
 /* ---- spec checks: the readings every valid mask obeys ------------------------- */
 
 /* Returns 0 for a valid mask, a negative code naming the first violated rule. */
 int oracle_validate(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
-                    int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T) {
+                    int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T, int64_t rand_block, int64_t n_rand, const int32_t* rand_pairs) {
   if (T <= 0) return -1;
   if (causal != 0 && causal != 1) return -2;
   if (causal == 1 && (window < 0 || radius != -1)) return -3;
@@ -87,6 +95,39 @@ int oracle_validate(int causal, int64_t window, int64_t radius, int64_t dilation
     if (gpos[a] < 0 || gpos[a] >= T) return -8;
     if (a > 0 && gpos[a] <= gpos[a - 1]) return -9; /* sorted, distinct */
   }
+  if (n_rand < 0) return -11;
+  if (n_rand > 0) {
+    if (rand_block != 16 && rand_block != 32 && rand_block != 64 && rand_block != 128)
+      return -11;
+    const int64_t nb = (T + rand_block - 1) / rand_block;
+    for (int64_t a = 0; a < n_rand; a++) {
+      const int64_t q = rand_pairs[2 * a], k = rand_pairs[2 * a + 1];
+      if (q < 0 || q >= nb || k < 0 || k >= nb) return -12;
+      if (a > 0) { /* sorted by (query block, key block), distinct */
+        const int64_t pq = rand_pairs[2 * a - 2], pk = rand_pairs[2 * a - 1];
+        if (q < pq || (q == pq && k <= pk)) return -13;
+      }
+    }
+  }
+  return 0;
+}
+
+/* Index of the first random pair whose query block is >= qb (pairs are sorted). */
+static int64_t rand_lower(const omask* m, int64_t qb) {
+  int64_t lo = 0, hi = m->n_rand;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) / 2;
+    if (m->rand_pairs[2 * mid] < qb) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+/* Is (i, j) inside one of the random blocks of i's query block? */
+static int in_random(const omask* m, int64_t i, int64_t j) {
+  if (m->n_rand == 0) return 0;
+  const int64_t qb = i / m->rand_block, kb = j / m->rand_block;
+  for (int64_t a = rand_lower(m, qb); a < m->n_rand && m->rand_pairs[2 * a] == qb; a++)
+    if (m->rand_pairs[2 * a + 1] == kb) return 1;
   return 0;
 }
 
@@ -103,6 +144,7 @@ static int allowed(const omask* m, int64_t i, int64_t j) {
   if (in_global(m, i)) return 1;                /* a global row reads every key */
   if (in_global(m, j)) return 1;                /* every query reads a global column */
   if (m->stride > 0 && j % m->stride == m->offset) return 1; /* strided column */
+  if (in_random(m, i, j)) return 1;             /* a random block of i's query block */
   const int64_t gap = i - j;
   if (llabs(gap) % m->dilation != 0) return 0;                  /* every d-th key only */
   if (m->causal) return m->window == 0 || gap < m->window * m->dilation; /* 0 <= i-j < w d */
@@ -110,9 +152,10 @@ static int allowed(const omask* m, int64_t i, int64_t j) {
 }
 
 int oracle_allowed(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
-                   int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
+                   int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T, int64_t rand_block, int64_t n_rand, const int32_t* rand_pairs,
                    int64_t i, int64_t j) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
   return allowed(&m, i, j);
 }
 
@@ -149,24 +192,39 @@ static int64_t row_set_union(const omask* m, int64_t i, int32_t* out) {
   }
   if (lo < 0) lo = 0;
   if (hi > jmax) hi = jmax;
-  /* three ascending streams: strided progression, global columns, local interval */
+  /* four ascending streams: strided progression, global columns, local interval,
+   * the columns of the random key blocks of i's query block (in key-block order) */
   int64_t js = (m->stride > 0) ? m->offset : T; /* next strided column */
   int64_t ag = 0;                                /* next global index */
   int64_t jl = lo + (i - lo) % m->dilation;       /* next local column (lo <= i) */
+  const int64_t qb = m->n_rand ? i / m->rand_block : -1;
+  int64_t ar = m->n_rand ? rand_lower(m, qb) : 0; /* current random pair */
+  int64_t jr = (ar < m->n_rand && m->rand_pairs[2 * ar] == qb)
+                   ? m->rand_pairs[2 * ar + 1] * m->rand_block : INT64_MAX;
   int64_t last = -1;
   for (;;) {
     int64_t cs = (js <= jmax) ? js : INT64_MAX;
     int64_t cg = (ag < m->n_global && m->global_pos[ag] <= jmax) ? m->global_pos[ag]
                                                                   : INT64_MAX;
     int64_t cl = (jl <= hi) ? jl : INT64_MAX;
+    int64_t cr = (jr <= jmax && jr < T) ? jr : INT64_MAX;
     int64_t c = cs < cg ? cs : cg;
     if (cl < c) c = cl;
+    if (cr < c) c = cr;
     if (c == INT64_MAX) break;
     if (c != last) out[n++] = (int32_t)c;
     last = c;
     if (c == cs) js += m->stride;
     if (c == cg) ag++;
     if (c == cl) jl += m->dilation;
+    if (c == cr) { /* next column of this block, or the first of the next block */
+      jr++;
+      if (jr % m->rand_block == 0 || jr >= T) {
+        ar++;
+        jr = (ar < m->n_rand && m->rand_pairs[2 * ar] == qb)
+                 ? m->rand_pairs[2 * ar + 1] * m->rand_block : INT64_MAX;
+      }
+    }
   }
   return n;
 }
@@ -174,17 +232,20 @@ static int64_t row_set_union(const omask* m, int64_t i, int32_t* out) {
 /* Allowed set of one query, ascending.  method 0: union of rule sets, 1: full scan.
  * `out` must hold T entries.  Returns |S_i|. */
 int64_t oracle_row_set(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
-                       int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
+                       int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T, int64_t rand_block, int64_t n_rand, const int32_t* rand_pairs,
                        int64_t i, int method, int32_t* out) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
   return method ? row_set_scan(&m, i, out) : row_set_union(&m, i, out);
 }
 
 /* Number of allowed (i, j) pairs: the sum of |S_i| (the glossary's edge count E). */
 int64_t oracle_count_pairs(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                            int64_t offset, int64_t n_global, const int32_t* gpos,
-                           int64_t T) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+                           int64_t T, int64_t rand_block, int64_t n_rand,
+                           const int32_t* rand_pairs) {
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
   int64_t total = 0;
 #pragma omp parallel
   {
@@ -199,9 +260,10 @@ int64_t oracle_count_pairs(int causal, int64_t window, int64_t radius, int64_t d
 /* Histogram of allowed pairs into BM x BN tiles: cnt[(i/BM) * nkb + (j/BN)].
  * `cnt` has ceil(T/BM) * ceil(T/BN) int32 entries and is overwritten. */
 void oracle_tile_counts(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
-                        int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T,
+                        int64_t offset, int64_t n_global, const int32_t* gpos, int64_t T, int64_t rand_block, int64_t n_rand, const int32_t* rand_pairs,
                         int64_t BM, int64_t BN, int32_t* cnt) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
   const int64_t nqb = (T + BM - 1) / BM, nkb = (T + BN - 1) / BN;
   memset(cnt, 0, sizeof(int32_t) * (size_t)(nqb * nkb));
 #pragma omp parallel
@@ -235,11 +297,13 @@ static double load_elem(const void* p, int dtype, int64_t idx) {
  * O: [n_rows][d] fp64, LSE: [n_rows] fp64 (natural log).  Returns total |S_i|. */
 int64_t oracle_attention_head(int causal, int64_t window, int64_t radius, int64_t dilation, int64_t stride,
                               int64_t offset, int64_t n_global, const int32_t* gpos,
-                              int64_t T, int64_t d, int dtype, const void* Q,
+                              int64_t T, int64_t rand_block, int64_t n_rand,
+                              const int32_t* rand_pairs, int64_t d, int dtype, const void* Q,
                               const void* K, const void* V, double scale,
                               const int64_t* rows, int64_t n_rows, double* O,
                               double* LSE) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
   int64_t total = 0;
 #pragma omp parallel
   {
@@ -342,10 +406,11 @@ static void bwd_row(const omask* m, int64_t i, int64_t d, int dtype, const void*
  * overwritten.  Sequential over rows (dK and dV gather from every row). */
 void oracle_attention_bwd_head(int causal, int64_t window, int64_t radius, int64_t dilation,
                                int64_t stride, int64_t offset, int64_t n_global,
-                               const int32_t* gpos, int64_t T, int64_t d, int dtype,
+                               const int32_t* gpos, int64_t T, int64_t rand_block, int64_t n_rand, const int32_t* rand_pairs, int64_t d, int dtype,
                                const void* Q, const void* K, const void* V, const void* dO,
                                double scale, double* dQ, double* dK, double* dV) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
   int32_t* set = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
   double* a = (double*)malloc(sizeof(double) * (size_t)T);
   double* da = (double*)malloc(sizeof(double) * (size_t)T);
@@ -363,11 +428,12 @@ void oracle_attention_bwd_head(int causal, int64_t window, int64_t radius, int64
  * parallel. */
 void oracle_attention_bwd_dq_rows(int causal, int64_t window, int64_t radius, int64_t dilation,
                                   int64_t stride, int64_t offset, int64_t n_global,
-                                  const int32_t* gpos, int64_t T, int64_t d, int dtype,
+                                  const int32_t* gpos, int64_t T, int64_t rand_block, int64_t n_rand, const int32_t* rand_pairs, int64_t d, int dtype,
                                   const void* Q, const void* K, const void* V, const void* dO,
                                   double scale, const int64_t* rows, int64_t n_rows,
                                   double* dQ_rows) {
-  omask m = {causal, window, radius, dilation, stride, offset, n_global, gpos, T};
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
 #pragma omp parallel
   {
     int32_t* set = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);

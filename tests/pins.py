@@ -32,15 +32,24 @@ GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
 def mask_of(e) -> oracle.Mask:
     return oracle.Mask(e["T"], e.get("causal", 1), e.get("window", 0),
                        e.get("radius", -1), e.get("stride", 0), e.get("offset", 0),
-                       e.get("global_pos", []), e.get("dilation", 1))
+                       e.get("global_pos", []), e.get("dilation", 1), e.get("rand_block", 0),
+                       e.get("rand_pairs", ()))
+
+
+def dense_of(e) -> np.ndarray:
+    return np_dense_mask(e["T"], e.get("causal", 1), e.get("window", 0), e.get("radius", -1),
+                         e.get("stride", 0), e.get("offset", 0), e.get("global_pos", []),
+                         e.get("dilation", 1), e.get("rand_block", 0), e.get("rand_pairs", ()))
 
 
 # ---------------------------------------------------------------- independent rules
 
-def np_dense_mask(T, causal, window, radius, stride, offset, gpos, dilation=1) -> np.ndarray:
+def np_dense_mask(T, causal, window, radius, stride, offset, gpos, dilation=1, rand_block=0,
+                  rand_pairs=()) -> np.ndarray:
     """Dense boolean mask, True = may attend, from index grids (independent of oracle.c).
     The dilated local rule is the "Attention variants" exercise's dilated(n, w, d):
-    gap >= 0, gap % d == 0, gap < w d (bidirectional: |gap| <= r d, |gap| % d == 0)."""
+    gap >= 0, gap % d == 0, gap < w d (bidirectional: |gap| <= r d, |gap| % d == 0).
+    Random blocks (BigBird): the b x b blocks (query block, key block) listed."""
     i, j = np.indices((T, T))
     past = j <= i
     gap = i - j
@@ -59,6 +68,13 @@ def np_dense_mask(T, causal, window, radius, stride, offset, gpos, dilation=1) -
     grow = np.broadcast_to(g[:, None], (T, T))
     m |= (gcol & past) if causal else gcol
     m |= (grow & past) if causal else grow
+    if rand_block and len(rand_pairs):
+        nb = -(-T // rand_block)
+        blk = np.zeros((nb, nb), dtype=bool)
+        rp = np.asarray(rand_pairs, dtype=np.int64).reshape(-1, 2)
+        blk[rp[:, 0], rp[:, 1]] = True
+        r = blk[i // rand_block, j // rand_block]
+        m |= (r & past) if causal else r
     return m
 
 
@@ -143,7 +159,25 @@ def small_specs(seed=0, n=60):
         dilation = int(rng.choice([1, 1, 1, 2, 3, 5]))
         out.append(dict(T=T, causal=causal, window=window, radius=radius, stride=stride,
                         offset=offset, global_pos=gpos, dilation=dilation))
+    # random blocks on a third of the specs, from a stream of their own (the draws
+    # above stay what they were)
+    rr = np.random.default_rng(seed + 1000)
+    for e in out:
+        if rr.random() < 1 / 3:
+            e["rand_block"], e["rand_pairs"] = random_blocks(e["T"], int(rr.choice([16, 32])),
+                                                             int(rr.integers(1, 4)), rr)
     return out
+
+
+def random_blocks(T, b, R, rng):
+    """BigBird-style random blocks: for every query block, R distinct key blocks drawn
+    uniformly from all blocks (fewer when there are fewer blocks); sorted pairs."""
+    nb = -(-T // b)
+    pairs = []
+    for q in range(nb):
+        for k in sorted(rng.choice(nb, size=min(R, nb), replace=False).tolist()):
+            pairs.append((q, int(k)))
+    return b, pairs
 
 
 # ---------------------------------------------------------------- count / set pins
@@ -265,8 +299,7 @@ def check_against_numpy_rules(seed=0):
         if m.validate() != 0:
             bad.append(f"valid spec rejected: {e}")
             continue
-        D = np_dense_mask(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
-                          e["offset"], e["global_pos"], e["dilation"])
+        D = dense_of(e)
         for i in range(e["T"]):
             u = m.row_set(i, "union").tolist()
             s = m.row_set(i, "scan").tolist()
@@ -276,8 +309,9 @@ def check_against_numpy_rules(seed=0):
                 break
         if m.count_pairs() != int(D.sum()):
             bad.append(f"count of {e}")
-        if closed_form_pairs(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
-                             e["offset"], e["global_pos"], e["dilation"]) != int(D.sum()):
+        if not e.get("rand_pairs") and closed_form_pairs(
+                e["T"], e["causal"], e["window"], e["radius"], e["stride"], e["offset"],
+                e["global_pos"], e["dilation"]) != int(D.sum()):
             bad.append(f"closed form of {e}")
         for BM, BN in [(4, 4), (8, 16), (128, 128)]:
             cnt = m.tile_counts(BM, BN)
@@ -291,8 +325,43 @@ def check_against_numpy_rules(seed=0):
     return bad
 
 
+def check_bigbird_cost():
+    """"Sparse and sliding-window attention", §Block-sparse attention: BigBird: a token
+    pays W + R + G instead of N, with block 64, W = 3 blocks = 192, R = 3 random blocks
+    and G = 2 global blocks.  Causal reading: window 192, the first 128 tokens global,
+    three random key blocks per query block drawn from the blocks that lie wholly before
+    the query block's window and after the global blocks, so the rules do not overlap:
+    every non-global row i >= 5 * 64 + 192 reads exactly 192 + 3 * 64 + 128 = 512 keys."""
+    bad = []
+    T, b = 2048, 64
+    rng = np.random.default_rng(11)
+    pairs = []
+    for q in range(T // b):
+        first_window_block = max(0, (q * b - 191) // b)
+        cand = [k for k in range(2, first_window_block)]
+        if len(cand) >= 3:
+            pairs += [(q, int(k)) for k in sorted(rng.choice(cand, 3, replace=False))]
+    m = oracle.Mask(T, 1, 192, -1, 0, 0, list(range(128)), 1, b, pairs)
+    if m.validate() != 0:
+        return ["BigBird spec rejected"]
+    have = {q for q, _ in pairs}
+    for i in range(5 * b + 192, T, 37):
+        if i // b not in have:
+            continue
+        n = len(m.row_set(i))
+        if n != 512:
+            bad.append(f"BigBird row {i}: {n} keys, page cost W + R + G = 512")
+    if not bad and not any(i // b in have for i in range(5 * b + 192, T, 37)):
+        bad.append("no eligible BigBird row")
+    return bad
+
+
 def check_rejects_invalid():
     bad = []
+    for rb, pairs in [(48, [(0, 0)]), (16, [(0, 5)]), (16, [(1, 0), (0, 0)]),
+                      (16, [(0, 1), (0, 1)]), (16, [(-1, 0)])]:
+        if oracle.Mask(40, 0, 0, 2, 0, 0, [], 1, rb, pairs).validate() == 0:
+            bad.append(f"invalid random blocks accepted: {rb} {pairs}")
     cases = [
         dict(T=0), dict(T=8, causal=2), dict(T=8, causal=1, window=-1),
         dict(T=8, causal=1, radius=2), dict(T=8, causal=0, radius=-2),
@@ -353,9 +422,7 @@ def check_sdpa_masked(seed=5):
         d = 8 + 8 * (n % 3)
         Q, K, V = _rand(T, d, 100 + n)
         sc = 0.7 / math.sqrt(d)
-        D = torch.from_numpy(np_dense_mask(T, e["causal"], e["window"], e["radius"],
-                                           e["stride"], e["offset"], e["global_pos"],
-                                           e["dilation"]))
+        D = torch.from_numpy(dense_of(e))
         q, k, v = (x.double()[None, None] for x in (Q, K, V))
         ref = torch.nn.functional.scaled_dot_product_attention(
             q, k, v, attn_mask=D[None, None], scale=sc)[0, 0].numpy()
@@ -446,9 +513,7 @@ def check_bwd_autograd(seed=21):
         g = torch.Generator().manual_seed(300 + n)
         Q, K, V, dO = (torch.randn(T, d, generator=g) for _ in range(4))
         sc = 0.6 / math.sqrt(d)
-        D = torch.from_numpy(np_dense_mask(T, e["causal"], e["window"], e["radius"],
-                                           e["stride"], e["offset"], e["global_pos"],
-                                           e["dilation"]))
+        D = torch.from_numpy(dense_of(e))
         q, k, v = (x.double().requires_grad_(True) for x in (Q, K, V))
         y = torch.nn.functional.scaled_dot_product_attention(
             q[None, None], k[None, None], v[None, None], attn_mask=D[None, None],
@@ -592,5 +657,5 @@ BWD_CHECKS = [check_bwd_autograd, check_bwd_finite_differences, check_bwd_invari
 
 COUNT_CHECKS = [check_page_counts, check_row_sets, check_reach, check_edge_formula,
                 check_dilated_counts, check_causal_equivalences, check_against_numpy_rules,
-                check_rejects_invalid]
+                check_rejects_invalid, check_bigbird_cost]
 ATTENTION_CHECKS = [check_sdpa_dense, check_sdpa_masked, check_special_values]

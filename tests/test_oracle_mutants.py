@@ -33,6 +33,13 @@ MUTANTS = {
     "lse_sign": ("LSE[r] = mx + log(l);", "LSE[r] = mx - log(l);"),
     "value_of_query_row": ("load_elem(V, dtype, j * d + k)", "load_elem(V, dtype, i * d + k)"),
     "key_transposed": ("load_elem(K, dtype, j * d + k)", "load_elem(K, dtype, k * d + j % d)"),
+    "random_ignored": ("if (in_random(m, i, j)) return 1;", ""),
+    "random_not_causal_in_set": ("int64_t cr = (jr <= jmax && jr < T) ? jr : INT64_MAX;",
+                                 "int64_t cr = (jr < T) ? jr : INT64_MAX;"),
+    "random_transposed": ("const int64_t qb = i / m->rand_block, kb = j / m->rand_block;",
+                          "const int64_t qb = j / m->rand_block, kb = i / m->rand_block;"),
+    "random_block_short": ("if (jr % m->rand_block == 0 || jr >= T)",
+                           "if (jr % m->rand_block == m->rand_block - 1 || jr >= T)"),
     "first_key_skipped": ("for (int64_t a = 0; a < n; a++) l +=", "for (int64_t a = 1; a < n; a++) l +="),
 }
 
