@@ -66,6 +66,10 @@ def mask_desc(p):
         s += f", stride={p['stride']} offset={p['offset']}"
     if len(p["global_pos"]):
         s += f", {len(p['global_pos'])} global tokens"
+    if p.get("dilation", 1) > 1:
+        s += f", dilation {p['dilation']}"
+    if p.get("rand_block"):
+        s += f", {len(p['rand_pairs'])} random blocks of {p['rand_block']}"
     return s
 
 

@@ -56,11 +56,12 @@ typedef enum { SPATTN_BF16 = 0, SPATTN_FP32 = 1 } spattn_dtype;
 /*
  * Mask specification.  Allowed pairs (i, j), 0 <= i, j < T, with d = dilation:
  *   causal = 1:  j <= i and ((i-j) % d == 0 and (i-j < window*d or window == 0)
- *                 or j strided or j global or i global)
+ *                 or j strided or j global or i global or (i, j) random)
  *   causal = 0:  (|i-j| % d == 0 and (|i-j| <= radius*d or radius == -1))
- *                 or j strided or j global or i global
- * where "j strided" means stride > 0 and j % stride == stride_offset, and
- * "global" means a member of global_pos.
+ *                 or j strided or j global or i global or (i, j) random
+ * where "j strided" means stride > 0 and j % stride == stride_offset, "global"
+ * means a member of global_pos, and "(i, j) random" means the pair
+ * (i / rand_block, j / rand_block) is listed in rand_pairs.
  * Sources: window counts the query itself (glossary, "Choose the available
  * reads": S_i = {max(1,i-w+1),...,i}); window 0 is the full causal triangle and
  * strided columns are read by every later query (octlm.ramaa.tech "Sparse
@@ -79,7 +80,13 @@ typedef enum { SPATTN_BF16 = 0, SPATTN_FP32 = 1 } spattn_dtype;
  * when stride == 0); 0 <= n_global <= T; global_pos is a HOST array of n_global
  * distinct positions in [0, T), any order (it is copied; the caller keeps
  * ownership); 0 <= dilation <= 2^31, and with dilation > 1 window and radius at
- * most 2^31.  Anything else is SPATTN_ERR_INVALID_SPEC.
+ * most 2^31.  Random blocks (BigBird's random connections, "Sparse and
+ * sliding-window attention", section "Block-sparse attention: BigBird"): n_rand
+ * >= 0 pairs (query block, key block) in a HOST array rand_pairs[2 * n_rand], any
+ * order, distinct, each block index in [0, ceil(T / rand_block)); rand_block one of
+ * 16, 32, 64, 128 when n_rand > 0 (ignored otherwise).  Which blocks are random is
+ * the caller's draw: the library takes the list as given.  Anything else is
+ * SPATTN_ERR_INVALID_SPEC.
  */
 typedef struct {
   int32_t causal;
@@ -90,6 +97,9 @@ typedef struct {
   int32_t n_global;
   const int32_t* global_pos;
   int64_t dilation;
+  int32_t rand_block;
+  int64_t n_rand;
+  const int32_t* rand_pairs;
 } spattn_mask_spec;
 
 typedef struct spattn_plan spattn_plan; /* opaque, owned by the library */

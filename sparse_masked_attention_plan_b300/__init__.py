@@ -44,7 +44,9 @@ class MaskSpec(ctypes.Structure):
     _fields_ = [("causal", ctypes.c_int32), ("window", ctypes.c_int64),
                 ("radius", ctypes.c_int64), ("stride", ctypes.c_int64),
                 ("stride_offset", ctypes.c_int64), ("n_global", ctypes.c_int32),
-                ("global_pos", ctypes.POINTER(ctypes.c_int32)), ("dilation", ctypes.c_int64)]
+                ("global_pos", ctypes.POINTER(ctypes.c_int32)), ("dilation", ctypes.c_int64),
+                ("rand_block", ctypes.c_int32), ("n_rand", ctypes.c_int64),
+                ("rand_pairs", ctypes.POINTER(ctypes.c_int32))]
 
 
 _lib = None
@@ -116,12 +118,17 @@ def _check(status: int):
         raise SpattnError(status, lib().spattn_last_error().decode())
 
 
-def make_spec(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=(), dilation=1):
-    """(MaskSpec, keepalive array) for the mask fields (see include/spattn.h)."""
+def make_spec(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=(), dilation=1,
+              rand_block=0, rand_pairs=()):
+    """(MaskSpec, keepalive arrays) for the mask fields (see include/spattn.h).
+    rand_pairs: (query block, key block) pairs of BigBird random blocks of size
+    rand_block."""
     g = np.ascontiguousarray(np.asarray(global_pos, dtype=np.int32))
+    r = np.ascontiguousarray(np.asarray(rand_pairs, dtype=np.int32).reshape(-1, 2))
     spec = MaskSpec(int(causal), int(window), int(radius), int(stride), int(offset), len(g),
-                    g.ctypes.data_as(_i32p) if len(g) else None, int(dilation))
-    return spec, g
+                    g.ctypes.data_as(_i32p) if len(g) else None, int(dilation),
+                    int(rand_block), len(r), r.ctypes.data_as(_i32p) if len(r) else None)
+    return spec, (g, r)
 
 
 def validate(T, **mask) -> int:
@@ -141,14 +148,16 @@ class Plan:
     """Block-sparse plan of one mask for sequence length T (owns device memory)."""
 
     def __init__(self, T, head_dim, causal=1, window=0, radius=-1, stride=0, offset=0,
-                 global_pos=(), dilation=1, stream=None):
+                 global_pos=(), dilation=1, rand_block=0, rand_pairs=(), stream=None):
         self.T = int(T)
         self.head_dim = int(head_dim)
         self.mask = dict(causal=int(causal), window=int(window), radius=int(radius),
                          stride=int(stride), offset=int(offset),
                          global_pos=np.asarray(global_pos, dtype=np.int32),
-                         dilation=int(dilation))
-        spec, keep = make_spec(causal, window, radius, stride, offset, global_pos, dilation)
+                         dilation=int(dilation), rand_block=int(rand_block),
+                         rand_pairs=np.asarray(rand_pairs, dtype=np.int32).reshape(-1, 2))
+        spec, keep = make_spec(causal, window, radius, stride, offset, global_pos, dilation,
+                               rand_block, rand_pairs)
         h = _vp()
         _check(lib().spattn_plan_create(ctypes.byref(spec), self.T, self.head_dim,
                                         _stream_handle(stream), ctypes.byref(h)))

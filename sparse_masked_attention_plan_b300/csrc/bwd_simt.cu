@@ -193,6 +193,14 @@ struct KvCfg {
   static constexpr int kSmemBytes = (2 * kBwdRows * kRowStride + 2 * kBwdRows) * 4 + kBwdRows * 4;
 };
 
+__device__ __forceinline__ bool in_random(const MaskDev& m, long long i, long long j) {
+  if (m.rand_block == 0) return false;
+  const int q = static_cast<int>(i / m.rand_block), k = static_cast<int>(j / m.rand_block);
+  for (int x = m.r_off[q]; x < m.r_off[q + 1]; ++x)
+    if (m.r_kb[x] == k) return true;
+  return false;
+}
+
 __device__ __forceinline__ bool band_allowed(const MaskDev& m, const uint32_t* colmask,
                                              long long i, long long j) {
   const long long gap = i - j;
@@ -206,7 +214,15 @@ __device__ __forceinline__ bool band_allowed(const MaskDev& m, const uint32_t* c
   if (local && m.dilation > 1) local = ((gap % m.dilation) + m.dilation) % m.dilation == 0;
   if (local) return true;
   const uint32_t w = colmask[(j / kTile) * 4 + (j % kTile) / 32];
-  return ((w >> (j & 31)) & 1u) && (!m.causal || j <= i);
+  return (((w >> (j & 31)) & 1u) || in_random(m, i, j)) && (!m.causal || j <= i);
+}
+
+// A key tile reached only by random blocks: the random keys that are not strided or
+// global columns (the packed entries cover those).
+__device__ __forceinline__ bool random_allowed(const MaskDev& m, const uint32_t* colmask,
+                                               long long i, long long j) {
+  const uint32_t w = colmask[(j / kTile) * 4 + (j % kTile) / 32];
+  return !((w >> (j & 31)) & 1u) && in_random(m, i, j) && (!m.causal || j <= i);
 }
 
 template <typename In, int D>
@@ -287,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) dkdv_kernel(const BwdArgs p, int uni
       if (ok) {
         if (kind == kKindPacked) ok = key >= e.z && key < e.w;
         else if (kind == kKindDense) ok = !m.causal || j <= i;
+        else if (kind == kKindRandom) ok = random_allowed(m, p.colmask, i, j);
         else ok = band_allowed(m, p.colmask, i, j);
       }
       const float pij = ok ? expf(s * p.scale - slse[r]) : 0.f;

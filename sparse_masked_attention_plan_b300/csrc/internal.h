@@ -13,7 +13,7 @@ constexpr int kTile = 128;  // BM = BN of the natural grid
 // Entry flag layout (see spattn_plan_copy_schedule in spattn.h).
 constexpr int kActive0 = 1, kActive1 = 2, kFull0 = 4, kFull1 = 8;
 constexpr int kKindShift = 4;
-constexpr int kKindBand = 0, kKindPacked = 1, kKindDense = 2;
+constexpr int kKindBand = 0, kKindPacked = 1, kKindDense = 2, kKindRandom = 3;
 constexpr int kItemGathered = 1;
 
 // Key-major (backward) schedule: a unit is 64 consecutive keys, either natural key
@@ -42,6 +42,9 @@ struct MaskDev {
   const int32_t* gpos;         // sorted distinct global positions [n_global]
   const int32_t* gpos_ns;      // sorted globals that are not strided [n_gns]
   const uint8_t* rowglobal;    // [T] 1 where the row is a global token
+  int32_t rand_block;          // random-block size b (0: no random blocks)
+  const int32_t* r_off;        // [ceil(T/b) + 1] random key blocks of query block q:
+  const int32_t* r_kb;         //   r_kb[r_off[q] .. r_off[q+1]), ascending
 };
 
 struct Schedule {
@@ -68,6 +71,11 @@ struct spattn_plan {
   int device = 0;
   std::vector<int32_t> gpos;     // sorted distinct
   std::vector<int32_t> gpos_ns;  // globals that are not strided columns
+  // random blocks (BigBird): block size and, per query block, its key blocks (CSR)
+  int32_t rand_block = 0;
+  std::vector<int32_t> r_off, r_kb;
+  int32_t* d_roff = nullptr;
+  int32_t* d_rkb = nullptr;
   // natural grid
   int32_t nqb = 0, nkb = 0;
   int64_t pairs = 0, n_full = 0, n_partial = 0, n_empty = 0, n_nonempty = 0;
@@ -123,6 +131,9 @@ struct spattn_plan {
     m.gpos = d_gpos;
     m.gpos_ns = d_gpos_ns;
     m.rowglobal = d_rowglobal;
+    m.rand_block = rand_block;
+    m.r_off = d_roff;
+    m.r_kb = d_rkb;
     return m;
   }
 

@@ -8,7 +8,8 @@
 // * Tile classification: for every (query block, key block) tile of the 128 x 128
 //   grid, the exact number of allowed pairs, from a per-row closed form (interval
 //   intersection for the local rule, arithmetic-progression counts for strided
-//   columns, binary search for global columns), then empty / full / partial.  The
+//   columns, binary search for global columns, per-block additions for BigBird's
+//   random blocks), then empty / full / partial.  The
 //   block-level skipping of "Attention variants", section "Use the library"
 //   (create_block_mask; "never loading zero blocks") rests on this classification;
 //   the per-tile counts sum to the glossary's edge count E ("Sparse attention",
@@ -98,9 +99,10 @@ __device__ int gns_count_grid(const MaskDev& m, int x, int y, int r, int d) {
   return c;
 }
 
-// Allowed keys j in [a, b] for query row i (closed form; a <= b inside [0, T)).
-// The local keys are the j of the local span with (i - j) % dilation == 0.
-__device__ int row_count(const MaskDev& m, int i, int a, int b) {
+// Keys j in [a, b] allowed by the local, strided and global rules for query row i
+// (closed form; a <= b inside [0, T)).  The local keys are the j of the local span
+// with (i - j) % dilation == 0.
+__device__ int row_count_base(const MaskDev& m, int i, int a, int b) {
   const int jmax = m.causal ? i : m.T - 1;
   if (b > jmax) b = jmax;
   if (b < a) return 0;
@@ -127,6 +129,33 @@ __device__ int row_count(const MaskDev& m, int i, int a, int b) {
                  (nl && m.stride > 0 ? crt_count(la, lb, m.offset, m.stride, res, d) : 0);
   const int ng = gns_count(m, a, b) - (nl ? gns_count_grid(m, la, lb, res, d) : 0);
   return nl + ns + ng;
+}
+
+// Allowed keys j in [a, b] for query row i: the rules above plus the random blocks of
+// i's query block, each adding its permitted keys that no other rule allows (the
+// blocks of one row are disjoint, so the additions do not overlap).
+__device__ int row_count(const MaskDev& m, int i, int a, int b) {
+  int c = row_count_base(m, i, a, b);
+  if (m.rand_block == 0 || m.rowglobal[i]) return c;
+  const int jmax = m.causal ? i : m.T - 1;
+  const int q = i / m.rand_block;
+  for (int x = m.r_off[q]; x < m.r_off[q + 1]; ++x) {
+    const int c0 = max(a, m.r_kb[x] * m.rand_block);
+    const int c1 = min(min(b, jmax), m.r_kb[x] * m.rand_block + m.rand_block - 1);
+    if (c0 <= c1) c += (c1 - c0 + 1) - row_count_base(m, i, c0, c1);
+  }
+  return c;
+}
+
+// Does a random block of a query row in [q0, q1] reach a key in [k0, k1]?
+__device__ bool rand_meets(const MaskDev& m, int q0, int q1, int k0, int k1) {
+  if (m.rand_block == 0) return false;
+  for (int q = q0 / m.rand_block; q <= q1 / m.rand_block; ++q)
+    for (int x = m.r_off[q]; x < m.r_off[q + 1]; ++x) {
+      const int c0 = m.r_kb[x] * m.rand_block;
+      if (c0 <= k1 && c0 + m.rand_block - 1 >= k0) return true;
+    }
+  return false;
 }
 
 // Can any (i in [q0,q1], j in [k0,k1]) be allowed by the local rule?  Conservative
@@ -206,7 +235,7 @@ __device__ int tile_count(const MaskDev& m, const uint32_t* colmask, int qb, int
   const int q0 = qb * kTile, q1 = min(q0 + kTile, m.T) - 1;
   const int k0 = kb * kTile, k1 = min(k0 + kTile, m.T) - 1;
   if (m.causal && k0 > q1) return 0;  // every key of the tile is in the future
-  if (!grow_in_qb && !local_meets(m, q0, q1, k0, k1)) {
+  if (!grow_in_qb && !local_meets(m, q0, q1, k0, k1) && !rand_meets(m, q0, q1, k0, k1)) {
     const uint32_t any = colmask[kb * 4] | colmask[kb * 4 + 1] | colmask[kb * 4 + 2] |
                          colmask[kb * 4 + 3];
     if (!any) return 0;  // no local pair, no strided or global column, no global row

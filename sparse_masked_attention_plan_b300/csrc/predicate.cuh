@@ -14,6 +14,12 @@
 //   so only c < lim - src is tested.
 // * dense walk of a global row: every key j <= i (causal) or every key
 //   ("Attention variants", section 4, with_global).
+// * random blocks (BigBird's random connections, "Sparse and sliding-window
+//   attention", section "Block-sparse attention: BigBird"): inside a band tile the
+//   columns of row i's random key blocks join the column mask (they are cut at hb
+//   like the strided ones); a key tile outside the band reached only by random blocks
+//   (kind "random") has no local span, and its mask is the random columns minus the
+//   strided and global ones, which the packed entries already cover.
 // Keys at or past T (ragged last tile) fall outside [lo, hi] and past hb.
 #pragma once
 
@@ -22,6 +28,23 @@
 #include "internal.h"
 
 namespace spattn {
+
+// Bits c of the 128-key tile at k0 that lie in a random key block of row i.
+__device__ __forceinline__ void random_bits(const MaskDev& m, int i, int k0, uint32_t (&w)[4]) {
+  w[0] = w[1] = w[2] = w[3] = 0u;
+  if (m.rand_block == 0 || i >= m.T) return;
+  const int q = i / m.rand_block;
+  for (int x = m.r_off[q]; x < m.r_off[q + 1]; ++x) {
+    const int c0 = m.r_kb[x] * m.rand_block - k0;
+    if (c0 < 0 || c0 >= kTile) continue;  // block sizes divide the tile: wholly in or out
+    const int c1 = c0 + m.rand_block - 1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int a = max(c0 - 32 * k, 0), b = min(c1 - 32 * k, 31);
+      if (a <= b) w[k] |= ((2u << b) - 1u) & (0xffffffffu << a);
+    }
+  }
+}
 
 struct RowPredicate {
   int lo, hi, hb;
@@ -62,6 +85,23 @@ __device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const u
     p.bits[1] = w.y;
     p.bits[2] = w.z;
     p.bits[3] = w.w;
+    if (m.rand_block) {
+      uint32_t r[4];
+      random_bits(m, i, k0, r);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) p.bits[k] |= r[k];
+    }
+  } else if (kind == kKindRandom) {
+    p.lo = 1;  // no local span
+    p.hi = 0;
+    p.hb = (m.causal ? min(i, m.T - 1) : m.T - 1) - k0;
+    const uint4 w = *reinterpret_cast<const uint4*>(colmask + 4 * e.z);
+    uint32_t r[4];
+    random_bits(m, i, k0, r);
+    p.bits[0] = r[0] & ~w.x;
+    p.bits[1] = r[1] & ~w.y;
+    p.bits[2] = r[2] & ~w.z;
+    p.bits[3] = r[3] & ~w.w;
   } else if (kind == kKindPacked) {
     p.lo = 0;
     p.hi = e.w - e.x - 1;

@@ -49,7 +49,8 @@ void free_plan_memory(spattn_plan* p) {
                   p->d_walk, p->d_err, p->sched[0].d_items, p->sched[0].d_entries,
                   p->sched[1].d_items, p->sched[1].d_entries, p->sched[2].d_items,
                   p->sched[2].d_entries, p->d_colmask_res, p->d_rowzero,
-                  p->bsched.d_items, p->bsched.d_entries, p->d_colidx, p->d_bscratch};
+                  p->bsched.d_items, p->bsched.d_entries, p->d_colidx, p->d_bscratch,
+                  p->d_roff, p->d_rkb};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -103,6 +104,27 @@ struct Sched {
     return b - k0 <= p->radius && k1 - a <= p->radius;
   }
   bool cols_in(int64_t x, int64_t y) const { return y >= x && upper(y) - lower(x) > 0; }
+  // Does a random block of the rows [a, b] reach a key in [k0, k1] (causal: k <= b)?
+  bool rand_in(int64_t a, int64_t b, int64_t k0, int64_t k1) const {
+    if (p->r_kb.empty() || a > b) return false;
+    if (p->causal) k1 = std::min(k1, b);
+    if (k0 > k1) return false;
+    const int64_t rb = p->rand_block;
+    for (int64_t q = a / rb; q <= b / rb; ++q)
+      for (int32_t x = p->r_off[q]; x < p->r_off[q + 1]; ++x) {
+        const int64_t c0 = int64_t(p->r_kb[x]) * rb, c1 = c0 + rb - 1;
+        if (c0 <= k1 && c1 >= k0) return true;
+      }
+    return false;
+  }
+  // The natural key tiles (of `tile` keys) that random blocks of rows [a, b] reach.
+  void rand_tiles(int64_t a, int64_t b, int64_t tile, std::vector<int64_t>* out) const {
+    if (p->r_kb.empty()) return;
+    const int64_t rb = p->rand_block;
+    for (int64_t q = a / rb; q <= b / rb; ++q)
+      for (int32_t x = p->r_off[q]; x < p->r_off[q + 1]; ++x)
+        out->push_back(int64_t(p->r_kb[x]) * rb / tile);
+  }
 };
 
 void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, int qtile_rows,
@@ -146,12 +168,31 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
         if (a >= T) continue;
         const int64_t b = std::min<int64_t>(a + qtile_rows, T) - 1;
         const bool active = h.local_meets(a, b, k0, k1) ||
-                            h.cols_in(k0, p->causal ? std::min(k1, b) : k1);
+                            h.cols_in(k0, p->causal ? std::min(k1, b) : k1) ||
+                            h.rand_in(a, b, k0, k1);
         if (!active) continue;
         flags |= kActive0 << t;
         if (!ragged && h.local_covers(a, b, k0, k1)) flags |= kFull0 << t;
       }
       if (flags & (kActive0 | kActive1)) push(static_cast<int32_t>(k0), flags, static_cast<int32_t>(kb), 0);
+    }
+    {  // key tiles outside the band that random blocks of the group's rows reach
+      std::vector<int64_t> rt;
+      h.rand_tiles(r0, r1, kTile, &rt);
+      std::sort(rt.begin(), rt.end());
+      rt.erase(std::unique(rt.begin(), rt.end()), rt.end());
+      for (int64_t kb : rt) {
+        if (kb >= kb_lo && kb <= kb_hi) continue;
+        const int64_t k0 = kb * kTile, k1 = std::min<int64_t>(k0 + kTile, T) - 1;
+        int32_t flags = kKindRandom << kKindShift;
+        for (int t = 0; t < n_qtiles; ++t) {
+          const int64_t a = r0 + int64_t(t) * qtile_rows;
+          if (a >= T) continue;
+          const int64_t b = std::min<int64_t>(a + qtile_rows, T) - 1;
+          if (h.rand_in(a, b, k0, k1)) flags |= kActive0 << t;
+        }
+        if (flags & (kActive0 | kActive1)) push(static_cast<int32_t>(k0), flags, static_cast<int32_t>(kb), 0);
+      }
     }
     if (nc > 0) {
       const int64_t a_idx = h.lower(kb_lo * kTile), b_idx = h.lower((kb_hi + 1) * kTile);
@@ -250,8 +291,25 @@ void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s) {
     const int64_t u_hi = std::min<int64_t>(nu_nat - 1, (kb_hi + 1) * (kTile / kBwdKeys) - 1);
     for (int64_t u = kb_lo * (kTile / kBwdKeys); u <= u_hi; ++u) {
       const int64_t k0 = u * kBwdKeys, k1 = std::min<int64_t>(k0 + kBwdKeys, T) - 1;
-      if (h.local_meets(r0, r1, k0, k1) || h.cols_in(k0, p->causal ? std::min(k1, r1) : k1))
+      if (h.local_meets(r0, r1, k0, k1) || h.cols_in(k0, p->causal ? std::min(k1, r1) : k1) ||
+          h.rand_in(r0, r1, k0, k1))
         add(nat[u], r0, kKindBand << kKindShift, 0, 0);
+    }
+    {  // units outside the band range that random blocks of the group's rows reach
+      std::vector<int64_t> ru;
+      h.rand_tiles(r0, r1, kBwdKeys, &ru);
+      std::vector<int64_t> all;
+      for (int64_t u0 : ru)  // a random block of b keys spans b / 64 units (or part of one)
+        for (int64_t u = u0; u < u0 + std::max<int64_t>(1, p->rand_block / kBwdKeys); ++u)
+          all.push_back(u);
+      std::sort(all.begin(), all.end());
+      all.erase(std::unique(all.begin(), all.end()), all.end());
+      const int64_t band_u0 = kb_lo * (kTile / kBwdKeys);
+      for (int64_t u : all) {
+        if (u >= nu_nat || (u >= band_u0 && u <= u_hi)) continue;
+        const int64_t k0 = u * kBwdKeys, k1 = std::min<int64_t>(k0 + kBwdKeys, T) - 1;
+        if (h.rand_in(r0, r1, k0, k1)) add(nat[u], r0, kKindRandom << kKindShift, 0, 0);
+      }
     }
     if (nc > 0) {
       const int64_t a_idx = h.lower(kb_lo * kTile), b_idx = h.lower((kb_hi + 1) * kTile);
@@ -361,6 +419,26 @@ spattn_status spattn_mask_validate(const spattn_mask_spec* spec, int64_t T) {
     for (size_t a = 1; a < g.size(); ++a)
       if (g[a] == g[a - 1]) return fail(SPATTN_ERR_INVALID_SPEC, "duplicate global position %d", g[a]);
   }
+  if (spec->n_rand < 0) return fail(SPATTN_ERR_INVALID_SPEC, "n_rand must be >= 0");
+  if (spec->n_rand > 0) {
+    const int64_t b = spec->rand_block;
+    if (b != 16 && b != 32 && b != 64 && b != 128)
+      return fail(SPATTN_ERR_INVALID_SPEC, "rand_block must be 16, 32, 64 or 128");
+    if (!spec->rand_pairs) return fail(SPATTN_ERR_NULL, "rand_pairs is NULL");
+    const int64_t nb = (T + b - 1) / b;
+    if (spec->n_rand > nb * nb) return fail(SPATTN_ERR_INVALID_SPEC, "more random pairs than blocks");
+    std::vector<int64_t> keys(static_cast<size_t>(spec->n_rand));
+    for (int64_t a = 0; a < spec->n_rand; ++a) {
+      const int64_t q = spec->rand_pairs[2 * a], k = spec->rand_pairs[2 * a + 1];
+      if (q < 0 || q >= nb || k < 0 || k >= nb)
+        return fail(SPATTN_ERR_INVALID_SPEC, "random pair (%lld, %lld) outside [0, %lld)",
+                    (long long)q, (long long)k, (long long)nb);
+      keys[a] = q * nb + k;
+    }
+    std::sort(keys.begin(), keys.end());
+    for (size_t a = 1; a < keys.size(); ++a)
+      if (keys[a] == keys[a - 1]) return fail(SPATTN_ERR_INVALID_SPEC, "duplicate random pair");
+  }
   return SPATTN_OK;
 }
 
@@ -400,6 +478,20 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
   if (p->stride > T) {  // at most one strided column, j == offset
     if (p->offset < T) p->stride = T; else { p->stride = 0; p->offset = 0; }
   }
+  if (spec->n_rand > 0) {  // random blocks as CSR: query block -> ascending key blocks
+    const int64_t b = spec->rand_block, nb = (T + b - 1) / b;
+    std::vector<std::pair<int32_t, int32_t>> pr;
+    for (int64_t a = 0; a < spec->n_rand; ++a)
+      pr.emplace_back(spec->rand_pairs[2 * a], spec->rand_pairs[2 * a + 1]);
+    std::sort(pr.begin(), pr.end());
+    p->rand_block = static_cast<int32_t>(b);
+    p->r_off.assign(static_cast<size_t>(nb) + 1, 0);
+    for (auto& x : pr) {
+      ++p->r_off[x.first + 1];
+      p->r_kb.push_back(x.second);
+    }
+    for (int64_t q = 0; q < nb; ++q) p->r_off[q + 1] += p->r_off[q];
+  }
   p->gpos.assign(spec->global_pos, spec->global_pos + spec->n_global);
   std::sort(p->gpos.begin(), p->gpos.end());
   for (int32_t x : p->gpos)
@@ -431,6 +523,12 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
     }                                                                                  \
   } while (0)
 
+  PLAN_TRY(dev_alloc(&p->d_roff, p->r_off.size()));
+  PLAN_TRY(dev_alloc(&p->d_rkb, p->r_kb.size()));
+  if (!p->r_kb.empty()) {
+    PLAN_TRY(cudaMemcpy(p->d_roff, p->r_off.data(), p->r_off.size() * 4, cudaMemcpyHostToDevice));
+    PLAN_TRY(cudaMemcpy(p->d_rkb, p->r_kb.data(), p->r_kb.size() * 4, cudaMemcpyHostToDevice));
+  }
   PLAN_TRY(dev_alloc(&p->d_gpos, p->gpos.size()));
   PLAN_TRY(dev_alloc(&p->d_gpos_ns, p->gpos_ns.size()));
   if (!p->gpos.empty())
@@ -495,7 +593,8 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
   // execution schedules
   build_schedule(p, &p->sched[0], 2 * kTile, kTile, 2, true);
   build_schedule(p, &p->sched[1], 64, 64, 1, true);
-  if (p->dilation > 1 && p->stride == 0 && p->gpos.empty() && T % p->dilation == 0) {
+  if (p->dilation > 1 && p->stride == 0 && p->gpos.empty() && p->r_kb.empty() &&
+      T % p->dilation == 0) {
     // dilated view: residue class r holds rows r, r + d, ...; there the dilated
     // window is a contiguous window of the same width over T / d rows
     spattn_plan v;

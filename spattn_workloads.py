@@ -50,6 +50,13 @@ WORKLOADS = {
                               radius=-1, stride=1024, offset=0, n_global=0),
     "t8k_full_causal": dict(B=1, H=32, T=8192, d=128, causal=1, window=0, radius=-1,
                             stride=0, offset=0, n_global=0),
+    # BigBird encoder ("Sparse and sliding-window attention", Block-sparse attention:
+    # BigBird): block 64, a window of 3 blocks (radius 96), R = 3 random key blocks
+    # per query block, G = 2 global blocks (the first 128 tokens); BigBird-base shape
+    # (12 heads of 64) at 4096 tokens.
+    "t4096_bigbird": dict(B=8, H=12, T=4096, d=64, causal=0, window=0, radius=96, stride=0,
+                          offset=0, n_global=0, global_first=128, rand_block=64, rand_per_block=3,
+                          rand_seed=0),
     # Longformer-style dilated window: 512 keys spaced 2 apart (a 1023-token span).
     "t32k_w512_d2": dict(B=1, H=32, T=32768, d=128, causal=1, window=512, radius=-1,
                          stride=0, offset=0, n_global=0, dilation=2),
@@ -83,10 +90,29 @@ def mask_params(name_or_cfg, seed_override=None) -> dict:
     """The mask-rule fields of a workload, with global positions drawn."""
     cfg = WORKLOADS[name_or_cfg] if isinstance(name_or_cfg, str) else name_or_cfg
     gseed = cfg.get("global_seed", 0) if seed_override is None else seed_override
-    return dict(causal=cfg["causal"], window=cfg["window"], radius=cfg["radius"],
-                stride=cfg["stride"], offset=cfg["offset"],
-                global_pos=global_positions(cfg["T"], cfg["n_global"], gseed),
-                dilation=cfg.get("dilation", 1))
+    if cfg.get("global_first"):
+        gpos = np.arange(cfg["global_first"], dtype=np.int32)
+    else:
+        gpos = global_positions(cfg["T"], cfg["n_global"], gseed)
+    out = dict(causal=cfg["causal"], window=cfg["window"], radius=cfg["radius"],
+               stride=cfg["stride"], offset=cfg["offset"], global_pos=gpos,
+               dilation=cfg.get("dilation", 1))
+    if cfg.get("rand_block"):
+        out["rand_block"] = cfg["rand_block"]
+        out["rand_pairs"] = random_block_pairs(cfg["T"], cfg["rand_block"],
+                                               cfg["rand_per_block"], cfg.get("rand_seed", 0))
+    return out
+
+
+def random_block_pairs(T: int, b: int, R: int, seed: int) -> np.ndarray:
+    """BigBird random connections as (query block, key block) pairs: for every query
+    block, R distinct key blocks drawn uniformly from all ceil(T / b) blocks with
+    numpy's PCG64 (fewer when there are fewer blocks).  [n, 2] int32, sorted."""
+    rng = np.random.default_rng(seed + 4242)
+    nb = -(-T // b)
+    pairs = [(q, int(k)) for q in range(nb)
+             for k in np.sort(rng.choice(nb, size=min(R, nb), replace=False))]
+    return np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
 
 
 def qkv(B: int, H: int, T: int, d: int, seed: int, dtype=torch.bfloat16):

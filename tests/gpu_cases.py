@@ -82,9 +82,7 @@ def run_and_compare(B, H, T, d, mask, dtype="bf16", seed=0, heads=None, rows=Non
     plan.check_device()
     O = o.float().cpu().numpy()
     L = lse.cpu().numpy()
-    m = oracle.Mask(T, mask.get("causal", 1), mask.get("window", 0), mask.get("radius", -1),
-                    mask.get("stride", 0), mask.get("offset", 0), mask.get("global_pos", ()),
-                    mask.get("dilation", 1))
+    m = oracle_mask(T, mask)
     heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     tol = TOL[dtype]
     worst = dict(max_abs=0.0, rel_l2=0.0, lse=0.0)
@@ -132,9 +130,12 @@ def check_grad(name, got, ref, dtype, where=""):
 
 
 def oracle_mask(T, mask):
+    rp = np.asarray(mask.get("rand_pairs", ()), dtype=np.int32).reshape(-1, 2)
+    rp = rp[np.lexsort((rp[:, 1], rp[:, 0]))] if len(rp) else rp
     return oracle.Mask(T, mask.get("causal", 1), mask.get("window", 0), mask.get("radius", -1),
-                       mask.get("stride", 0), mask.get("offset", 0), mask.get("global_pos", ()),
-                       mask.get("dilation", 1))
+                       mask.get("stride", 0), mask.get("offset", 0),
+                       np.sort(np.asarray(mask.get("global_pos", ()), dtype=np.int32)),
+                       mask.get("dilation", 1), mask.get("rand_block", 0), rp)
 
 
 def run_bwd(B, H, T, d, mask, dtype="bf16", seed=0, scale=None, plan=None):

@@ -58,11 +58,13 @@ def test_version(built):
 def test_validate_accepts_what_the_oracle_accepts(oracle_mod, built, seed):
     for e in small_specs(seed, n=60):
         m = oracle.Mask(e["T"], e["causal"], e["window"], e["radius"], e["stride"],
-                        e["offset"], e["global_pos"], e["dilation"])
+                        e["offset"], e["global_pos"], e["dilation"], e.get("rand_block", 0),
+                        e.get("rand_pairs", ()))
         assert m.validate() == 0
         st = sp.validate(e["T"], causal=e["causal"], window=e["window"], radius=e["radius"],
                          stride=e["stride"], offset=e["offset"], global_pos=e["global_pos"],
-                         dilation=e["dilation"])
+                         dilation=e["dilation"], rand_block=e.get("rand_block", 0),
+                         rand_pairs=e.get("rand_pairs", ()))
         assert st == sp.OK, (e, built.spattn_last_error())
 
 
@@ -73,16 +75,21 @@ INVALID = [
     dict(T=8, stride=4, offset=4), dict(T=8, stride=0, offset=1),
     dict(T=8, global_pos=[8]), dict(T=8, global_pos=[-1]), dict(T=8, global_pos=[3, 3]),
     dict(T=8, dilation=-1),
+    dict(T=40, causal=0, radius=2, rand_block=48, rand_pairs=[(0, 0)]),
+    dict(T=40, causal=0, radius=2, rand_block=16, rand_pairs=[(0, 3)]),
+    dict(T=40, causal=0, radius=2, rand_block=16, rand_pairs=[(0, 1), (0, 1)]),
+    dict(T=40, causal=0, radius=2, rand_block=16, rand_pairs=[(-1, 0)]),
 ]
 
 
 @pytest.mark.parametrize("case", INVALID, ids=[str(c) for c in INVALID])
 def test_validate_rejects_what_the_oracle_rejects(oracle_mod, built, case):
-    c = dict(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=[], dilation=1)
+    c = dict(causal=1, window=0, radius=-1, stride=0, offset=0, global_pos=[], dilation=1,
+             rand_block=0, rand_pairs=[])
     c.update(case)
     T = c.pop("T")
     m = oracle.Mask(T, c["causal"], c["window"], c["radius"], c["stride"], c["offset"],
-                    c["global_pos"], c["dilation"])
+                    c["global_pos"], c["dilation"], c["rand_block"], c["rand_pairs"])
     assert m.validate() != 0
     assert sp.validate(T, **c) != sp.OK
 

@@ -125,15 +125,25 @@ def test_backward_is_deterministic(oracle_mod):
 
 def _key_major_cover(plan, T, mask):
     """How often the key-major schedule visits each (query, key) pair: a band entry
-    visits the allowed pairs of its non-global rows inside its unit, a packed entry
-    its packed columns [a, b), a gathered dense entry the allowed pairs of its global
-    rows inside its unit."""
+    visits the allowed pairs of its non-global rows inside its unit, a random entry
+    their random-block pairs that are not sparse columns, a packed entry its packed
+    columns [a, b), a gathered dense entry the allowed pairs of its global rows inside
+    its unit."""
     items, ents, _ = plan.schedule(3)
     cols = plan.columns()
     g = np.asarray(sorted(mask.get("global_pos", [])), dtype=np.int64)
     M = np_dense_mask(T, mask.get("causal", 1), mask.get("window", 0), mask.get("radius", -1),
                       mask.get("stride", 0), mask.get("offset", 0), list(g),
-                      mask.get("dilation", 1))
+                      mask.get("dilation", 1), mask.get("rand_block", 0),
+                      mask.get("rand_pairs", ()))
+    Rm = np.zeros((T, T), bool)  # the random blocks alone
+    rb = mask.get("rand_block", 0)
+    for q, k in np.asarray(mask.get("rand_pairs", ()), dtype=np.int64).reshape(-1, 2):
+        Rm[q * rb:(q + 1) * rb, k * rb:(k + 1) * rb] = True
+    if mask.get("causal", 1):
+        Rm &= np.tri(T, dtype=bool)
+    colset = np.zeros(T, bool)
+    colset[cols] = True
     isg = np.zeros(T, bool)
     isg[g] = True
     cov = np.zeros((T, T), np.int32)
@@ -152,7 +162,10 @@ def _key_major_cover(plan, T, mask):
                 cov[np.ix_(rows, keys)] += 1
             else:
                 keys = np.arange(key0, min(key0 + 64, T))
-                sub = M[np.ix_(rows, keys)].astype(np.int32)
+                if kind == 3:  # random-only unit: random keys that are not sparse columns
+                    sub = (Rm[np.ix_(rows, keys)] & ~colset[keys][None, :]).astype(np.int32)
+                else:
+                    sub = M[np.ix_(rows, keys)].astype(np.int32)
                 cov[np.ix_(rows, keys)] += sub
     return cov, M
 

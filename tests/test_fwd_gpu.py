@@ -50,6 +50,15 @@ SWEEP = [
     (1, 1, 513, 128, dict(causal=1, window=0, dilation=3)),
     (1, 2, 1024, 128, dict(causal=0, radius=50, dilation=4)),
     (2, 1, 600, 64, dict(causal=1, window=70, dilation=6)),
+    # BigBird random blocks ("Sparse and sliding-window attention", Block-sparse
+    # attention: BigBird): alone, with globals, with strided columns, causal
+    (1, 2, 700, 64, dict(causal=0, radius=40, global_pos=[0, 1, 650], rand_block=64,
+                         rand_pairs=[(0, 9), (1, 5), (3, 0), (3, 10), (10, 2), (10, 10)])),
+    (2, 1, 520, 128, dict(causal=1, window=70, stride=33, offset=4, rand_block=16,
+                          rand_pairs=[(20, 3), (20, 19), (31, 0), (32, 32), (5, 30)])),
+    (1, 2, 600, 128, dict(causal=0, radius=0, rand_block=128, rand_pairs=[(0, 4), (4, 0), (2, 2)])),
+    (1, 1, 1100, 64, dict(causal=1, window=96, global_pos=list(range(64)), rand_block=32,
+                          rand_pairs=[(q, (7 * q + 3) % (q + 1)) for q in range(35)])),
 ]
 
 

@@ -3,7 +3,8 @@ import pytest
 
 import oracle
 import spattn_workloads as W
-from pins import ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS, DECODE_CHECKS, closed_form_pairs
+from pins import (ATTENTION_CHECKS, BWD_CHECKS, COUNT_CHECKS, DECODE_CHECKS, closed_form_pairs,
+                  dense_of)
 
 
 @pytest.mark.parametrize("check", COUNT_CHECKS + ATTENTION_CHECKS + BWD_CHECKS + DECODE_CHECKS,
@@ -20,8 +21,13 @@ def test_workload_pair_counts_closed_form(oracle_mod, name):
     p = W.mask_params(name)
     m = oracle.Mask.from_params(cfg["T"], p)
     assert m.validate() == 0
-    cf = closed_form_pairs(cfg["T"], p["causal"], p["window"], p["radius"], p["stride"],
-                           p["offset"], p["global_pos"], p["dilation"])
+    if p.get("rand_block"):
+        # random blocks: the numpy dense restatement (the inclusion-exclusion form has
+        # no random term)
+        cf = int(dense_of(dict(T=cfg["T"], **p)).sum())
+    else:
+        cf = closed_form_pairs(cfg["T"], p["causal"], p["window"], p["radius"], p["stride"],
+                               p["offset"], p["global_pos"], p["dilation"])
     assert m.count_pairs() == cf
 
 

@@ -9,7 +9,8 @@ import torch
 import oracle
 import spattn_workloads as W
 import sparse_masked_attention_plan_b300 as sp
-from pins import small_specs
+import gpu_cases
+from pins import random_blocks, small_specs
 
 pytestmark = pytest.mark.gpu
 
@@ -34,13 +35,18 @@ EDGE_SPECS = [
     dict(T=500, causal=1, window=0, dilation=7),
     dict(T=300, causal=1, window=40, dilation=301),
     dict(T=1000, causal=0, radius=3, dilation=200),
+    # BigBird random blocks, with and without the other rules
+    dict(T=700, causal=0, radius=40, global_pos=[0, 1, 650], rand_block=64,
+         rand_pairs=[(0, 9), (1, 5), (3, 0), (3, 10), (10, 2), (10, 10)]),
+    dict(T=520, causal=1, window=70, stride=33, offset=4, rand_block=16,
+         rand_pairs=[(20, 3), (20, 19), (31, 0), (32, 32), (5, 30)]),
+    dict(T=600, causal=0, radius=0, rand_block=128, rand_pairs=[(0, 4), (4, 0), (2, 2)]),
+    dict(T=900, causal=1, window=0, rand_block=32, rand_pairs=[(27, 28), (28, 0)]),
 ]
 
 
 def oracle_mask(T, p):
-    return oracle.Mask(T, p.get("causal", 1), p.get("window", 0), p.get("radius", -1),
-                       p.get("stride", 0), p.get("offset", 0), p.get("global_pos", ()),
-                       p.get("dilation", 1))
+    return gpu_cases.oracle_mask(T, p)
 
 
 def expected_columns(T, p):
@@ -101,6 +107,9 @@ def test_random_spec_plans_match_oracle(oracle_mod, seed):
                  stride=s, offset=int(rng.integers(0, s)) if s else 0,
                  global_pos=np.sort(rng.choice(T, int(rng.choice([0, 1, 9])), replace=False)),
                  dilation=int(rng.choice([1, 1, 2, 3, 130])))
+        if rng.random() < 0.4:
+            e["rand_block"], e["rand_pairs"] = random_blocks(T, int(rng.choice([16, 64, 128])),
+                                                             int(rng.integers(1, 4)), rng)
         check_plan(T, e)
 
 
@@ -130,6 +139,13 @@ def covered_keys(plan_sched, cols, T, group_rows, qtile_rows, i, grow, p):
     return keys
 
 
+def in_random(p, i, j):
+    b = p.get("rand_block", 0)
+    if not b:
+        return False
+    return (i // b, j // b) in {tuple(x) for x in np.asarray(p["rand_pairs"]).reshape(-1, 2).tolist()}
+
+
 def entry_keys(src, f, lim, t, i, T, cols, colset, causal, p):
     kind = (f >> 4) & 3
     full = bool(f & (4 << t))  # the kernels skip the predicate: the whole tile counts
@@ -143,12 +159,16 @@ def entry_keys(src, f, lim, t, i, T, cols, colset, causal, p):
             ok = False
         elif kind == 2:
             ok = (j <= i) if causal else True
+        elif kind == 3:  # random-only tile: random keys that are not sparse columns
+            ok = in_random(p, i, j) and j not in colset and (j <= i or not causal)
         elif causal:
             w, dl = p.get("window", 0), p.get("dilation", 1)
-            ok = j <= i and (((w == 0 or i - j < w * dl) and (i - j) % dl == 0) or j in colset)
+            ok = j <= i and (((w == 0 or i - j < w * dl) and (i - j) % dl == 0) or
+                             j in colset or in_random(p, i, j))
         else:
             r, dl = p.get("radius", -1), p.get("dilation", 1)
-            ok = ((r < 0 or abs(i - j) <= r * dl) and abs(i - j) % dl == 0) or j in colset
+            ok = (((r < 0 or abs(i - j) <= r * dl) and abs(i - j) % dl == 0) or j in colset or
+                  in_random(p, i, j))
         if ok:
             out.append(j)
     return out
