@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) dkdv_kernel(const BwdArgs p, int uni
 }
 
 template <typename In, int D>
-cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st) {
+cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st, bool with_dq) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -361,7 +361,7 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st) {
   const long long rb = (rows + kWarps - 1) / kWarps;
   rowdot_kernel<In, D><<<static_cast<unsigned>(rb), kThreads, 0, st>>>(
       static_cast<const In*>(a.O), static_cast<const In*>(a.dO), a.Dvec, rows);
-  if (a.n_q_items > 0)
+  if (with_dq && a.n_q_items > 0)
     dq_kernel<In, D><<<dim3(a.n_q_items, a.BH), kThreads, DqCfg<D>::kSmemBytes, st>>>(a);
   if (a.n_packed_units > 0)
     dkdv_kernel<In, D><<<dim3(a.n_packed_units, a.BH), kThreads, KvCfg<D>::kSmemBytes, st>>>(a, 0);
@@ -373,13 +373,13 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st) {
+cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st, bool with_dq) {
   if (a.bf16) {
-    if (d == 64) return launch_typed<__nv_bfloat16, 64>(a, st);
-    if (d == 128) return launch_typed<__nv_bfloat16, 128>(a, st);
+    if (d == 64) return launch_typed<__nv_bfloat16, 64>(a, st, with_dq);
+    if (d == 128) return launch_typed<__nv_bfloat16, 128>(a, st, with_dq);
   } else {
-    if (d == 64) return launch_typed<float, 64>(a, st);
-    if (d == 128) return launch_typed<float, 128>(a, st);
+    if (d == 64) return launch_typed<float, 64>(a, st, with_dq);
+    if (d == 128) return launch_typed<float, 128>(a, st, with_dq);
   }
   return cudaErrorInvalidValue;
 }

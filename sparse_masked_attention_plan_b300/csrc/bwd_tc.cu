@@ -1,0 +1,398 @@
+// bwd_tc.cu -- bf16 backward pass on the tcgen05 tensor cores: dQ.
+//
+// For a query row i with allowed set S_i, the saved log-sum-exp LSE_i and the row
+// dot D_i = dO_i . O_i, the chain rule through the softmax over S_i ("Sparse
+// attention" glossary, section "Choose the available reads", differentiated) gives
+//     P_ij = exp(scale q_i.k_j - LSE_i),  dS_ij = P_ij (dO_i.v_j - D_i)   (j in S_i),
+//     dQ_i = scale sum_j dS_ij k_j.
+// A CTA owns one 128-row query tile of one (batch, head) and walks the key tiles the
+// forward schedule gives that tile (band tiles, packed sparse columns, dense walks of
+// global rows), with the forward's per-row predicate inside partial tiles.
+// Warp roles (192 threads):
+//   warps 0-3  elementwise: P and dS of one query row per thread (its TMEM lane)
+//   warp 4     TMA producer: Q and dO tiles once, then K and V tiles into a ring
+//   warp 5     MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
+//              memory), then dQ += dS K with dS (bf16) from TMEM and the same K tile
+//              read as an MN-major operand
+// TMEM: S [0,128), dP [128,256), dQ [256,256+d).  dS overwrites the first 64 columns
+// of S; the tensor pipe runs products in issue order, so the next tile's S (issued
+// after dQ) cannot overwrite dS before dQ has read it.  P needs no running maximum:
+// the forward's LSE already normalises it.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "predicate.cuh"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace spattn {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+
+template <int D>
+struct DqCfg {
+  static constexpr int kChunkBytes = kTile * 64 * 2;  // 128 rows x 64 bf16, one swizzle span
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kSmemQ = 2 * kTileBytes;  // Q and dO
+  static constexpr int kSmemKV = kStages * kTileBytes;
+  static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
+                       kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 2,
+                       kBarDone = 2 * kStages + 3, kNumBars = 2 * kStages + 4;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+};
+
+struct DqParams {
+  __nv_bfloat16* dQ;
+  const float* LSE;
+  const float* Dvec;
+  float scale;
+  float scale_log2;
+  const uint32_t* colmask;
+  MaskDev mask;
+  const int4* items;
+  const int4* entries;
+  int* err;
+  uint64_t budget;
+  int BH;
+};
+
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  using C = DqCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, a_desc + off16, b_desc + off16, C::kIdescQK, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t a_tmem, uint64_t k_mn_desc,
+                                         bool accumulate) {
+  using C = DqCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, k_mn_desc + ((kk * 16 * 128) >> 4), C::kIdescDQ,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQg, const __grid_constant__ CUtensorMap tmdOg,
+                     const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
+                     const DqParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_addr(smem);
+  const uint32_t sdO = sQ + C::kTileBytes;
+  const uint32_t sKV = sQ + C::kSmemQ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemQ + C::kSmemKV);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  const uint32_t bar0 = smem_addr(bars);
+#define BAR(k) (bar0 + 8u * static_cast<uint32_t>(k))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA = (work item, query tile t, (batch, head)); heads vary fastest so neighbouring
+  // CTAs of one item share nothing but the items of one head share K/V tiles in L2
+  const int bh = blockIdx.x % p.BH;
+  const int rank = (blockIdx.x / p.BH) >> 1;
+  const int t = (blockIdx.x / p.BH) & 1;
+  const int4 item = p.items[rank];
+  const int n_ent = item.z;
+  const int4* ents = p.entries + item.y;
+  const bool gathered = (item.w & kItemGathered) != 0;
+  const MaskDev& m = p.mask;
+  const int qrow0 = item.x + t * kTile;  // first row (or gathered index) of the tile
+  const int active_bit = kActive0 << t, full_bit = kFull0 << t;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(BAR(C::kBarFull + s), 1);
+      mbar_init(BAR(C::kBarEmpty + s), 1);
+    }
+    mbar_init(BAR(C::kBarQ), 1);
+    mbar_init(BAR(C::kBarS), 1);
+    mbar_init(BAR(C::kBarP), 128);
+    mbar_init(BAR(C::kBarDone), 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    const void* mapQ = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
+    const void* mapdO = gathered ? static_cast<const void*>(&tmdOg) : static_cast<const void*>(&tmdO);
+    if (elect_one()) {
+      mbar_arrive_expect_tx(BAR(C::kBarQ), 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_4d(sQ + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64, 0, qrow0, bh);
+        tma_load_4d(sdO + c * C::kChunkBytes, mapdO, BAR(C::kBarQ), c * 64, 0, qrow0, bh);
+      }
+    }
+    __syncwarp();
+    int issued = 0;
+    bool ok = true;
+    for (int n = 0; n < n_ent && ok; ++n) {
+      const int4 e = ents[n];
+      if (!(e.y & active_bit)) continue;
+      const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const int it = issued;
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout))) {
+          ok = false;
+          break;
+        }
+        const void* map = kv ? (packed ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV))
+                             : (packed ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK));
+        if (elect_one()) {
+          mbar_arrive_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
+                        c * 64, 0, e.x, bh);
+        }
+        __syncwarp();
+        ++issued;
+      }
+    }
+    for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+      mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
+                kErrTimeout);
+    mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t do_desc = smem_desc_sw128(sdO, 16, 1024);
+    const uint64_t kv_kdesc = smem_desc_sw128(sKV, 16, 1024);             // slot 0, K-major
+    const uint64_t kv_mndesc = smem_desc_sw128(sKV, C::kChunkBytes, 1024);  // slot 0, MN-major
+    constexpr uint32_t kSlot16 = C::kTileBytes >> 4;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout));
+    if (ok) {
+      tc_fence_after();
+      uint32_t pph = 0;
+      int done = 0;
+      int it = 0;
+      for (int n = 0; n < n_ent; ++n) {
+        const int4 e = ents[n];
+        if (!(e.y & active_bit)) continue;
+        const int kit = it, vit = it + 1;
+        it += 2;
+        const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1,
+                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) issue_kmajor<D>(tmem + C::kColS, q_desc, kv_kdesc + ks * kSlot16);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + vs), (vit / C::kStages) & 1,
+                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+          issue_kmajor<D>(tmem + C::kColDP, do_desc, kv_kdesc + vs * kSlot16);
+          mma_commit(BAR(C::kBarS));
+          mma_commit(BAR(C::kBarEmpty + vs));  // V is no longer needed
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP), pph, p.budget, p.err, kErrTimeout))) {
+          ok = false;
+          break;
+        }
+        pph ^= 1u;
+        tc_fence_after();
+        if (elect_one()) {
+          issue_dq<D>(tmem + C::kColDQ, tmem + C::kColS, kv_mndesc + ks * kSlot16, done > 0);
+          mma_commit(BAR(C::kBarEmpty + ks));
+        }
+        __syncwarp();
+        ++done;
+      }
+    }
+    if (elect_one()) mma_commit(BAR(C::kBarDone));
+    __syncwarp();
+    mbar_wait(BAR(C::kBarDone), 0, p.budget, p.err, kErrTimeout);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise warps
+    const int r = (warp << 5) | lane;
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+    int i;
+    bool valid;
+    if (gathered) {
+      const int a = qrow0 + r;
+      valid = a < m.n_global;
+      i = valid ? m.gpos[a] : 0;
+    } else {
+      i = qrow0 + r;
+      valid = i < m.T;
+    }
+    const size_t row = static_cast<size_t>(bh) * m.T + static_cast<size_t>(i);
+    const float lse2 = valid ? p.LSE[row] * 1.4426950408889634f : 0.f;
+    const float dsc = p.scale;
+    const float dterm = valid ? -p.Dvec[row] * dsc : 0.f;
+    const float c2 = p.scale_log2;
+    uint32_t sph = 0;
+    int n_done = 0;
+    for (int n = 0; n < n_ent; ++n) {
+      const int4 e = ents[n];
+      if (!(e.y & active_bit)) continue;
+      const bool got = mbar_wait(BAR(C::kBarS), sph, p.budget, p.err, kErrTimeout);
+      if (!__all_sync(0xffffffffu, got)) break;
+      sph ^= 1u;
+      tc_fence_after();
+      uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (!(e.y & full_bit)) row_mask(make_predicate(m, p.colmask, e, i), w);
+      if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
+      // dS = scale P (dP - D) with P = 2^(s scale log2 e - LSE log2 e), 32 columns at a
+      // time; the bf16 result of chunk q lands in columns 16q .. 16q+15, all of which
+      // the chunks up to q have already read
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(lane_base + C::kColS + 32 * q, sv);
+        tmem_ld32(lane_base + C::kColDP + 32 * q, dv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          const int c0 = 2 * b;
+          float x0 = fmaf(__uint_as_float(sv[c0]), c2, -lse2);
+          float x1 = fmaf(__uint_as_float(sv[c0 + 1]), c2, -lse2);
+          float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          if (!((w[q] >> c0) & 1u)) p0 = 0.f;
+          if (!((w[q] >> (c0 + 1)) & 1u)) p1 = 0.f;
+          const float g0 = p0 * fmaf(__uint_as_float(dv[c0]), dsc, dterm);
+          const float g1 = p1 * fmaf(__uint_as_float(dv[c0 + 1]), dsc, dterm);
+          pk[b] = pack_bf16x2(g0, g1);
+        }
+        tmem_st16(lane_base + C::kColS + 16 * q, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(C::kBarP));
+      ++n_done;
+    }
+    // ---------------------------------------------------------- epilogue
+    const bool write = valid && (gathered || !m.rowglobal[i]);
+    bool have = false;
+    if (n_done > 0) {
+      have = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarDone), 0, p.budget, p.err, kErrTimeout));
+      if (have) tc_fence_after();
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.dQ + row * D);
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t o[32];
+      if (have) {
+        tmem_ld32(lane_base + C::kColDQ + 32 * q, o);
+      } else {
+#pragma unroll
+        for (int b = 0; b < 32; ++b) o[b] = 0u;
+      }
+      if (write) {
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 x;
+          x.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]), __uint_as_float(o[8 * v4 + 1]));
+          x.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]), __uint_as_float(o[8 * v4 + 3]));
+          x.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]), __uint_as_float(o[8 * v4 + 5]));
+          x.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]), __uint_as_float(o[8 * v4 + 7]));
+          dst[4 * q + v4] = x;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+#undef BAR
+}
+
+template <int D>
+cudaError_t launch_dq_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
+  using C = DqCfg<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const long long T = a.mask.T;
+  CUtensorMap mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc;
+  bool ok = make_map(&mQ, a.Q, D, T, a.BH) && make_map(&mdO, a.dO, D, T, a.BH) &&
+            make_map(&mK, a.K, D, T, a.BH) && make_map(&mV, a.V, D, T, a.BH);
+  ok = ok && (a.n_cols > 0 ? make_map(&mKc, a.Kc, D, a.n_cols, a.BH) && make_map(&mVc, a.Vc, D, a.n_cols, a.BH)
+                           : (mKc = mK, mVc = mV, true));
+  ok = ok && (a.mask.n_global > 0 ? make_map(&mQg, a.Qg, D, a.mask.n_global, a.BH) &&
+                                        make_map(&mdOg, a.dOg, D, a.mask.n_global, a.BH)
+                                  : (mQg = mQ, mdOg = mdO, true));
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  DqParams kp;
+  kp.dQ = static_cast<__nv_bfloat16*>(a.dQ);
+  kp.LSE = a.LSE;
+  kp.Dvec = a.Dvec;
+  kp.scale = a.scale;
+  kp.scale_log2 = a.scale * 1.4426950408889634f;
+  kp.colmask = a.colmask;
+  kp.mask = a.mask;
+  kp.items = a.items;
+  kp.entries = a.entries;
+  kp.err = a.err;
+  kp.budget = a.wait_budget_cycles;
+  kp.BH = a.BH;
+  const long long ctas = static_cast<long long>(a.n_items) * 2 * a.BH;
+  if (ctas > 0x7fffffffLL) {
+    *why = "too many work items";
+    return cudaErrorInvalidValue;
+  }
+  bwd_dq_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, st>>>(
+      mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why) {
+  if (a.n_items == 0) return cudaSuccess;
+  if (d == 64) return launch_dq_d<64>(a, st, why);
+  if (d == 128) return launch_dq_d<128>(a, st, why);
+  *why = "head dim must be 64 or 128";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace spattn

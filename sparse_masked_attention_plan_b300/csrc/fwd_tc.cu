@@ -38,6 +38,7 @@
 #include "internal.h"
 #include "predicate.cuh"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace spattn {
 namespace {
@@ -471,45 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// [BH][rows * dview][D] bf16 seen as {D, dview, rows, BH}: element (x, r, q, bh) is
-// row q * dview + r of head bh.  Boxes of 128 rows (q) x 64 columns, one residue r,
-// 128-byte swizzle, zero fill past `rows`.  dview = 1 is the plain [BH][rows][D].
-bool make_map(CUtensorMap* map, const void* base, int D, long long rows, long long BH,
-              long long dview = 1) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  if (rows < 1) rows = 1;
-  const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(dview),
-                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[3] = {row_bytes, row_bytes * static_cast<cuuint64_t>(dview),
-                           row_bytes * static_cast<cuuint64_t>(dview) * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int D>
 cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {

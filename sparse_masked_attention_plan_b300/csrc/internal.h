@@ -233,7 +233,34 @@ struct BwdArgs {
   int32_t n_packed_units;
   int32_t n_units;
 };
-cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st);
+// with_dq = false leaves dQ to the tensor-core kernel (the row dots are still written)
+cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st, bool with_dq = true);
+
+// bwd_tc.cu (bf16 dQ on the tensor cores; walks the tensor-core forward schedule)
+struct BwdTcArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* dO;
+  const void* Kc;   // packed sparse-column K, V rows [BH][n_cols][d]
+  const void* Vc;
+  const void* Qg;   // gathered global-row Q, dO rows [BH][n_global][d]
+  const void* dOg;
+  void* dQ;
+  const float* LSE;
+  const float* Dvec;
+  int32_t BH;
+  int32_t n_cols;
+  float scale;
+  const uint32_t* colmask;
+  MaskDev mask;
+  const int4* items;
+  const int4* entries;
+  int32_t n_items;
+  int* err;
+  uint64_t wait_budget_cycles;
+};
+cudaError_t launch_bwd_dq_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why);
 
 // decode.cu (one generation step against a ring-buffer KV cache)
 struct DecodeArgs {

@@ -790,9 +790,16 @@ spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   if (!(scale > 0.f) || !std::isfinite(scale))
     return fail(SPATTN_ERR_INVALID_SPEC, "scale must be positive and finite");
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const bool tc = dtype == SPATTN_BF16;
   const size_t dvec_bytes = (size_t(BH) * p->T * 4 + 255) / 256 * 256;
   const size_t kc_bytes = size_t(BH) * p->n_cols * p->d * 4;
-  const size_t need = dvec_bytes + 2 * kc_bytes;
+  // bf16: packed K/V of the sparse columns and gathered Q/dO of the global rows for
+  // the tensor-core dQ kernel
+  const int64_t ng = static_cast<int64_t>(p->gpos.size());
+  const size_t row_b = size_t(p->d) * 2;
+  const size_t pk_bytes = tc ? (size_t(BH) * p->n_cols * row_b + 255) / 256 * 256 : 0;
+  const size_t pg_bytes = tc ? (size_t(BH) * ng * row_b + 255) / 256 * 256 : 0;
+  const size_t need = dvec_bytes + 2 * kc_bytes + 2 * pk_bytes + 2 * pg_bytes;
   if (need > p->bscratch_bytes) {
     if (p->d_bscratch) {
       CUDA_TRY(cudaStreamSynchronize(stream));
@@ -832,8 +839,50 @@ spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   a.u_entries = p->bsched.d_entries;
   a.n_packed_units = p->bsched.n_packed_units;
   a.n_units = static_cast<int32_t>(p->bsched.items.size() / 4);
-  cudaError_t e = spattn::launch_bwd_simt(p->d, a, stream);
+  cudaError_t e = spattn::launch_bwd_simt(p->d, a, stream, !tc);
   if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+  if (tc) {
+    uint8_t* pk = base + dvec_bytes + 2 * kc_bytes;
+    void* Kc = pk;
+    void* Vc = pk + pk_bytes;
+    void* Qg = pk + 2 * pk_bytes;
+    void* dOg = pk + 2 * pk_bytes + pg_bytes;
+    if (p->n_cols > 0 || ng > 0) {
+      CUDA_TRY(spattn::launch_pack(Q, K, V, Kc, Vc, Qg, p->d_cols, p->n_cols, p->d_gpos,
+                                   static_cast<int32_t>(ng), BH, p->T, static_cast<int32_t>(row_b),
+                                   stream));
+      if (ng > 0)  // the same gather of the global rows, of dO
+        CUDA_TRY(spattn::launch_pack(dO, K, V, nullptr, nullptr, dOg, p->d_cols, 0, p->d_gpos,
+                                     static_cast<int32_t>(ng), BH, p->T,
+                                     static_cast<int32_t>(row_b), stream));
+    }
+    spattn::BwdTcArgs t;
+    t.Q = Q;
+    t.K = K;
+    t.V = V;
+    t.dO = dO;
+    t.Kc = p->n_cols ? Kc : K;
+    t.Vc = p->n_cols ? Vc : V;
+    t.Qg = ng ? Qg : Q;
+    t.dOg = ng ? dOg : dO;
+    t.dQ = dQ;
+    t.LSE = LSE;
+    t.Dvec = a.Dvec;
+    t.BH = static_cast<int32_t>(BH);
+    t.n_cols = p->n_cols;
+    t.scale = scale;
+    t.colmask = p->d_colmask;
+    t.mask = p->mask_dev();
+    t.items = p->sched[0].d_items;
+    t.entries = p->sched[0].d_entries;
+    t.n_items = static_cast<int32_t>(p->sched[0].items.size() / 4);
+    t.err = p->d_err;
+    t.wait_budget_cycles = p->wait_budget_cycles;
+    const char* why = "";
+    e = spattn::launch_bwd_dq_tc(p->d, t, stream, &why);
+    if (e != cudaSuccess)
+      return fail(SPATTN_ERR_CUDA, "tensor-core dQ launch: %s (%s)", cudaGetErrorString(e), why);
+  }
   return SPATTN_OK;
 }
 
