@@ -168,6 +168,10 @@ spattn_status spattn_plan_copy_columns(const spattn_plan* plan, int32_t* cols, i
  *          global_pos (rows gathered from the global list); a packed entry reads
  *          packed columns [a, b) of its unit.  Rows that are global tokens take
  *          part only in gathered entries.
+ * which = 4: the same at 128-key units and 128-row groups: the schedule of the
+ *          bf16 (tensor-core) dK/dV kernel.  Entry kind 3 (both key-major forms and
+ *          the forward forms) is a key tile outside the band that only BigBird random
+ *          blocks reach.
  * *n_items / *n_entries receive the sizes; arrays shorter than that are an
  * error (SPATTN_ERR_SHAPE) and nothing is written.  items/entries may be NULL to
  * query the sizes.  *tile_products receives the number of (query tile, key tile)

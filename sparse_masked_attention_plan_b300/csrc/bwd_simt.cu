@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) dkdv_kernel(const BwdArgs p, int uni
 }
 
 template <typename In, int D>
-cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st, bool with_dq) {
+cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st, bool with_dq, bool with_dkdv) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -363,6 +363,7 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st, bool with_dq) {
       static_cast<const In*>(a.O), static_cast<const In*>(a.dO), a.Dvec, rows);
   if (with_dq && a.n_q_items > 0)
     dq_kernel<In, D><<<dim3(a.n_q_items, a.BH), kThreads, DqCfg<D>::kSmemBytes, st>>>(a);
+  if (!with_dkdv) return cudaGetLastError();
   if (a.n_packed_units > 0)
     dkdv_kernel<In, D><<<dim3(a.n_packed_units, a.BH), kThreads, KvCfg<D>::kSmemBytes, st>>>(a, 0);
   const int nat = a.n_units - a.n_packed_units;
@@ -373,13 +374,14 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t st, bool with_dq) {
 
 }  // namespace
 
-cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st, bool with_dq) {
+cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st, bool with_dq,
+                            bool with_dkdv) {
   if (a.bf16) {
-    if (d == 64) return launch_typed<__nv_bfloat16, 64>(a, st, with_dq);
-    if (d == 128) return launch_typed<__nv_bfloat16, 128>(a, st, with_dq);
+    if (d == 64) return launch_typed<__nv_bfloat16, 64>(a, st, with_dq, with_dkdv);
+    if (d == 128) return launch_typed<__nv_bfloat16, 128>(a, st, with_dq, with_dkdv);
   } else {
-    if (d == 64) return launch_typed<float, 64>(a, st, with_dq);
-    if (d == 128) return launch_typed<float, 128>(a, st, with_dq);
+    if (d == 64) return launch_typed<float, 64>(a, st, with_dq, with_dkdv);
+    if (d == 128) return launch_typed<float, 128>(a, st, with_dq, with_dkdv);
   }
   return cudaErrorInvalidValue;
 }

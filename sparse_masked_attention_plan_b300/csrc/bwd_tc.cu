@@ -1,4 +1,5 @@
-// bwd_tc.cu -- bf16 backward pass on the tcgen05 tensor cores: dQ.
+// bwd_tc.cu -- bf16 backward pass on the tcgen05 tensor cores: dQ (query-major) and
+// dK, dV (key-major).
 //
 // For a query row i with allowed set S_i, the saved log-sum-exp LSE_i and the row
 // dot D_i = dO_i . O_i, the chain rule through the softmax over S_i ("Sparse
@@ -339,6 +340,466 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef BAR
 }
 
+// ---------------------------------------------------------------- dK, dV (key-major)
+//
+//     dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i   (i with j in S_i)
+// A CTA owns one 128-key unit (natural keys, or packed sparse columns) of one (batch,
+// head): its K and V tiles stay in shared memory while the 128-row query tiles that
+// read it stream through a ring (Q and dO per stage).  Per query tile:
+//   S^T = K Q^T and dP^T = V dO^T (tensor cores, TMEM lanes = keys, columns = queries);
+//   elementwise (thread = key): P^T = 2^(S^T scale log2 e - LSE log2 e) under the
+//   key's mask, dS^T = scale P^T (dP^T - D), both to TMEM as bf16 over their own
+//   first 64 columns;
+//   dV += P^T dO and dK += dS^T Q (A from TMEM; dO and Q read as MN-major operands).
+// The per-query LSE and D of the tile go through shared memory; a query that is not a
+// row of this tile (past the end, or a global row summed by its own dense walk) gets
+// LSE = +inf, which makes its weight 0 without a mask.  The key-side mask is a few
+// spans per thread: the key's local window seen from the key (the rows whose window
+// holds it), all later rows for a strided or global column, the query blocks that
+// list the key's block as random (transposed lists), a range of packed columns, or
+// the suffix of gathered global rows at or after the key.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d).
+
+template <int D>
+struct KvCfg {
+  static constexpr int kChunkBytes = kTile * 64 * 2;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = D == 128 ? 2 : 4;  // one stage = the Q and dO tiles
+  static constexpr int kSmemKV = 2 * kTileBytes;
+  static constexpr int kSmemRing = kStages * 2 * kTileBytes;
+  static constexpr int kSmemVec = 2 * 2 * kTile * 4;  // LSE and D, double-buffered
+  static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages,
+                       kBarS = 1 + 2 * kStages, kBarP = 2 + 2 * kStages,
+                       kBarDone = 3 + 2 * kStages, kBarVec = 4 + 2 * kStages,
+                       kNumBars = 6 + 2 * kStages;
+  static constexpr int kSmemBytes = kSmemKV + kSmemRing + kSmemVec + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 0, 1);
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+struct KvParams {
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  float* dKc;  // packed-column partial sums [BH][n_cols][d] (fp32)
+  float* dVc;
+  const float* LSE;
+  const float* Dvec;
+  float scale;
+  float scale_log2;
+  const uint32_t* colmask;
+  MaskDev mask;
+  const int32_t* cols;
+  const int32_t* colidx;
+  const int32_t* rt_off;
+  const int32_t* rt_qb;
+  const int4* units;
+  const int4* entries;
+  int unit0;
+  int n_cols;
+  int* err;
+  uint64_t budget;
+  int BH;
+};
+
+// Bits of [a, b] (tile columns) in the four 32-bit words.
+__device__ __forceinline__ void add_span(int a, int b, uint32_t (&w)[4]) {
+  a = max(a, 0);
+  b = min(b, kTile - 1);
+  if (a > b) return;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] |= span_bits(a, b, 32 * k);
+}
+
+// The query columns of the tile at row q0 that may read key j (packed index c_pk for
+// packed units), for an entry of `kind`; rows that are not rows of the tile are
+// removed separately (LSE = +inf).
+__device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, int q0, int j,
+                                         int c_pk, uint32_t (&w)[4]) {
+  const MaskDev& m = p.mask;
+  w[0] = w[1] = w[2] = w[3] = 0u;
+  if (kind == kKindPacked) {
+    if (c_pk >= e.z && c_pk < e.w) w[0] = w[1] = w[2] = w[3] = 0xffffffffu;
+    return;
+  }
+  if (kind == kKindDense) {  // gathered global rows q0 .. : every key j <= their position
+    const int nr = min(kTile, m.n_global - q0);
+    int r0 = 0;
+    if (m.causal) {
+      int lo = 0, hi = nr;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (m.gpos[q0 + mid] < j) lo = mid + 1; else hi = mid;
+      }
+      r0 = lo;
+    }
+    add_span(r0, nr - 1, w);
+    return;
+  }
+  const int jc = j - q0;  // the key's own column
+  const int cut = m.causal ? jc : 0;
+  uint32_t extra[4] = {0u, 0u, 0u, 0u};
+  const uint32_t cw = p.colmask[(j / kTile) * 4 + (j % kTile) / 32];
+  const bool colbit = (cw >> (j & 31)) & 1u;
+  if (m.rand_block && !(kind == kKindRandom && colbit)) {
+    const int kb = j / m.rand_block;
+    for (int x = p.rt_off[kb]; x < p.rt_off[kb + 1]; ++x) {
+      const int r0 = p.rt_qb[x] * m.rand_block - q0;
+      add_span(max(r0, cut), r0 + m.rand_block - 1, extra);
+    }
+  }
+  if (kind == kKindRandom) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = extra[k];
+    return;
+  }
+  if (colbit) add_span(cut, kTile - 1, extra);
+  RowPredicate pr;
+  const int d = m.dilation;
+  if (m.causal) {
+    pr.lo = jc;
+    pr.hi = m.window ? jc + (m.window - 1) * d : m.T - 1 - q0;
+  } else {
+    pr.lo = m.radius >= 0 ? jc - m.radius * d : 0;
+    pr.hi = m.radius >= 0 ? jc + m.radius * d : kTile - 1;
+  }
+  pr.hi = min(pr.hi, kTile - 1);
+  pr.hb = kTile - 1;
+  pr.dil = d;
+  pr.res = ((jc % d) + d) % d;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) pr.bits[k] = extra[k];
+  row_mask(pr, w);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmQg, const __grid_constant__ CUtensorMap tmdOg,
+                       const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
+                       const KvParams p) {
+  using C = KvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sK = smem_addr(smem);
+  const uint32_t sV = sK + C::kTileBytes;
+  const uint32_t sRing = sK + C::kSmemKV;  // stage s: Q at +0, dO at +kTileBytes
+  float* s_vec = reinterpret_cast<float*>(smem + C::kSmemKV + C::kSmemRing);  // [2][LSE, D][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemKV + C::kSmemRing + C::kSmemVec);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  const uint32_t bar0 = smem_addr(bars);
+#define BAR(k) (bar0 + 8u * static_cast<uint32_t>(k))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x % p.BH;
+  const int4 unit = p.units[p.unit0 + blockIdx.x / p.BH];
+  const bool packed_unit = (unit.w & kUnitPacked) != 0;
+  const int n_ent = unit.z;
+  const int4* ents = p.entries + unit.y;
+  const MaskDev& m = p.mask;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::kBarKV), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(BAR(C::kBarFull + s), 1);
+      mbar_init(BAR(C::kBarEmpty + s), 1);
+    }
+    mbar_init(BAR(C::kBarS), 1);
+    mbar_init(BAR(C::kBarP), 128);
+    mbar_init(BAR(C::kBarDone), 1);
+    mbar_init(BAR(C::kBarVec + 0), 128);
+    mbar_init(BAR(C::kBarVec + 1), 128);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      const void* mk = packed_unit ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK);
+      const void* mv = packed_unit ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV);
+      mbar_arrive_expect_tx(BAR(C::kBarKV), 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_4d(sK + c * C::kChunkBytes, mk, BAR(C::kBarKV), c * 64, 0, unit.x, bh);
+        tma_load_4d(sV + c * C::kChunkBytes, mv, BAR(C::kBarKV), c * 64, 0, unit.x, bh);
+      }
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int n = 0; n < n_ent; ++n) {
+      const int4 e = ents[n];
+      const bool gathered = (e.y & kEntryGathered) != 0;
+      const int s = n % C::kStages;
+      const uint32_t ph = (n / C::kStages) & 1;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout)))
+        break;
+      const void* mq = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
+      const void* md = gathered ? static_cast<const void*>(&tmdOg) : static_cast<const void*>(&tmdO);
+      if (elect_one()) {
+        const uint32_t dst = sRing + s * 2 * C::kTileBytes;
+        mbar_arrive_expect_tx(BAR(C::kBarFull + s), 2 * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d(dst + c * C::kChunkBytes, mq, BAR(C::kBarFull + s), c * 64, 0, e.x, bh);
+          tma_load_4d(dst + C::kTileBytes + c * C::kChunkBytes, md, BAR(C::kBarFull + s), c * 64, 0,
+                      e.x, bh);
+        }
+      }
+      __syncwarp();
+      ++issued;
+    }
+    for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+      mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
+                kErrTimeout);
+    mbar_wait(BAR(C::kBarKV), 0, p.budget, p.err, kErrTimeout);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
+    const uint64_t v_desc = smem_desc_sw128(sV, 16, 1024);
+    const uint64_t ring_k = smem_desc_sw128(sRing, 16, 1024);              // stage 0 Q, K-major
+    const uint64_t ring_mn = smem_desc_sw128(sRing, C::kChunkBytes, 1024);  // stage 0 Q, MN-major
+    constexpr uint32_t kStage16 = (2 * C::kTileBytes) >> 4, kDo16 = C::kTileBytes >> 4;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarKV), 0, p.budget, p.err, kErrTimeout));
+    if (ok) {
+      tc_fence_after();
+      uint32_t pph = 0;
+      for (int n = 0; n < n_ent; ++n) {
+        const uint32_t s = n % C::kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + s), (n / C::kStages) & 1,
+                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+          issue_kmajor<D>(tmem + C::kColS, k_desc, ring_k + s * kStage16);
+          issue_kmajor<D>(tmem + C::kColDP, v_desc, ring_k + s * kStage16 + kDo16);
+          mma_commit(BAR(C::kBarS));
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP), pph, p.budget, p.err, kErrTimeout))) {
+          ok = false;
+          break;
+        }
+        pph ^= 1u;
+        tc_fence_after();
+        if (elect_one()) {
+          issue_dq<D>(tmem + C::kColDV, tmem + C::kColS, ring_mn + s * kStage16 + kDo16, n > 0);
+          issue_dq<D>(tmem + C::kColDK, tmem + C::kColDP, ring_mn + s * kStage16, n > 0);
+          mma_commit(BAR(C::kBarEmpty + s));
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) mma_commit(BAR(C::kBarDone));
+    __syncwarp();
+    mbar_wait(BAR(C::kBarDone), 0, p.budget, p.err, kErrTimeout);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise warps
+    const int kk = (warp << 5) | lane;  // key row of the unit = TMEM lane
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+    const int key = unit.x + kk;
+    const bool key_valid = packed_unit ? key < p.n_cols : key < m.T;
+    const int j = key_valid ? (packed_unit ? p.cols[key] : key) : 0;
+    const float c2 = p.scale_log2, dsc = p.scale;
+    const size_t head = static_cast<size_t>(bh) * m.T;
+    uint32_t sph = 0;
+    int n_done = 0;
+    for (int n = 0; n < n_ent; ++n) {
+      const int4 e = ents[n];
+      const bool gathered = (e.y & kEntryGathered) != 0;
+      const int kind = (e.y >> kKindShift) & 3;
+      // this tile's per-query LSE and D, one column per thread, double-buffered: buffer
+      // n & 1 is rewritten at tile n + 2, after every thread has passed tile n + 1's
+      // barrier (and so has finished tile n)
+      float* s_lse = s_vec + (n & 1) * 2 * kTile;
+      float* s_dd = s_lse + kTile;
+      {
+        int i = -1;
+        const int a = e.x + kk;
+        if (gathered) {
+          if (a < m.n_global) i = m.gpos[a];
+        } else if (a < m.T && !m.rowglobal[a]) {
+          i = a;
+        }
+        s_lse[kk] = i >= 0 ? p.LSE[head + i] * 1.4426950408889634f : INFINITY;
+        s_dd[kk] = i >= 0 ? p.Dvec[head + i] * dsc : 0.f;
+      }
+      mbar_arrive(BAR(C::kBarVec + (n & 1)));
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + (n & 1)), (n >> 1) & 1, p.budget,
+                                             p.err, kErrTimeout)))
+        break;
+      uint32_t w[4];
+      key_mask(p, kind, e, e.x, j, key, w);
+      if (!key_valid) w[0] = w[1] = w[2] = w[3] = 0u;
+      const bool got = mbar_wait(BAR(C::kBarS), sph, p.budget, p.err, kErrTimeout);
+      if (!__all_sync(0xffffffffu, got)) break;
+      sph ^= 1u;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(lane_base + C::kColS + 32 * q, sv);
+        tmem_ld32(lane_base + C::kColDP + 32 * q, dv);
+        uint32_t pp[16], pg[16];
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          const int c0 = 32 * q + 2 * b;
+          float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * b]), c2, -s_lse[c0]));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * b + 1]), c2, -s_lse[c0 + 1]));
+          if (!((w[q] >> (2 * b)) & 1u)) p0 = 0.f;
+          if (!((w[q] >> (2 * b + 1)) & 1u)) p1 = 0.f;
+          const float g0 = p0 * fmaf(__uint_as_float(dv[2 * b]), dsc, -s_dd[c0]);
+          const float g1 = p1 * fmaf(__uint_as_float(dv[2 * b + 1]), dsc, -s_dd[c0 + 1]);
+          pp[b] = pack_bf16x2(p0, p1);
+          pg[b] = pack_bf16x2(g0, g1);
+        }
+        tmem_st16(lane_base + C::kColS + 16 * q, pp);
+        tmem_st16(lane_base + C::kColDP + 16 * q, pg);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(C::kBarP));
+      ++n_done;
+    }
+    // ---------------------------------------------------------- epilogue
+    bool have = false;
+    if (n_done > 0) {
+      have = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarDone), 0, p.budget, p.err, kErrTimeout));
+      if (have) tc_fence_after();
+    }
+    const int cpk = (!packed_unit && key_valid && p.n_cols) ? p.colidx[j] : -1;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // 0: dV, 1: dK
+      const uint32_t col = half ? C::kColDK : C::kColDV;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        if (have) {
+          tmem_ld32(lane_base + col + 32 * q, o);
+        } else {
+#pragma unroll
+          for (int b = 0; b < 32; ++b) o[b] = 0u;
+        }
+        if (!key_valid) continue;
+        if (packed_unit) {
+          float* dst = (half ? p.dKc : p.dVc) + (static_cast<size_t>(bh) * p.n_cols + key) * D + 32 * q;
+#pragma unroll
+          for (int b = 0; b < 32; b += 4)
+            *reinterpret_cast<float4*>(dst + b) =
+                make_float4(__uint_as_float(o[b]), __uint_as_float(o[b + 1]),
+                            __uint_as_float(o[b + 2]), __uint_as_float(o[b + 3]));
+          continue;
+        }
+        float f[32];
+#pragma unroll
+        for (int b = 0; b < 32; ++b) f[b] = __uint_as_float(o[b]);
+        if (cpk >= 0) {
+          const float* src = (half ? p.dKc : p.dVc) + (static_cast<size_t>(bh) * p.n_cols + cpk) * D + 32 * q;
+#pragma unroll
+          for (int b = 0; b < 32; b += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + b);
+            f[b] += x.x;
+            f[b + 1] += x.y;
+            f[b + 2] += x.z;
+            f[b + 3] += x.w;
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>((half ? p.dK : p.dV) + (head + j) * D + 32 * q);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 x;
+          x.x = pack_bf16x2(f[8 * v4 + 0], f[8 * v4 + 1]);
+          x.y = pack_bf16x2(f[8 * v4 + 2], f[8 * v4 + 3]);
+          x.z = pack_bf16x2(f[8 * v4 + 4], f[8 * v4 + 5]);
+          x.w = pack_bf16x2(f[8 * v4 + 6], f[8 * v4 + 7]);
+          dst[v4] = x;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+#undef BAR
+}
+
+template <int D>
+cudaError_t launch_kv_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
+  using C = KvCfg<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const long long T = a.mask.T;
+  CUtensorMap mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc;
+  bool ok = make_map(&mQ, a.Q, D, T, a.BH) && make_map(&mdO, a.dO, D, T, a.BH) &&
+            make_map(&mK, a.K, D, T, a.BH) && make_map(&mV, a.V, D, T, a.BH);
+  ok = ok && (a.n_cols > 0 ? make_map(&mKc, a.Kc, D, a.n_cols, a.BH) && make_map(&mVc, a.Vc, D, a.n_cols, a.BH)
+                           : (mKc = mK, mVc = mV, true));
+  ok = ok && (a.mask.n_global > 0 ? make_map(&mQg, a.Qg, D, a.mask.n_global, a.BH) &&
+                                        make_map(&mdOg, a.dOg, D, a.mask.n_global, a.BH)
+                                  : (mQg = mQ, mdOg = mdO, true));
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  KvParams kp;
+  kp.dK = static_cast<__nv_bfloat16*>(a.dK);
+  kp.dV = static_cast<__nv_bfloat16*>(a.dV);
+  kp.dKc = a.dKc;
+  kp.dVc = a.dVc;
+  kp.LSE = a.LSE;
+  kp.Dvec = a.Dvec;
+  kp.scale = a.scale;
+  kp.scale_log2 = a.scale * 1.4426950408889634f;
+  kp.colmask = a.colmask;
+  kp.mask = a.mask;
+  kp.cols = a.cols;
+  kp.colidx = a.colidx;
+  kp.rt_off = a.rt_off;
+  kp.rt_qb = a.rt_qb;
+  kp.units = a.units;
+  kp.entries = a.u_entries;
+  kp.n_cols = a.n_cols;
+  kp.err = a.err;
+  kp.budget = a.wait_budget_cycles;
+  kp.BH = a.BH;
+  // packed units first: their partial sums are added by the natural units
+  const int parts[2][2] = {{0, a.n_packed_units}, {a.n_packed_units, a.n_units}};
+  for (const auto& pr : parts) {
+    const long long ctas = static_cast<long long>(pr[1] - pr[0]) * a.BH;
+    if (ctas <= 0) continue;
+    if (ctas > 0x7fffffffLL) {
+      *why = "too many key units";
+      return cudaErrorInvalidValue;
+    }
+    kp.unit0 = pr[0];
+    bwd_dkdv_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, st>>>(
+        mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc, kp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_dq_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
   using C = DqCfg<D>;
@@ -386,6 +847,13 @@ cudaError_t launch_dq_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
 }
 
 }  // namespace
+
+cudaError_t launch_bwd_dkdv_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why) {
+  if (d == 64) return launch_kv_d<64>(a, st, why);
+  if (d == 128) return launch_kv_d<128>(a, st, why);
+  *why = "head dim must be 64 or 128";
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_bwd_dq_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why) {
   if (a.n_items == 0) return cudaSuccess;

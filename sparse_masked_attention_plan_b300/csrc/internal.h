@@ -102,8 +102,13 @@ struct spattn_plan {
   uint8_t* d_rowzero = nullptr;       // no global rows
   // key-major schedule of the backward pass and the packed index of every key
   // (-1 where the key is not a sparse column)
-  spattn::Schedule bsched;
+  spattn::Schedule bsched;     // 64-key units, 64-row groups (FP32-unit kernels)
+  spattn::Schedule bsched_tc;  // 128-key units, 128-row groups (tensor-core kernel)
   int32_t* d_colidx = nullptr;
+  // random blocks transposed (key block -> query blocks), for the key-major kernels
+  std::vector<int32_t> rt_off, rt_qb;
+  int32_t* d_rtoff = nullptr;
+  int32_t* d_rtqb = nullptr;
   // packing scratch (packed K, V of the sparse columns and gathered global-row Q)
   void* d_scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -233,8 +238,9 @@ struct BwdArgs {
   int32_t n_packed_units;
   int32_t n_units;
 };
-// with_dq = false leaves dQ to the tensor-core kernel (the row dots are still written)
-cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st, bool with_dq = true);
+// The row dots D_i always; dQ and dK/dV unless the tensor-core kernels take them.
+cudaError_t launch_bwd_simt(int d, const BwdArgs& a, cudaStream_t st, bool with_dq = true,
+                            bool with_dkdv = true);
 
 // bwd_tc.cu (bf16 dQ on the tensor cores; walks the tensor-core forward schedule)
 struct BwdTcArgs {
@@ -259,8 +265,22 @@ struct BwdTcArgs {
   int32_t n_items;
   int* err;
   uint64_t wait_budget_cycles;
+  // key-major dK / dV
+  void* dK;
+  void* dV;
+  float* dKc;
+  float* dVc;
+  const int32_t* cols;
+  const int32_t* colidx;
+  const int32_t* rt_off;
+  const int32_t* rt_qb;
+  const int4* units;
+  const int4* u_entries;
+  int32_t n_packed_units;
+  int32_t n_units;
 };
 cudaError_t launch_bwd_dq_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why);
+cudaError_t launch_bwd_dkdv_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why);
 
 // decode.cu (one generation step against a ring-buffer KV cache)
 struct DecodeArgs {

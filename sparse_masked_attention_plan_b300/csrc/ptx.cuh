@@ -33,6 +33,11 @@ __device__ __forceinline__ bool elect_one() {
 
 // Named barrier over `count` threads (a multiple of 32) that also ANDs a predicate:
 // every participating thread gets the AND of all threads' `pred`.
+// Named barrier `id` (1..15) among `count` threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
   asm volatile(

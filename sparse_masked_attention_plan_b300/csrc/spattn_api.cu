@@ -50,7 +50,8 @@ void free_plan_memory(spattn_plan* p) {
                   p->sched[1].d_items, p->sched[1].d_entries, p->sched[2].d_items,
                   p->sched[2].d_entries, p->d_colmask_res, p->d_rowzero,
                   p->bsched.d_items, p->bsched.d_entries, p->d_colidx, p->d_bscratch,
-                  p->d_roff, p->d_rkb};
+                  p->d_roff, p->d_rkb, p->bsched_tc.d_items, p->bsched_tc.d_entries,
+                  p->d_rtoff, p->d_rtqb};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -261,24 +262,26 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
 }
 
 // Key-major schedule of the backward pass: the same decomposition of every row's
-// allowed set as the forward schedule with 64-row groups (band keys of the natural
-// grid inside the group's band range, packed sparse columns outside it, dense walks
-// for global rows), listed per 64-key unit instead of per query group, so that the
-// gradient of every key is summed inside one CTA.
-void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s) {
+// allowed set as the forward schedule (band keys of the natural grid inside the
+// group's band range, packed sparse columns outside it, random-block tiles, dense
+// walks for global rows), with groups of kRows query rows listed per unit of kKeys
+// keys instead of per query group, so that the gradient of every key is summed inside
+// one CTA.  kKeys divides the 128-key tile; kRows is 64 or 128.
+void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s, int64_t kRows,
+                        int64_t kKeys) {
   using namespace spattn;
   Sched h{p};
   const int64_t T = p->T;
   const int64_t nc = p->n_cols;
-  const int64_t nu_nat = (T + kBwdKeys - 1) / kBwdKeys, nu_pk = (nc + kBwdKeys - 1) / kBwdKeys;
+  const int64_t nu_nat = (T + kKeys - 1) / kKeys, nu_pk = (nc + kKeys - 1) / kKeys;
   std::vector<std::vector<int32_t>> nat(nu_nat), pk(nu_pk);
   auto add = [](std::vector<int32_t>& v, int64_t q0, int32_t flags, int64_t a, int64_t b) {
     v.insert(v.end(), {static_cast<int32_t>(q0), flags, static_cast<int32_t>(a),
                        static_cast<int32_t>(b)});
   };
   const int64_t d = p->dilation;
-  for (int64_t r0 = 0; r0 < T; r0 += kBwdRows) {
-    const int64_t r1 = std::min<int64_t>(r0 + kBwdRows, T) - 1;
+  for (int64_t r0 = 0; r0 < T; r0 += kRows) {
+    const int64_t r1 = std::min<int64_t>(r0 + kRows, T) - 1;
     int64_t jlo, jhi;
     if (p->causal) {
       jlo = p->window ? std::max<int64_t>(0, r0 - (p->window - 1) * d) : 0;
@@ -288,26 +291,26 @@ void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s) {
       jhi = p->radius >= 0 ? std::min<int64_t>(T - 1, r1 + p->radius * d) : T - 1;
     }
     const int64_t kb_lo = jlo / kTile, kb_hi = jhi / kTile;
-    const int64_t u_hi = std::min<int64_t>(nu_nat - 1, (kb_hi + 1) * (kTile / kBwdKeys) - 1);
-    for (int64_t u = kb_lo * (kTile / kBwdKeys); u <= u_hi; ++u) {
-      const int64_t k0 = u * kBwdKeys, k1 = std::min<int64_t>(k0 + kBwdKeys, T) - 1;
+    const int64_t u_hi = std::min<int64_t>(nu_nat - 1, (kb_hi + 1) * (kTile / kKeys) - 1);
+    for (int64_t u = kb_lo * (kTile / kKeys); u <= u_hi; ++u) {
+      const int64_t k0 = u * kKeys, k1 = std::min<int64_t>(k0 + kKeys, T) - 1;
       if (h.local_meets(r0, r1, k0, k1) || h.cols_in(k0, p->causal ? std::min(k1, r1) : k1) ||
           h.rand_in(r0, r1, k0, k1))
         add(nat[u], r0, kKindBand << kKindShift, 0, 0);
     }
     {  // units outside the band range that random blocks of the group's rows reach
       std::vector<int64_t> ru;
-      h.rand_tiles(r0, r1, kBwdKeys, &ru);
+      h.rand_tiles(r0, r1, kKeys, &ru);
       std::vector<int64_t> all;
       for (int64_t u0 : ru)  // a random block of b keys spans b / 64 units (or part of one)
-        for (int64_t u = u0; u < u0 + std::max<int64_t>(1, p->rand_block / kBwdKeys); ++u)
+        for (int64_t u = u0; u < u0 + std::max<int64_t>(1, p->rand_block / kKeys); ++u)
           all.push_back(u);
       std::sort(all.begin(), all.end());
       all.erase(std::unique(all.begin(), all.end()), all.end());
-      const int64_t band_u0 = kb_lo * (kTile / kBwdKeys);
+      const int64_t band_u0 = kb_lo * (kTile / kKeys);
       for (int64_t u : all) {
         if (u >= nu_nat || (u >= band_u0 && u <= u_hi)) continue;
-        const int64_t k0 = u * kBwdKeys, k1 = std::min<int64_t>(k0 + kBwdKeys, T) - 1;
+        const int64_t k0 = u * kKeys, k1 = std::min<int64_t>(k0 + kKeys, T) - 1;
         if (h.rand_in(r0, r1, k0, k1)) add(nat[u], r0, kKindRandom << kKindShift, 0, 0);
       }
     }
@@ -316,20 +319,20 @@ void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s) {
       const int64_t e_idx = p->causal ? h.upper(r1) : nc;
       const int64_t ranges[2][2] = {{0, std::min(a_idx, e_idx)}, {b_idx, e_idx}};
       for (auto& rg : ranges)
-        for (int64_t u = rg[0] / kBwdKeys; rg[0] < rg[1] && u <= (rg[1] - 1) / kBwdKeys; ++u)
-          add(pk[u], r0, kKindPacked << kKindShift, std::max(rg[0], u * kBwdKeys),
-              std::min(rg[1], (u + 1) * kBwdKeys));
+        for (int64_t u = rg[0] / kKeys; rg[0] < rg[1] && u <= (rg[1] - 1) / kKeys; ++u)
+          add(pk[u], r0, kKindPacked << kKindShift, std::max(rg[0], u * kKeys),
+              std::min(rg[1], (u + 1) * kKeys));
     }
   }
   const int64_t ng = static_cast<int64_t>(p->gpos.size());
-  for (int64_t q0 = 0; q0 < ng; q0 += kBwdRows) {
-    const int64_t last = p->gpos[std::min<int64_t>(q0 + kBwdRows, ng) - 1];
-    const int64_t u_hi = (p->causal ? last : T - 1) / kBwdKeys;
+  for (int64_t q0 = 0; q0 < ng; q0 += kRows) {
+    const int64_t last = p->gpos[std::min<int64_t>(q0 + kRows, ng) - 1];
+    const int64_t u_hi = (p->causal ? last : T - 1) / kKeys;
     for (int64_t u = 0; u <= u_hi; ++u)
       add(nat[u], q0, (kKindDense << kKindShift) | kEntryGathered, 0, 0);
   }
-  s->group_rows = kBwdRows;
-  s->qtile_rows = kBwdRows;
+  s->group_rows = kRows;
+  s->qtile_rows = kRows;
   s->n_qtiles = 1;
   s->items.clear();
   s->entries.clear();
@@ -343,8 +346,8 @@ void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s) {
     s->entries.insert(s->entries.end(), v.begin(), v.end());
     s->tile_products += cnt;
   };
-  for (int64_t u = 0; u < nu_pk; ++u) emit(pk[u], u * kBwdKeys, kUnitPacked);
-  for (int64_t u = 0; u < nu_nat; ++u) emit(nat[u], u * kBwdKeys, 0);
+  for (int64_t u = 0; u < nu_pk; ++u) emit(pk[u], u * kKeys, kUnitPacked);
+  for (int64_t u = 0; u < nu_nat; ++u) emit(nat[u], u * kKeys, 0);
 }
 
 spattn_status upload_schedule(spattn::Schedule* s) {
@@ -612,13 +615,34 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
     if (e == cudaSuccess) e = cudaMemset(p->d_rowzero, 0, size_t(v.T));
     if (e != cudaSuccess) return bail(fail(SPATTN_ERR_CUDA, "plan: %s", cudaGetErrorString(e)));
   }
-  build_bwd_schedule(p, &p->bsched);
+  build_bwd_schedule(p, &p->bsched, spattn::kBwdRows, spattn::kBwdKeys);
+  build_bwd_schedule(p, &p->bsched_tc, spattn::kTile, spattn::kTile);
+  {  // random blocks transposed: key block -> the query blocks that list it
+    if (!p->r_kb.empty()) {
+      const int64_t nb = static_cast<int64_t>(p->r_off.size()) - 1;
+      p->rt_off.assign(static_cast<size_t>(nb) + 1, 0);
+      for (int32_t k : p->r_kb) ++p->rt_off[k + 1];
+      for (int64_t q = 0; q < nb; ++q) p->rt_off[q + 1] += p->rt_off[q];
+      p->rt_qb.assign(p->r_kb.size(), 0);
+      std::vector<int32_t> fill(p->rt_off.begin(), p->rt_off.end() - 1);
+      for (int64_t q = 0; q < nb; ++q)
+        for (int32_t x = p->r_off[q]; x < p->r_off[q + 1]; ++x) p->rt_qb[fill[p->r_kb[x]]++] = static_cast<int32_t>(q);
+    }
+    cudaError_t e = dev_alloc(&p->d_rtoff, p->rt_off.size());
+    if (e == cudaSuccess) e = dev_alloc(&p->d_rtqb, p->rt_qb.size());
+    if (e == cudaSuccess && !p->rt_qb.empty())
+      e = cudaMemcpy(p->d_rtoff, p->rt_off.data(), p->rt_off.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !p->rt_qb.empty())
+      e = cudaMemcpy(p->d_rtqb, p->rt_qb.data(), p->rt_qb.size() * 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return bail(fail(SPATTN_ERR_CUDA, "plan: %s", cudaGetErrorString(e)));
+  }
   for (auto& s : p->sched) {
     spattn_status us = upload_schedule(&s);
     if (us != SPATTN_OK) return bail(us);
   }
   {
     spattn_status us = upload_schedule(&p->bsched);
+    if (us == SPATTN_OK) us = upload_schedule(&p->bsched_tc);
     if (us != SPATTN_OK) return bail(us);
     std::vector<int32_t> colidx(size_t(T), -1);
     for (int32_t c = 0; c < p->n_cols; ++c) colidx[p->cols[c]] = c;
@@ -673,8 +697,8 @@ spattn_status spattn_plan_copy_schedule(const spattn_plan* p, int32_t which, int
                                         int64_t entry_cap, int64_t* n_entries,
                                         int64_t* tile_products) {
   if (!p) return fail(SPATTN_ERR_NULL, "plan is NULL");
-  if (which < 0 || which > 3) return fail(SPATTN_ERR_SHAPE, "which must be 0, 1, 2 or 3");
-  const spattn::Schedule& s = which == 3 ? p->bsched : p->sched[which];
+  if (which < 0 || which > 4) return fail(SPATTN_ERR_SHAPE, "which must be 0 .. 4");
+  const spattn::Schedule& s = which == 4 ? p->bsched_tc : which == 3 ? p->bsched : p->sched[which];
   const int64_t ni = s.items.size() / 4, ne = s.entries.size() / 4;
   if (n_items) *n_items = ni;
   if (n_entries) *n_entries = ne;
@@ -839,7 +863,7 @@ spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
   a.u_entries = p->bsched.d_entries;
   a.n_packed_units = p->bsched.n_packed_units;
   a.n_units = static_cast<int32_t>(p->bsched.items.size() / 4);
-  cudaError_t e = spattn::launch_bwd_simt(p->d, a, stream, !tc);
+  cudaError_t e = spattn::launch_bwd_simt(p->d, a, stream, !tc, !tc);
   if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   if (tc) {
     uint8_t* pk = base + dvec_bytes + 2 * kc_bytes;
@@ -878,10 +902,25 @@ spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
     t.n_items = static_cast<int32_t>(p->sched[0].items.size() / 4);
     t.err = p->d_err;
     t.wait_budget_cycles = p->wait_budget_cycles;
+    t.dK = dK;
+    t.dV = dV;
+    t.dKc = a.dKc;
+    t.dVc = a.dVc;
+    t.cols = p->d_cols;
+    t.colidx = p->d_colidx;
+    t.rt_off = p->d_rtoff;
+    t.rt_qb = p->d_rtqb;
+    t.units = p->bsched_tc.d_items;
+    t.u_entries = p->bsched_tc.d_entries;
+    t.n_packed_units = p->bsched_tc.n_packed_units;
+    t.n_units = static_cast<int32_t>(p->bsched_tc.items.size() / 4);
     const char* why = "";
     e = spattn::launch_bwd_dq_tc(p->d, t, stream, &why);
     if (e != cudaSuccess)
       return fail(SPATTN_ERR_CUDA, "tensor-core dQ launch: %s (%s)", cudaGetErrorString(e), why);
+    e = spattn::launch_bwd_dkdv_tc(p->d, t, stream, &why);
+    if (e != cudaSuccess)
+      return fail(SPATTN_ERR_CUDA, "tensor-core dK/dV launch: %s (%s)", cudaGetErrorString(e), why);
   }
   return SPATTN_OK;
 }

@@ -123,13 +123,13 @@ def test_backward_is_deterministic(oracle_mod):
         assert np.array_equal(a, b)
 
 
-def _key_major_cover(plan, T, mask):
+def _key_major_cover(plan, T, mask, which=3, rows_per=64, keys_per=64):
     """How often the key-major schedule visits each (query, key) pair: a band entry
     visits the allowed pairs of its non-global rows inside its unit, a random entry
     their random-block pairs that are not sparse columns, a packed entry its packed
     columns [a, b), a gathered dense entry the allowed pairs of its global rows inside
     its unit."""
-    items, ents, _ = plan.schedule(3)
+    items, ents, _ = plan.schedule(which)
     cols = plan.columns()
     g = np.asarray(sorted(mask.get("global_pos", [])), dtype=np.int64)
     M = np_dense_mask(T, mask.get("causal", 1), mask.get("window", 0), mask.get("radius", -1),
@@ -152,16 +152,16 @@ def _key_major_cover(plan, T, mask):
         for q0, ef, a, b in ents[off:off + cnt]:
             kind = (ef >> 4) & 3
             if ef & 1:
-                rows = g[q0:q0 + 64]
+                rows = g[q0:q0 + rows_per]
             else:
-                rows = np.arange(q0, min(q0 + 64, T))
+                rows = np.arange(q0, min(q0 + rows_per, T))
                 rows = rows[~isg[rows]]
             if packed_unit:
                 assert kind == 1
                 keys = cols[a:b]
                 cov[np.ix_(rows, keys)] += 1
             else:
-                keys = np.arange(key0, min(key0 + 64, T))
+                keys = np.arange(key0, min(key0 + keys_per, T))
                 if kind == 3:  # random-only unit: random keys that are not sparse columns
                     sub = (Rm[np.ix_(rows, keys)] & ~colset[keys][None, :]).astype(np.int32)
                 else:
@@ -170,11 +170,12 @@ def _key_major_cover(plan, T, mask):
     return cov, M
 
 
+@pytest.mark.parametrize("granule", [(3, 64, 64), (4, 128, 128)], ids=["fp32", "tc"])
 @pytest.mark.parametrize("k", range(len(SWEEP)))
-def test_key_major_schedule_covers_every_pair_once(k):
+def test_key_major_schedule_covers_every_pair_once(k, granule):
     _, _, T, d, mask = SWEEP[k]
     plan = sp.Plan(T, d, **mask)
-    cov, M = _key_major_cover(plan, T, mask)
+    cov, M = _key_major_cover(plan, T, mask, *granule)
     bad = np.argwhere(cov != M.astype(np.int32))
     assert bad.size == 0, f"pairs visited {cov[tuple(bad[0])]} times, allowed {M[tuple(bad[0])]}: {bad[:5]}"
 
