@@ -422,7 +422,7 @@ def run_ours_bwd(args, cfg, p):
             "metric": BWD_METRIC, "pass": "bwd", "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16 in/out, fp32 arithmetic", "data": "synthetic",
+            "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d,
                        "mask": mask_desc(p), "pairs_per_head": info["pairs_per_head"],
                        "l2": "inputs larger than L2" if 6 * q.numel() * 2 > 126e6

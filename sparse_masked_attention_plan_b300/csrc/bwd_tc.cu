@@ -9,15 +9,18 @@
 // A CTA owns one 128-row query tile of one (batch, head) and walks the key tiles the
 // forward schedule gives that tile (band tiles, packed sparse columns, dense walks of
 // global rows), with the forward's per-row predicate inside partial tiles.
-// Warp roles (192 threads):
-//   warps 0-3  elementwise: P and dS of one query row per thread (its TMEM lane)
-//   warp 4     TMA producer: Q and dO tiles once, then K and V tiles into a ring
-//   warp 5     MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
+// Warp roles (320 threads):
+//   warps 0-7  elementwise: P and dS of one query row per thread (its TMEM lane), warps
+//              0-3 for key columns 0-63, warps 4-7 for columns 64-127 (two warps per
+//              sub-partition hide each other's latency)
+//   warp 8     TMA producer: Q and dO tiles once, then K and V tiles into a ring
+//   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
 //              memory), then dQ += dS K with dS (bf16) from TMEM and the same K tile
 //              read as an MN-major operand
-// TMEM: S [0,128), dP [128,256), dQ [256,256+d).  dS overwrites the first 64 columns
-// of S; the tensor pipe runs products in issue order, so the next tile's S (issued
-// after dQ) cannot overwrite dS before dQ has read it.  P needs no running maximum:
+// TMEM: S [0,128), dP [128,256), dQ [256,256+d).  dS (bf16) overwrites S: each
+// warpgroup packs its 64 columns into the first 32 of its own half; the tensor pipe runs
+// products in issue order, so the next tile's S (issued after dQ) cannot overwrite dS
+// before dQ has read it.  P needs no running maximum:
 // the forward's LSE already normalises it.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -35,9 +38,9 @@
 namespace spattn {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 
 template <int D>
 struct DqCfg {
@@ -47,9 +50,11 @@ struct DqCfg {
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;  // Q and dO
   static constexpr int kSmemKV = kStages * kTileBytes;
+  // kBarP + q: chunk q (keys 32q .. 32q+31) of dS is in TMEM; one barrier per chunk
+  // so each completes once per key tile and a waiter can never miss a phase
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
                        kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 2,
-                       kBarDone = 2 * kStages + 3, kNumBars = 2 * kStages + 4;
+                       kBarDone = 2 * kStages + 6, kNumBars = 2 * kStages + 7;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
@@ -81,14 +86,25 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint64_t a_desc, u
   }
 }
 
+// Where chunk q (tile columns 32q .. 32q+31) of a bf16 result lives in TMEM, relative to
+// the fp32 region it was computed from: each warpgroup packs its two chunks into the
+// first half of its own 64 columns, which only it reads, so no warpgroup overwrites
+// columns the other has yet to load.
+__device__ __forceinline__ uint32_t chunk_col(int q) { return 64u * (q >> 1) + 16u * (q & 1); }
+
+// k-steps 2 chunk, 2 chunk + 1 of an accumulating product over the 128-wide tile
+// dimension: the 32 columns one elementwise chunk has just written to TMEM (A, at
+// a_chunk) against rows 32 chunk .. of the MN-major shared-memory operand (B).
 template <int D>
-__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t a_tmem, uint64_t k_mn_desc,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_acc_chunk(uint32_t d_tmem, uint32_t a_chunk, uint64_t b_mn_desc,
+                                                int chunk, bool accumulate) {
   using C = DqCfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + kk * 8, k_mn_desc + ((kk * 16 * 128) >> 4), C::kIdescDQ,
+  for (int k = 0; k < 2; ++k) {
+    const int kk = 2 * chunk + k;
+    mma_ts(d_tmem, a_chunk + k * 8, b_mn_desc + ((kk * 16 * 128) >> 4), C::kIdescDQ,
            (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 template <int D>
@@ -131,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::kBarQ), 1);
     mbar_init(BAR(C::kBarS), 1);
-    mbar_init(BAR(C::kBarP), 128);
+    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 128);
     mbar_init(BAR(C::kBarDone), 1);
     fence_barrier_init();
   }
@@ -159,8 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     int issued = 0;
     bool ok = true;
+    int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     for (int n = 0; n < n_ent && ok; ++n) {
-      const int4 e = ents[n];
+      const int4 e = e_next;
+      if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: latency off the issue path
       if (!(e.y & active_bit)) continue;
       const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
 #pragma unroll
@@ -204,8 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pph = 0;
       int done = 0;
       int it = 0;
+      int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
       for (int n = 0; n < n_ent; ++n) {
-        const int4 e = ents[n];
+        const int4 e = e_next;
+        if (n + 1 < n_ent) e_next = ents[n + 1];
         if (!(e.y & active_bit)) continue;
         const int kit = it, vit = it + 1;
         it += 2;
@@ -224,16 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(BAR(C::kBarEmpty + vs));  // V is no longer needed
         }
         __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP), pph, p.budget, p.err, kErrTimeout))) {
-          ok = false;
-          break;
+        // dQ += dS K, 32 keys at a time as the elementwise warps hand over each chunk
+        for (int q = 0; q < 4 && ok; ++q) {
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), pph, p.budget, p.err, kErrTimeout))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one())
+            issue_acc_chunk<D>(tmem + C::kColDQ, tmem + C::kColS + chunk_col(q), kv_mndesc + ks * kSlot16,
+                               q, done > 0);
+          __syncwarp();
         }
+        if (!ok) break;
         pph ^= 1u;
-        tc_fence_after();
-        if (elect_one()) {
-          issue_dq<D>(tmem + C::kColDQ, tmem + C::kColS, kv_mndesc + ks * kSlot16, done > 0);
-          mma_commit(BAR(C::kBarEmpty + ks));
-        }
+        if (elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
         __syncwarp();
         ++done;
       }
@@ -244,8 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise warps
-    const int r = (warp << 5) | lane;
-    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+    const int wg = warp >> 2;  // column half
+    const int r = ((warp & 3) << 5) | lane;
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
     int i;
     bool valid;
     if (gathered) {
@@ -261,44 +287,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float dsc = p.scale;
     const float dterm = valid ? -p.Dvec[row] * dsc : 0.f;
     const float c2 = p.scale_log2;
+    const uint64_t c2x2 = f32x2(c2, c2), nl2x2 = f32x2(-lse2, -lse2);
+    const uint64_t dsc2 = f32x2(dsc, dsc), dterm2 = f32x2(dterm, dterm);
     uint32_t sph = 0;
     int n_done = 0;
+    int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     for (int n = 0; n < n_ent; ++n) {
-      const int4 e = ents[n];
+      const int4 e = e_next;
+      if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead, consumed next iteration
       if (!(e.y & active_bit)) continue;
+      // the row's mask words, computed before the wait so their loads overlap the products
+      uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (!(e.y & full_bit)) row_mask(make_predicate(m, p.colmask, e, i), w);
       const bool got = mbar_wait(BAR(C::kBarS), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
       tc_fence_after();
-      uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (!(e.y & full_bit)) row_mask(make_predicate(m, p.colmask, e, i), w);
       if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
       // dS = scale P (dP - D) with P = 2^(s scale log2 e - LSE log2 e), 32 columns at a
       // time; the bf16 result of chunk q lands in columns 16q .. 16q+15, all of which
       // the chunks up to q have already read
+      {
+        const int h = wg;
+        uint32_t sv64[64], dv64[64];  // S and dP of columns 64h .. 64h+63, one wait
+        tmem_ld64x2(lane_base + C::kColS + 64 * h, sv64, lane_base + C::kColDP + 64 * h, dv64);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(lane_base + C::kColS + 32 * q, sv);
-        tmem_ld32(lane_base + C::kColDP + 32 * q, dv);
+      for (int qq = 0; qq < 2; ++qq) {
+        const int q = 2 * h + qq;
+        const uint32_t* sv = sv64 + 32 * qq;
+        const uint32_t* dv = dv64 + 32 * qq;
         uint32_t pk[16];
+        const bool all = w[q] == 0xffffffffu;
 #pragma unroll
         for (int b = 0; b < 16; ++b) {
           const int c0 = 2 * b;
-          float x0 = fmaf(__uint_as_float(sv[c0]), c2, -lse2);
-          float x1 = fmaf(__uint_as_float(sv[c0 + 1]), c2, -lse2);
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])), c2x2,
+                                nl2x2), x0, x1);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          if (!((w[q] >> c0) & 1u)) p0 = 0.f;
-          if (!((w[q] >> (c0 + 1)) & 1u)) p1 = 0.f;
-          const float g0 = p0 * fmaf(__uint_as_float(dv[c0]), dsc, dterm);
-          const float g1 = p1 * fmaf(__uint_as_float(dv[c0 + 1]), dsc, dterm);
+          if (!all) {
+            if (!((w[q] >> c0) & 1u)) p0 = 0.f;
+            if (!((w[q] >> (c0 + 1)) & 1u)) p1 = 0.f;
+          }
+          const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
+                                        dsc2, dterm2);
+          float g0, g1;
+          f32x2_split(mul_f32x2(f32x2(p0, p1), t2), g0, g1);
           pk[b] = pack_bf16x2(g0, g1);
         }
-        tmem_st16(lane_base + C::kColS + 16 * q, pk);
+        tmem_st16(lane_base + C::kColS + chunk_col(q), pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(BAR(C::kBarP));
+      }
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
@@ -310,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint4* dst = reinterpret_cast<uint4*>(p.dQ + row * D);
 #pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
+    for (int qh = 0; qh < D / 64; ++qh) {  // this warpgroup's half of the d columns
+      const int q = wg * (D / 64) + qh;
       uint32_t o[32];
       if (have) {
         tmem_ld32(lane_base + C::kColDQ + 32 * q, o);
@@ -343,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- dK, dV (key-major)
 //
 //     dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i   (i with j in S_i)
+// Warp roles as in the dQ kernel (warps 0-7 elementwise over the two query-column
+// halves, 8 producer, 9 MMA).
 // A CTA owns one 128-key unit (natural keys, or packed sparse columns) of one (batch,
 // head): its K and V tiles stay in shared memory while the 128-row query tiles that
 // read it stream through a ring (Q and dO per stage).  Per query tile:
@@ -369,13 +414,13 @@ struct KvCfg {
   static constexpr int kSmemKV = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * 2 * kTileBytes;
   static constexpr int kSmemVec = 2 * 2 * kTile * 4;  // LSE and D, double-buffered
+  // kBarP + q: chunk q (queries 32q .. 32q+31) of P^T and dS^T is in TMEM
   static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages,
                        kBarS = 1 + 2 * kStages, kBarP = 2 + 2 * kStages,
-                       kBarDone = 3 + 2 * kStages, kBarVec = 4 + 2 * kStages,
-                       kNumBars = 6 + 2 * kStages;
+                       kBarDone = 6 + 2 * kStages, kBarVec = 7 + 2 * kStages,
+                       kNumBars = 9 + 2 * kStages;
   static constexpr int kSmemBytes = kSmemKV + kSmemRing + kSmemVec + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
-  static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 0, 1);
+  // products use the dQ kernel's issue helpers (same shapes: 128 x 128 and 128 x d)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
 
@@ -508,10 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::kBarEmpty + s), 1);
     }
     mbar_init(BAR(C::kBarS), 1);
-    mbar_init(BAR(C::kBarP), 128);
+    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 128);
     mbar_init(BAR(C::kBarDone), 1);
-    mbar_init(BAR(C::kBarVec + 0), 128);
-    mbar_init(BAR(C::kBarVec + 1), 128);
+    mbar_init(BAR(C::kBarVec + 0), 256);
+    mbar_init(BAR(C::kBarVec + 1), 256);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -537,8 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     int issued = 0;
+    int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     for (int n = 0; n < n_ent; ++n) {
-      const int4 e = ents[n];
+      const int4 e = e_next;
+      if (n + 1 < n_ent) e_next = ents[n + 1];
       const bool gathered = (e.y & kEntryGathered) != 0;
       const int s = n % C::kStages;
       const uint32_t ph = (n / C::kStages) & 1;
@@ -587,17 +634,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(BAR(C::kBarS));
         }
         __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP), pph, p.budget, p.err, kErrTimeout))) {
-          ok = false;
-          break;
+        // dV += P^T dO and dK += dS^T Q, 32 queries at a time as each chunk arrives
+        for (int q = 0; q < 4 && ok; ++q) {
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), pph, p.budget, p.err, kErrTimeout))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            issue_acc_chunk<D>(tmem + C::kColDV, tmem + C::kColS + chunk_col(q),
+                               ring_mn + s * kStage16 + kDo16, q, n > 0);
+            issue_acc_chunk<D>(tmem + C::kColDK, tmem + C::kColDP + chunk_col(q),
+                               ring_mn + s * kStage16, q, n > 0);
+          }
+          __syncwarp();
         }
+        if (!ok) break;
         pph ^= 1u;
-        tc_fence_after();
-        if (elect_one()) {
-          issue_dq<D>(tmem + C::kColDV, tmem + C::kColS, ring_mn + s * kStage16 + kDo16, n > 0);
-          issue_dq<D>(tmem + C::kColDK, tmem + C::kColDP, ring_mn + s * kStage16, n > 0);
-          mma_commit(BAR(C::kBarEmpty + s));
-        }
+        if (elect_one()) mma_commit(BAR(C::kBarEmpty + s));
         __syncwarp();
       }
     }
@@ -607,36 +661,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise warps
-    const int kk = (warp << 5) | lane;  // key row of the unit = TMEM lane
-    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+    const int wg = warp >> 2;  // query-column half (and, in the epilogue, dV or dK)
+    const int kk = ((warp & 3) << 5) | lane;  // key row of the unit = TMEM lane
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
     const int key = unit.x + kk;
     const bool key_valid = packed_unit ? key < p.n_cols : key < m.T;
     const int j = key_valid ? (packed_unit ? p.cols[key] : key) : 0;
     const float c2 = p.scale_log2, dsc = p.scale;
+    const uint64_t c2x2 = f32x2(c2, c2), dsc2 = f32x2(dsc, dsc);
     const size_t head = static_cast<size_t>(bh) * m.T;
     uint32_t sph = 0;
     int n_done = 0;
+    // this thread's query column of an entry (warpgroup 0 loads them): LSE and D, one
+    // entry ahead so the global loads overlap the previous tile's work
+    auto column_values = [&](const int4& e, float& lse_v, float& dd_v) {
+      int i = -1;
+      const int a = e.x + kk;
+      if (e.y & kEntryGathered) {
+        if (a < m.n_global) i = m.gpos[a];
+      } else if (a < m.T && !m.rowglobal[a]) {
+        i = a;
+      }
+      lse_v = i >= 0 ? p.LSE[head + i] * 1.4426950408889634f : INFINITY;
+      dd_v = i >= 0 ? p.Dvec[head + i] * dsc : 0.f;
+    };
+    int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
+    float lse_next = 0.f, dd_next = 0.f;
+    if (n_ent && wg == 0) column_values(e_next, lse_next, dd_next);
     for (int n = 0; n < n_ent; ++n) {
-      const int4 e = ents[n];
-      const bool gathered = (e.y & kEntryGathered) != 0;
+      const int4 e = e_next;
+      const float lse_cur = lse_next, dd_cur = dd_next;
+      if (n + 1 < n_ent) e_next = ents[n + 1];
       const int kind = (e.y >> kKindShift) & 3;
       // this tile's per-query LSE and D, one column per thread, double-buffered: buffer
       // n & 1 is rewritten at tile n + 2, after every thread has passed tile n + 1's
       // barrier (and so has finished tile n)
       float* s_lse = s_vec + (n & 1) * 2 * kTile;
       float* s_dd = s_lse + kTile;
-      {
-        int i = -1;
-        const int a = e.x + kk;
-        if (gathered) {
-          if (a < m.n_global) i = m.gpos[a];
-        } else if (a < m.T && !m.rowglobal[a]) {
-          i = a;
-        }
-        s_lse[kk] = i >= 0 ? p.LSE[head + i] * 1.4426950408889634f : INFINITY;
-        s_dd[kk] = i >= 0 ? p.Dvec[head + i] * dsc : 0.f;
+      if (wg == 0) {
+        s_lse[kk] = lse_cur;
+        s_dd[kk] = dd_cur;
       }
       mbar_arrive(BAR(C::kBarVec + (n & 1)));
+      if (wg == 0 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next);
       if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + (n & 1)), (n >> 1) & 1, p.budget,
                                              p.err, kErrTimeout)))
         break;
@@ -647,30 +714,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
       tc_fence_after();
+      {
+        const int hh = wg;
+        uint32_t sv64[64], dv64[64];  // S^T and dP^T of columns 64hh .. 64hh+63, one wait
+        tmem_ld64x2(lane_base + C::kColS + 64 * hh, sv64, lane_base + C::kColDP + 64 * hh, dv64);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(lane_base + C::kColS + 32 * q, sv);
-        tmem_ld32(lane_base + C::kColDP + 32 * q, dv);
+      for (int qq = 0; qq < 2; ++qq) {
+        const int q = 2 * hh + qq;
+        const uint32_t* sv = sv64 + 32 * qq;
+        const uint32_t* dv = dv64 + 32 * qq;
         uint32_t pp[16], pg[16];
+        const bool all = w[q] == 0xffffffffu;
 #pragma unroll
-        for (int b = 0; b < 16; ++b) {
+        for (int b = 0; b < 16; b += 2) {  // four columns per step: one vector load each
           const int c0 = 32 * q + 2 * b;
-          float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * b]), c2, -s_lse[c0]));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * b + 1]), c2, -s_lse[c0 + 1]));
-          if (!((w[q] >> (2 * b)) & 1u)) p0 = 0.f;
-          if (!((w[q] >> (2 * b + 1)) & 1u)) p1 = 0.f;
-          const float g0 = p0 * fmaf(__uint_as_float(dv[2 * b]), dsc, -s_dd[c0]);
-          const float g1 = p1 * fmaf(__uint_as_float(dv[2 * b + 1]), dsc, -s_dd[c0 + 1]);
-          pp[b] = pack_bf16x2(p0, p1);
-          pg[b] = pack_bf16x2(g0, g1);
+          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c0);
+          const float4 d4 = *reinterpret_cast<const float4*>(s_dd + c0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int x = 2 * (b + h);  // column within the chunk
+            const float la = h ? l4.z : l4.x, lb = h ? l4.w : l4.y;
+            const float da = h ? d4.z : d4.x, db = h ? d4.w : d4.y;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), c2x2,
+                                  f32x2(-la, -lb)), x0, x1);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            if (!all) {
+              if (!((w[q] >> x) & 1u)) p0 = 0.f;
+              if (!((w[q] >> (x + 1)) & 1u)) p1 = 0.f;
+            }
+            const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1])),
+                                          dsc2, f32x2(-da, -db));
+            float g0, g1;
+            f32x2_split(mul_f32x2(f32x2(p0, p1), t2), g0, g1);
+            pp[b + h] = pack_bf16x2(p0, p1);
+            pg[b + h] = pack_bf16x2(g0, g1);
+          }
         }
-        tmem_st16(lane_base + C::kColS + 16 * q, pp);
-        tmem_st16(lane_base + C::kColDP + 16 * q, pg);
+        tmem_st16(lane_base + C::kColS + chunk_col(q), pp);
+        tmem_st16(lane_base + C::kColDP + chunk_col(q), pg);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(C::kBarP + q));  // queries 32q .. 32q+31 of P^T and dS^T are in TMEM
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(BAR(C::kBarP));
+      }
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
@@ -680,8 +767,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (have) tc_fence_after();
     }
     const int cpk = (!packed_unit && key_valid && p.n_cols) ? p.colidx[j] : -1;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {  // 0: dV, 1: dK
+    {
+      const int half = wg;  // warpgroup 0 writes dV, warpgroup 1 dK
       const uint32_t col = half ? C::kColDK : C::kColDV;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
