@@ -41,11 +41,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # 32K / W=4096 workload, from the ncu capture summarised in
 # profiles/fwd_tc_t32k_w4096.md (captured with H=8, 251.0 MB, scaled by 32/8 heads),
 # valid only for the kernel source with this hash; any other source reports null.
-TRAFFIC = {"kernel_sha": "a7b8bfe485cc9f3d", "bytes_per_launch": 1004.0e6, "workload": "t32k_w4096"}
+TRAFFIC = {"kernel_sha": "7e831f82a2f9cc44", "bytes_per_launch": 999.4e6, "workload": "t32k_w4096"}
+# The same for the backward's dominant kernel (bwd_dkdv_tc, profiles/bwd_tc_t32k_w4096.md,
+# H=4 capture x 8) and the decode kernel (profiles/decode_b8_w4096.md, B=8 capture, x 4
+# for B=32), keyed by their source hashes.
+BWD_TRAFFIC = {"kernel_sha": "a167f46651193842", "bytes_per_launch": 1358.1e6,
+               "workload": "t32k_w4096", "file": "bwd_tc.cu"}
+DEC_TRAFFIC = {"kernel_sha": "1500b47262601fb8", "file": "decode.cu",
+               "bytes_per_launch": {"decode_b8_w4096": 138.1e6, "decode_b32_w4096": 552.6e6}}
 
 
-def kernel_sha() -> str:
-    p = os.path.join(ROOT, "sparse_masked_attention_plan_b300", "csrc", "fwd_tc.cu")
+def kernel_sha(name: str = "fwd_tc.cu") -> str:
+    p = os.path.join(ROOT, "sparse_masked_attention_plan_b300", "csrc", name)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
@@ -429,7 +436,12 @@ def run_ours_bwd(args, cfg, p):
                              else "inputs fit in L2"},
             "roofline": {"bound": "tensor", "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                         "frac": achieved / peaks["bf16_tflops"],
+                         "traffic": (BWD_TRAFFIC["bytes_per_launch"]
+                                     if kernel_sha(BWD_TRAFFIC["file"]) == BWD_TRAFFIC["kernel_sha"]
+                                     and args.workload == BWD_TRAFFIC["workload"]
+                                     and not args.heads else None),
+                         "traffic_kernel": "bwd_dkdv_tc_kernel",
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "executed_tflops": achieved * 1.4,
                          "kernel": "rowdot + pack + bwd_dq_tc + bwd_dkdv_tc (whole step)",
@@ -538,7 +550,11 @@ def run_decode(args):
                        "l2": f"cache larger than L2 ({kv_bytes / 1e6:.0f} MB of K/V)"},
             "tokens_per_s": world * B / (ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": (DEC_TRAFFIC["bytes_per_launch"].get(args.decode_workload)
+                                     if kernel_sha(DEC_TRAFFIC["file"]) == DEC_TRAFFIC["kernel_sha"]
+                                     else None),
+                         "traffic_kernel": "decode_kernel",
                          "peak_source": f"{src} hbm_gbs",
                          "kernel": "kv_append + decode + combine (whole step)",
                          "kernel_ms": step_ms},
