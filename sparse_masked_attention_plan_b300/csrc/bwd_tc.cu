@@ -17,10 +17,10 @@
 //   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
 //              memory), then dQ += dS K with dS (bf16) from TMEM and the same K tile
 //              read as an MN-major operand
-// TMEM: S [0,128), dP [128,256), dQ [256,256+d).  dS (bf16) overwrites S: each
-// warpgroup packs its 64 columns into the first 32 of its own half; the tensor pipe runs
-// products in issue order, so the next tile's S (issued after dQ) cannot overwrite dS
-// before dQ has read it.  P needs no running maximum:
+// TMEM: per key half h (64 keys), S at 128h and dP at 128h + 64; dQ at 256.  dS (bf16)
+// overwrites the half's own S; the tensor pipe runs products in issue order, so the next
+// tile's S (issued after this half's dQ products) cannot overwrite dS before dQ has
+// read it.  The halves ping-pong between the two elementwise warpgroups.  P needs no running maximum:
 // the forward's LSE already normalises it.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -52,13 +52,15 @@ struct DqCfg {
   static constexpr int kSmemKV = kStages * kTileBytes;
   // kBarP + q: chunk q (keys 32q .. 32q+31) of dS is in TMEM; one barrier per chunk
   // so each completes once per key tile and a waiter can never miss a phase
+  // kBarS + h: S and dP of key half h are in TMEM
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
-                       kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 2,
-                       kBarDone = 2 * kStages + 6, kNumBars = 2 * kStages + 7;
+                       kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
+                       kBarDone = 2 * kStages + 7, kNumBars = 2 * kStages + 8;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0, 0);
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // TMEM: key half h has S at 128h and dP at 128h + 64 (64 columns each); dQ at 256
+  static constexpr uint32_t kColDQ = 256;
 };
 
 struct DqParams {
@@ -76,21 +78,20 @@ struct DqParams {
   int BH;
 };
 
+// A (128 rows) x B^T (64 rows, one half of a 128-row tile), both K-major over d: the
+// S and dP products of one tile half.  The B descriptor points at the half's first row
+// (64 rows x 128 bytes = 8 KB into each 64-column chunk).
 template <int D>
-__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+__device__ __forceinline__ void issue_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
   using C = DqCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, a_desc + off16, b_desc + off16, C::kIdescQK, kk > 0 ? 1u : 0u);
+    mma_ss(d_tmem, a_desc + off16, b_desc + off16, C::kIdescHalf, kk > 0 ? 1u : 0u);
   }
 }
+constexpr uint32_t kHalfRows16 = (64 * 128) >> 4;  // descriptor offset of a tile's row 64
 
-// Where chunk q (tile columns 32q .. 32q+31) of a bf16 result lives in TMEM, relative to
-// the fp32 region it was computed from: each warpgroup packs its two chunks into the
-// first half of its own 64 columns, which only it reads, so no warpgroup overwrites
-// columns the other has yet to load.
-__device__ __forceinline__ uint32_t chunk_col(int q) { return 64u * (q >> 1) + 16u * (q & 1); }
 
 // k-steps 2 chunk, 2 chunk + 1 of an accumulating product over the 128-wide tile
 // dimension: the 32 columns one elementwise chunk has just written to TMEM (A, at
@@ -146,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::kBarEmpty + s), 1);
     }
     mbar_init(BAR(C::kBarQ), 1);
-    mbar_init(BAR(C::kBarS), 1);
+    mbar_init(BAR(C::kBarS + 0), 1);
+    mbar_init(BAR(C::kBarS + 1), 1);
     for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 128);
     mbar_init(BAR(C::kBarDone), 1);
     fence_barrier_init();
@@ -219,48 +221,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout));
     if (ok) {
       tc_fence_after();
-      uint32_t pph = 0;
-      int done = 0;
-      int it = 0;
-      int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
-      for (int n = 0; n < n_ent; ++n) {
-        const int4 e = e_next;
-        if (n + 1 < n_ent) e_next = ents[n + 1];
-        if (!(e.y & active_bit)) continue;
-        const int kit = it, vit = it + 1;
-        it += 2;
-        const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1,
-                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
-        tc_fence_after();
-        if (elect_one()) issue_kmajor<D>(tmem + C::kColS, q_desc, kv_kdesc + ks * kSlot16);
-        __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + vs), (vit / C::kStages) & 1,
-                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
-        tc_fence_after();
+      // Key tiles in halves of 64 keys, ping-pong: S and dP of the next tile's half 0 are
+      // issued as soon as this tile's half 0 has been handed back (dS in TMEM and its dQ
+      // products issued), while the other warpgroup still works on half 1.
+      auto next_active = [&](int x) {
+        while (x < n_ent && !(ents[x].y & active_bit)) ++x;
+        return x;
+      };
+      auto wait_kv = [&](int it) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + it % C::kStages),
+                                                 (it / C::kStages) & 1, p.budget, p.err,
+                                                 kErrTimeout)) &&
+               __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + (it + 1) % C::kStages),
+                                                 ((it + 1) / C::kStages) & 1, p.budget, p.err,
+                                                 kErrTimeout));
+      };
+      auto issue_sdp = [&](int it, int h) {  // S and dP of key half h of the tile at `it`
+        const uint32_t ks = it % C::kStages, vs = (it + 1) % C::kStages;
         if (elect_one()) {
-          issue_kmajor<D>(tmem + C::kColDP, do_desc, kv_kdesc + vs * kSlot16);
-          mma_commit(BAR(C::kBarS));
-          mma_commit(BAR(C::kBarEmpty + vs));  // V is no longer needed
+          issue_half<D>(tmem + 128 * h, q_desc, kv_kdesc + ks * kSlot16 + h * kHalfRows16);
+          issue_half<D>(tmem + 128 * h + 64, do_desc, kv_kdesc + vs * kSlot16 + h * kHalfRows16);
+          mma_commit(BAR(C::kBarS + h));
+          if (h == 1) mma_commit(BAR(C::kBarEmpty + vs));  // V is no longer needed
         }
         __syncwarp();
-        // dQ += dS K, 32 keys at a time as the elementwise warps hand over each chunk
-        for (int q = 0; q < 4 && ok; ++q) {
-          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), pph, p.budget, p.err, kErrTimeout))) {
-            ok = false;
-            break;
-          }
+      };
+      int it = 0, done = 0;
+      int n = next_active(0);
+      if (n < n_ent) {
+        if (!wait_kv(0)) ok = false;
+        if (ok) {
           tc_fence_after();
-          if (elect_one())
-            issue_acc_chunk<D>(tmem + C::kColDQ, tmem + C::kColS + chunk_col(q), kv_mndesc + ks * kSlot16,
-                               q, done > 0);
-          __syncwarp();
+          issue_sdp(0, 0);
+          issue_sdp(0, 1);
         }
-        if (!ok) break;
-        pph ^= 1u;
-        if (elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
-        __syncwarp();
+      }
+      while (ok && n < n_ent) {
+        const int n1 = next_active(n + 1);
+        const uint32_t ks = it % C::kStages;
+        const uint32_t par = done & 1;
+        for (int h = 0; h < 2 && ok; ++h) {
+          // dQ += dS K over this half's keys, 32 at a time as the chunks arrive
+          for (int c = 0; c < 2; ++c) {
+            const int q = 2 * h + c;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), par, p.budget, p.err,
+                                                   kErrTimeout))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one())
+              issue_acc_chunk<D>(tmem + C::kColDQ, tmem + 128 * h + 16 * c,
+                                 kv_mndesc + ks * kSlot16, q, done > 0);
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (h == 1 && elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
+          __syncwarp();
+          if (n1 < n_ent) {
+            if (h == 0 && !wait_kv(it + 2)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sdp(it + 2, h);
+          }
+        }
+        it += 2;
         ++done;
+        n = n1;
       }
     }
     if (elect_one()) mma_commit(BAR(C::kBarDone));
@@ -299,18 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row's mask words, computed before the wait so their loads overlap the products
       uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (!(e.y & full_bit)) row_mask(make_predicate(m, p.colmask, e, i), w);
-      const bool got = mbar_wait(BAR(C::kBarS), sph, p.budget, p.err, kErrTimeout);
+      const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
       tc_fence_after();
       if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
       // dS = scale P (dP - D) with P = 2^(s scale log2 e - LSE log2 e), 32 columns at a
-      // time; the bf16 result of chunk q lands in columns 16q .. 16q+15, all of which
-      // the chunks up to q have already read
+      // time; the bf16 result of chunk qq lands over this half's S, already loaded
       {
         const int h = wg;
-        uint32_t sv64[64], dv64[64];  // S and dP of columns 64h .. 64h+63, one wait
-        tmem_ld64x2(lane_base + C::kColS + 64 * h, sv64, lane_base + C::kColDP + 64 * h, dv64);
+        uint32_t sv64[64], dv64[64];  // S and dP of key half h (columns 64h .. 64h+63)
+        tmem_ld64x2(lane_base + 128 * h, sv64, lane_base + 128 * h + 64, dv64);
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * h + qq;
@@ -335,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           f32x2_split(mul_f32x2(f32x2(p0, p1), t2), g0, g1);
           pk[b] = pack_bf16x2(g0, g1);
         }
-        tmem_st16(lane_base + C::kColS + chunk_col(q), pk);
+        tmem_st16(lane_base + 128 * h + 16 * qq, pk);  // over this half's own S
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
@@ -403,7 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // holds it), all later rows for a strided or global column, the query blocks that
 // list the key's block as random (transposed lists), a range of packed columns, or
 // the suffix of gathered global rows at or after the key.
-// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d).
+// TMEM: per query half h (64 queries), S^T at 128h and dP^T at 128h + 64; dV at 256,
+// dK at 256 + d.  The two halves ping-pong: the next tile's half-0 products start as soon
+// as this tile's half 0 has been handed back, while warpgroup 1 works on half 1.
 
 template <int D>
 struct KvCfg {
@@ -413,15 +443,17 @@ struct KvCfg {
   static constexpr int kStages = D == 128 ? 2 : 4;  // one stage = the Q and dO tiles
   static constexpr int kSmemKV = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * 2 * kTileBytes;
-  static constexpr int kSmemVec = 2 * 2 * kTile * 4;  // LSE and D, double-buffered
+  // LSE and D of each warpgroup's 64 query columns, double-buffered: [wg][buf][2][64]
+  static constexpr int kSmemVec = 2 * 2 * 2 * 64 * 4;
   // kBarP + q: chunk q (queries 32q .. 32q+31) of P^T and dS^T is in TMEM
   static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages,
-                       kBarS = 1 + 2 * kStages, kBarP = 2 + 2 * kStages,
-                       kBarDone = 6 + 2 * kStages, kBarVec = 7 + 2 * kStages,
-                       kNumBars = 9 + 2 * kStages;
+                       kBarS = 1 + 2 * kStages, kBarP = 3 + 2 * kStages,
+                       kBarDone = 7 + 2 * kStages, kBarVec = 8 + 2 * kStages,
+                       kNumBars = 12 + 2 * kStages;  // kBarVec + 2 wg + buf
   static constexpr int kSmemBytes = kSmemKV + kSmemRing + kSmemVec + kNumBars * 8 + 16 + 1024;
-  // products use the dQ kernel's issue helpers (same shapes: 128 x 128 and 128 x d)
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // products use the dQ kernel's issue helpers (same shapes: 128 x 64 and 128 x d).
+  // TMEM: query half h has S^T at 128h and dP^T at 128h + 64; dV, dK after them
+  static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 };
 
 struct KvParams {
@@ -532,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = smem_addr(smem);
   const uint32_t sV = sK + C::kTileBytes;
   const uint32_t sRing = sK + C::kSmemKV;  // stage s: Q at +0, dO at +kTileBytes
-  float* s_vec = reinterpret_cast<float*>(smem + C::kSmemKV + C::kSmemRing);  // [2][LSE, D][128]
+  float* s_vec = reinterpret_cast<float*>(smem + C::kSmemKV + C::kSmemRing);  // [wg][buf][LSE, D][64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemKV + C::kSmemRing + C::kSmemVec);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   const uint32_t bar0 = smem_addr(bars);
@@ -552,11 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::kBarFull + s), 1);
       mbar_init(BAR(C::kBarEmpty + s), 1);
     }
-    mbar_init(BAR(C::kBarS), 1);
+    mbar_init(BAR(C::kBarS + 0), 1);
+    mbar_init(BAR(C::kBarS + 1), 1);
     for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 128);
     mbar_init(BAR(C::kBarDone), 1);
-    mbar_init(BAR(C::kBarVec + 0), 256);
-    mbar_init(BAR(C::kBarVec + 1), 256);
+    for (int k = 0; k < 4; ++k) mbar_init(BAR(C::kBarVec + k), 128);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -622,37 +654,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarKV), 0, p.budget, p.err, kErrTimeout));
     if (ok) {
       tc_fence_after();
-      uint32_t pph = 0;
-      for (int n = 0; n < n_ent; ++n) {
+      // Query tiles in halves of 64 queries, ping-pong (as in the dQ kernel): the next
+      // tile's half-0 products go out as soon as this tile's half 0 has been handed back.
+      auto wait_q = [&](int n) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + n % C::kStages),
+                                                 (n / C::kStages) & 1, p.budget, p.err,
+                                                 kErrTimeout));
+      };
+      auto issue_sdp = [&](int n, int h) {  // S^T and dP^T of query half h of tile n
         const uint32_t s = n % C::kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + s), (n / C::kStages) & 1,
-                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
-        tc_fence_after();
         if (elect_one()) {
-          issue_kmajor<D>(tmem + C::kColS, k_desc, ring_k + s * kStage16);
-          issue_kmajor<D>(tmem + C::kColDP, v_desc, ring_k + s * kStage16 + kDo16);
-          mma_commit(BAR(C::kBarS));
+          issue_half<D>(tmem + 128 * h, k_desc, ring_k + s * kStage16 + h * kHalfRows16);
+          issue_half<D>(tmem + 128 * h + 64, v_desc, ring_k + s * kStage16 + kDo16 + h * kHalfRows16);
+          mma_commit(BAR(C::kBarS + h));
         }
         __syncwarp();
-        // dV += P^T dO and dK += dS^T Q, 32 queries at a time as each chunk arrives
-        for (int q = 0; q < 4 && ok; ++q) {
-          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), pph, p.budget, p.err, kErrTimeout))) {
-            ok = false;
-            break;
-          }
+      };
+      if (n_ent > 0) {
+        if (!wait_q(0)) ok = false;
+        if (ok) {
           tc_fence_after();
-          if (elect_one()) {
-            issue_acc_chunk<D>(tmem + C::kColDV, tmem + C::kColS + chunk_col(q),
-                               ring_mn + s * kStage16 + kDo16, q, n > 0);
-            issue_acc_chunk<D>(tmem + C::kColDK, tmem + C::kColDP + chunk_col(q),
-                               ring_mn + s * kStage16, q, n > 0);
-          }
-          __syncwarp();
+          issue_sdp(0, 0);
+          issue_sdp(0, 1);
         }
-        if (!ok) break;
-        pph ^= 1u;
-        if (elect_one()) mma_commit(BAR(C::kBarEmpty + s));
-        __syncwarp();
+      }
+      for (int n = 0; ok && n < n_ent; ++n) {
+        const uint32_t s = n % C::kStages;
+        const uint32_t par = n & 1;
+        for (int h = 0; h < 2 && ok; ++h) {
+          // dV += P^T dO and dK += dS^T Q over this half's queries, chunk by chunk
+          for (int c = 0; c < 2; ++c) {
+            const int q = 2 * h + c;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), par, p.budget, p.err,
+                                                   kErrTimeout))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              issue_acc_chunk<D>(tmem + C::kColDV, tmem + 128 * h + 16 * c,
+                                 ring_mn + s * kStage16 + kDo16, q, n > 0);
+              issue_acc_chunk<D>(tmem + C::kColDK, tmem + 128 * h + 64 + 16 * c,
+                                 ring_mn + s * kStage16, q, n > 0);
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (h == 1 && elect_one()) mma_commit(BAR(C::kBarEmpty + s));
+          __syncwarp();
+          if (n + 1 < n_ent) {
+            if (h == 0 && !wait_q(n + 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sdp(n + 1, h);
+          }
+        }
       }
     }
     if (elect_one()) mma_commit(BAR(C::kBarDone));
@@ -672,11 +730,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t head = static_cast<size_t>(bh) * m.T;
     uint32_t sph = 0;
     int n_done = 0;
-    // this thread's query column of an entry (warpgroup 0 loads them): LSE and D, one
-    // entry ahead so the global loads overlap the previous tile's work
+    // LSE and D of query column 64 wg + kk of an entry (threads kk < 64 of each
+    // warpgroup load their half's columns), one entry ahead so the global loads overlap
+    // the previous tile's work
     auto column_values = [&](const int4& e, float& lse_v, float& dd_v) {
       int i = -1;
-      const int a = e.x + kk;
+      const int a = e.x + 64 * wg + kk;
       if (e.y & kEntryGathered) {
         if (a < m.n_global) i = m.gpos[a];
       } else if (a < m.T && !m.rowglobal[a]) {
@@ -687,37 +746,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     float lse_next = 0.f, dd_next = 0.f;
-    if (n_ent && wg == 0) column_values(e_next, lse_next, dd_next);
+    if (n_ent && kk < 64) column_values(e_next, lse_next, dd_next);
     for (int n = 0; n < n_ent; ++n) {
       const int4 e = e_next;
       const float lse_cur = lse_next, dd_cur = dd_next;
       if (n + 1 < n_ent) e_next = ents[n + 1];
       const int kind = (e.y >> kKindShift) & 3;
-      // this tile's per-query LSE and D, one column per thread, double-buffered: buffer
-      // n & 1 is rewritten at tile n + 2, after every thread has passed tile n + 1's
-      // barrier (and so has finished tile n)
-      float* s_lse = s_vec + (n & 1) * 2 * kTile;
-      float* s_dd = s_lse + kTile;
-      if (wg == 0) {
+      // this warpgroup's 64 query columns' LSE and D, double-buffered per warpgroup:
+      // buffer n & 1 is rewritten at tile n + 2, after all 128 threads of the warpgroup
+      // have passed tile n + 1's barrier (and so have finished tile n); the two
+      // warpgroups never wait for each other
+      float* s_lse = s_vec + (wg * 2 + (n & 1)) * 2 * 64;
+      float* s_dd = s_lse + 64;
+      if (kk < 64) {
         s_lse[kk] = lse_cur;
         s_dd[kk] = dd_cur;
       }
-      mbar_arrive(BAR(C::kBarVec + (n & 1)));
-      if (wg == 0 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next);
-      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + (n & 1)), (n >> 1) & 1, p.budget,
-                                             p.err, kErrTimeout)))
+      mbar_arrive(BAR(C::kBarVec + wg * 2 + (n & 1)));
+      if (kk < 64 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next);
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + wg * 2 + (n & 1)), (n >> 1) & 1,
+                                             p.budget, p.err, kErrTimeout)))
         break;
       uint32_t w[4];
       key_mask(p, kind, e, e.x, j, key, w);
       if (!key_valid) w[0] = w[1] = w[2] = w[3] = 0u;
-      const bool got = mbar_wait(BAR(C::kBarS), sph, p.budget, p.err, kErrTimeout);
+      const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
       tc_fence_after();
       {
         const int hh = wg;
-        uint32_t sv64[64], dv64[64];  // S^T and dP^T of columns 64hh .. 64hh+63, one wait
-        tmem_ld64x2(lane_base + C::kColS + 64 * hh, sv64, lane_base + C::kColDP + 64 * hh, dv64);
+        uint32_t sv64[64], dv64[64];  // S^T and dP^T of query half hh (columns 64hh ..)
+        tmem_ld64x2(lane_base + 128 * hh, sv64, lane_base + 128 * hh + 64, dv64);
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * hh + qq;
@@ -727,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool all = w[q] == 0xffffffffu;
 #pragma unroll
         for (int b = 0; b < 16; b += 2) {  // four columns per step: one vector load each
-          const int c0 = 32 * q + 2 * b;
+          const int c0 = 32 * qq + 2 * b;  // column within this warpgroup's 64
           const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c0);
           const float4 d4 = *reinterpret_cast<const float4*>(s_dd + c0);
 #pragma unroll
@@ -751,8 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pg[b + h] = pack_bf16x2(g0, g1);
           }
         }
-        tmem_st16(lane_base + C::kColS + chunk_col(q), pp);
-        tmem_st16(lane_base + C::kColDP + chunk_col(q), pg);
+        tmem_st16(lane_base + 128 * hh + 16 * qq, pp);       // over this half's own S^T
+        tmem_st16(lane_base + 128 * hh + 64 + 16 * qq, pg);  // over this half's own dP^T
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(BAR(C::kBarP + q));  // queries 32q .. 32q+31 of P^T and dS^T are in TMEM
