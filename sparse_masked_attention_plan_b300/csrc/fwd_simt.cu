@@ -109,9 +109,6 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(const SParams p) {
     const float* Ks = packed ? p.Kc : p.K;
     const float* Vs = packed ? p.Vc : p.V;
     const long long src_rows = packed ? p.n_cols : T;
-    RowPredicate pr[kRowsPerWarp];
-#pragma unroll
-    for (int k = 0; k < kRowsPerWarp; ++k) pr[k] = make_predicate(m, p.colmask, e, rows_i[k]);
 
     for (int sb = 0; sb < kTile / kSub; ++sb) {
       __syncthreads();
@@ -136,7 +133,8 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(const SParams p) {
         float dot = 0.f;
 #pragma unroll 16
         for (int c = 0; c < D; ++c) dot = fmaf(q[c], kr[c], dot);
-        const bool ok = full || pred_allowed(pr[k], cidx);
+        // the row's predicate, rebuilt here rather than held for all rows (registers)
+        const bool ok = full || pred_allowed(make_predicate(m, p.colmask, e, rows_i[k]), cidx);
         const float s = ok ? dot * p.scale : -INFINITY;
         float mx = s;
 #pragma unroll
