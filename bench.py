@@ -39,12 +39,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the tensor-core forward kernel on the
 # 32K / W=4096 workload, from the ncu capture summarised in
-# profiles/fwd_tc_t32k_w4096.md (captured with H=8, 251.0 MB, scaled by 32/8 heads),
+# the forward kernel's profile summary (captured with H=8, 249.6 MB, scaled by 32/8 heads),
 # valid only for the kernel source with this hash; any other source reports null.
-TRAFFIC = {"kernel_sha": "7e831f82a2f9cc44", "bytes_per_launch": 999.4e6, "workload": "t32k_w4096"}
-# The same for the backward's dominant kernel (bwd_dkdv_tc, profiles/bwd_tc_t32k_w4096.md,
-# H=4 capture x 8) and the decode kernel (profiles/decode_b8_w4096.md, B=8 capture, x 4
-# for B=32), keyed by their source hashes.
+TRAFFIC = {"kernel_sha": "9618899bf5ccef92", "bytes_per_launch": 998.6e6, "workload": "t32k_w4096"}
+# The same for the backward's dominant kernel (bwd_dkdv_tc, H=4 capture x 8) and the
+# decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
 BWD_TRAFFIC = {"kernel_sha": "a167f46651193842", "bytes_per_launch": 1358.1e6,
                "workload": "t32k_w4096", "file": "bwd_tc.cu"}
 DEC_TRAFFIC = {"kernel_sha": "1500b47262601fb8", "file": "decode.cu",
