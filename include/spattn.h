@@ -217,10 +217,13 @@ spattn_status spattn_fwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_d
  *   dQ_i = scale sum_j ds_ij k_j,  dK_j = scale sum_i ds_ij q_i,  dV_j = sum_i alpha_ij dO_i.
  * Q, K, V, O, dO, dQ, dK, dV: [B, H, T, d] of `dtype`, contiguous, 16-byte aligned;
  * LSE: [B, H, T] fp32 (required).  dQ, dK, dV are overwritten (every row is
- * written; nothing needs zeroing).  All products and sums run in fp32 on FP32 FMA
- * units with no atomics, so the result is the same on every call; bf16 outputs
- * are rounded once, to nearest even.  The first call for a given B*H may allocate
- * the plan's backward scratch (row dots and packed-column partial sums).
+ * written; nothing needs zeroing).  bf16 runs on the tcgen05 tensor cores (bf16
+ * products, fp32 accumulation; P and dS rounded to bf16 as product operands), fp32
+ * on FP32 FMA units; neither uses atomics (every row's dQ and every key's dK, dV is
+ * summed inside one CTA), so the result is the same on every call.  Outputs of bf16
+ * calls are rounded once, to nearest even.  The first call for a given B*H may
+ * allocate the plan's backward scratch (row dots, packed-column partial sums and,
+ * for bf16, packed copies of the sparse-column K, V and global-row Q, dO).
  * Errors: NULL, SHAPE, DTYPE, ALIGN, INVALID_SPEC (scale), CUDA.
  */
 spattn_status spattn_bwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_dtype dtype,

@@ -1,4 +1,6 @@
-// bwd_simt.cu -- gradients of block-sparse masked attention on the FP32 FMA units.
+// bwd_simt.cu -- gradients of block-sparse masked attention on the FP32 FMA units
+// (fp32 inputs; bf16 inputs use this file's row-dot kernel and the tensor-core
+// kernels of bwd_tc.cu).
 //
 // For y_i = sum_{j in S_i} alpha_ij v_j with alpha_ij = softmax over S_i of
 // s_ij = scale q_i . k_j ("Sparse attention" glossary, section "Choose the
