@@ -75,7 +75,9 @@ struct DqParams {
   const int4* entries;
   int* err;
   uint64_t budget;
-  int BH;
+  int BH;     // work units along the head axis: (batch, head) x residue classes
+  int dview;  // residue classes of a dilated view (1: rows are the sequence itself)
+  int T_out;  // sequence length (the mask's T times dview)
 };
 
 // A (128 rows) x B^T (64 rows, one half of a 128-row tile), both K-major over d: the
@@ -130,7 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA = (work item, query tile t, (batch, head)); heads vary fastest so neighbouring
   // CTAs of one item share nothing but the items of one head share K/V tiles in L2
-  const int bh = blockIdx.x % p.BH;
+  // a unit along the head axis is a (batch, head) and, in a dilated view, a residue
+  // class r: its row q is sequence position q * dview + r
+  const int res = (blockIdx.x % p.BH) % p.dview, bh = (blockIdx.x % p.BH) / p.dview;
   const int rank = (blockIdx.x / p.BH) >> 1;
   const int t = (blockIdx.x / p.BH) & 1;
   const int4 item = p.items[rank];
@@ -170,8 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(BAR(C::kBarQ), 2 * C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(sQ + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64, 0, qrow0, bh);
-        tma_load_4d(sdO + c * C::kChunkBytes, mapdO, BAR(C::kBarQ), c * 64, 0, qrow0, bh);
+        tma_load_4d(sQ + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64, gathered ? 0 : res, qrow0, bh);
+        tma_load_4d(sdO + c * C::kChunkBytes, mapdO, BAR(C::kBarQ), c * 64, gathered ? 0 : res, qrow0,
+                    bh);
       }
     }
     __syncwarp();
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
-                        c * 64, 0, e.x, bh);
+                        c * 64, packed ? 0 : res, e.x, bh);
         }
         __syncwarp();
         ++issued;
@@ -311,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       i = qrow0 + r;
       valid = i < m.T;
     }
-    const size_t row = static_cast<size_t>(bh) * m.T + static_cast<size_t>(i);
+    const size_t row = static_cast<size_t>(bh) * p.T_out +
+                       (gathered ? static_cast<size_t>(i) : static_cast<size_t>(i) * p.dview + res);
     const float lse2 = valid ? p.LSE[row] * 1.4426950408889634f : 0.f;
     const float dsc = p.scale;
     const float dterm = valid ? -p.Dvec[row] * dsc : 0.f;
@@ -477,7 +483,9 @@ struct KvParams {
   int n_cols;
   int* err;
   uint64_t budget;
-  int BH;
+  int BH;     // work units along the head axis: (batch, head) x residue classes
+  int dview;  // residue classes of a dilated view (1: rows are the sequence itself)
+  int T_out;  // sequence length (the mask's T times dview)
 };
 
 // Bits of [a, b] (tile columns) in the four 32-bit words.
@@ -571,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define BAR(k) (bar0 + 8u * static_cast<uint32_t>(k))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x % p.BH;
+  const int res = (blockIdx.x % p.BH) % p.dview, bh = (blockIdx.x % p.BH) / p.dview;
   const int4 unit = p.units[p.unit0 + blockIdx.x / p.BH];
   const bool packed_unit = (unit.w & kUnitPacked) != 0;
   const int n_ent = unit.z;
@@ -608,8 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(BAR(C::kBarKV), 2 * C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(sK + c * C::kChunkBytes, mk, BAR(C::kBarKV), c * 64, 0, unit.x, bh);
-        tma_load_4d(sV + c * C::kChunkBytes, mv, BAR(C::kBarKV), c * 64, 0, unit.x, bh);
+        tma_load_4d(sK + c * C::kChunkBytes, mk, BAR(C::kBarKV), c * 64, packed_unit ? 0 : res,
+                    unit.x, bh);
+        tma_load_4d(sV + c * C::kChunkBytes, mv, BAR(C::kBarKV), c * 64, packed_unit ? 0 : res,
+                    unit.x, bh);
       }
     }
     __syncwarp();
@@ -631,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(BAR(C::kBarFull + s), 2 * C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d(dst + c * C::kChunkBytes, mq, BAR(C::kBarFull + s), c * 64, 0, e.x, bh);
-          tma_load_4d(dst + C::kTileBytes + c * C::kChunkBytes, md, BAR(C::kBarFull + s), c * 64, 0,
+          const int r4 = gathered ? 0 : res;
+          tma_load_4d(dst + c * C::kChunkBytes, mq, BAR(C::kBarFull + s), c * 64, r4, e.x, bh);
+          tma_load_4d(dst + C::kTileBytes + c * C::kChunkBytes, md, BAR(C::kBarFull + s), c * 64, r4,
                       e.x, bh);
         }
       }
@@ -727,7 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = key_valid ? (packed_unit ? p.cols[key] : key) : 0;
     const float c2 = p.scale_log2, dsc = p.scale;
     const uint64_t c2x2 = f32x2(c2, c2), dsc2 = f32x2(dsc, dsc);
-    const size_t head = static_cast<size_t>(bh) * m.T;
+    const size_t head = static_cast<size_t>(bh) * p.T_out;
+    // sequence position of view row x (gathered global rows are positions already)
+    auto seq = [&](int x) { return static_cast<size_t>(x) * p.dview + res; };
     uint32_t sph = 0;
     int n_done = 0;
     // LSE and D of query column 64 wg + kk of an entry (threads kk < 64 of each
@@ -741,8 +754,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (a < m.T && !m.rowglobal[a]) {
         i = a;
       }
-      lse_v = i >= 0 ? p.LSE[head + i] * 1.4426950408889634f : INFINITY;
-      dd_v = i >= 0 ? p.Dvec[head + i] * dsc : 0.f;
+      const size_t at = head + ((e.y & kEntryGathered) ? static_cast<size_t>(i) : seq(i));
+      lse_v = i >= 0 ? p.LSE[at] * 1.4426950408889634f : INFINITY;
+      dd_v = i >= 0 ? p.Dvec[at] * dsc : 0.f;
     };
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     float lse_next = 0.f, dd_next = 0.f;
@@ -863,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             f[b + 3] += x.w;
           }
         }
-        uint4* dst = reinterpret_cast<uint4*>((half ? p.dK : p.dV) + (head + j) * D + 32 * q);
+        uint4* dst = reinterpret_cast<uint4*>((half ? p.dK : p.dV) + (head + seq(j)) * D + 32 * q);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 x;
@@ -895,10 +909,11 @@ cudaError_t launch_kv_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const long long T = a.mask.T;
+  const long long T = a.mask.T;  // rows per residue class
+  const long long dv = a.dview;
   CUtensorMap mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc;
-  bool ok = make_map(&mQ, a.Q, D, T, a.BH) && make_map(&mdO, a.dO, D, T, a.BH) &&
-            make_map(&mK, a.K, D, T, a.BH) && make_map(&mV, a.V, D, T, a.BH);
+  bool ok = make_map(&mQ, a.Q, D, T, a.BH, dv) && make_map(&mdO, a.dO, D, T, a.BH, dv) &&
+            make_map(&mK, a.K, D, T, a.BH, dv) && make_map(&mV, a.V, D, T, a.BH, dv);
   ok = ok && (a.n_cols > 0 ? make_map(&mKc, a.Kc, D, a.n_cols, a.BH) && make_map(&mVc, a.Vc, D, a.n_cols, a.BH)
                            : (mKc = mK, mVc = mV, true));
   ok = ok && (a.mask.n_global > 0 ? make_map(&mQg, a.Qg, D, a.mask.n_global, a.BH) &&
@@ -928,11 +943,13 @@ cudaError_t launch_kv_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
   kp.n_cols = a.n_cols;
   kp.err = a.err;
   kp.budget = a.wait_budget_cycles;
-  kp.BH = a.BH;
+  kp.BH = a.BH * static_cast<int>(dv);
+  kp.dview = static_cast<int>(dv);
+  kp.T_out = static_cast<int>(T * dv);
   // packed units first: their partial sums are added by the natural units
   const int parts[2][2] = {{0, a.n_packed_units}, {a.n_packed_units, a.n_units}};
   for (const auto& pr : parts) {
-    const long long ctas = static_cast<long long>(pr[1] - pr[0]) * a.BH;
+    const long long ctas = static_cast<long long>(pr[1] - pr[0]) * a.BH * dv;
     if (ctas <= 0) continue;
     if (ctas > 0x7fffffffLL) {
       *why = "too many key units";
@@ -957,10 +974,11 @@ cudaError_t launch_dq_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
                                     C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const long long T = a.mask.T;
+  const long long T = a.mask.T;  // rows per residue class
+  const long long dv = a.dview;
   CUtensorMap mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc;
-  bool ok = make_map(&mQ, a.Q, D, T, a.BH) && make_map(&mdO, a.dO, D, T, a.BH) &&
-            make_map(&mK, a.K, D, T, a.BH) && make_map(&mV, a.V, D, T, a.BH);
+  bool ok = make_map(&mQ, a.Q, D, T, a.BH, dv) && make_map(&mdO, a.dO, D, T, a.BH, dv) &&
+            make_map(&mK, a.K, D, T, a.BH, dv) && make_map(&mV, a.V, D, T, a.BH, dv);
   ok = ok && (a.n_cols > 0 ? make_map(&mKc, a.Kc, D, a.n_cols, a.BH) && make_map(&mVc, a.Vc, D, a.n_cols, a.BH)
                            : (mKc = mK, mVc = mV, true));
   ok = ok && (a.mask.n_global > 0 ? make_map(&mQg, a.Qg, D, a.mask.n_global, a.BH) &&
@@ -982,8 +1000,10 @@ cudaError_t launch_dq_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
   kp.entries = a.entries;
   kp.err = a.err;
   kp.budget = a.wait_budget_cycles;
-  kp.BH = a.BH;
-  const long long ctas = static_cast<long long>(a.n_items) * 2 * a.BH;
+  kp.BH = a.BH * static_cast<int>(dv);
+  kp.dview = static_cast<int>(dv);
+  kp.T_out = static_cast<int>(T * dv);
+  const long long ctas = static_cast<long long>(a.n_items) * 2 * a.BH * dv;
   if (ctas > 0x7fffffffLL) {
     *why = "too many work items";
     return cudaErrorInvalidValue;

@@ -104,6 +104,7 @@ struct spattn_plan {
   // (-1 where the key is not a sparse column)
   spattn::Schedule bsched;     // 64-key units, 64-row groups (FP32-unit kernels)
   spattn::Schedule bsched_tc;  // 128-key units, 128-row groups (tensor-core kernel)
+  spattn::Schedule bsched_res;  // the same over the residue classes of a dilated view
   int32_t* d_colidx = nullptr;
   // random blocks transposed (key block -> query blocks), for the key-major kernels
   std::vector<int32_t> rt_off, rt_qb;
@@ -278,6 +279,7 @@ struct BwdTcArgs {
   const int4* u_entries;
   int32_t n_packed_units;
   int32_t n_units;
+  int32_t dview = 1;  // residue classes of a dilated view (mask.T is then T / dview)
 };
 cudaError_t launch_bwd_dq_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why);
 cudaError_t launch_bwd_dkdv_tc(int d, const BwdTcArgs& a, cudaStream_t st, const char** why);

@@ -51,7 +51,7 @@ void free_plan_memory(spattn_plan* p) {
                   p->sched[2].d_entries, p->d_colmask_res, p->d_rowzero,
                   p->bsched.d_items, p->bsched.d_entries, p->d_colidx, p->d_bscratch,
                   p->d_roff, p->d_rkb, p->bsched_tc.d_items, p->bsched_tc.d_entries,
-                  p->d_rtoff, p->d_rtqb};
+                  p->d_rtoff, p->d_rtqb, p->bsched_res.d_items, p->bsched_res.d_entries};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -607,6 +607,7 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
     v.radius = p->radius;
     v.dilation = 1;
     build_schedule(&v, &p->sched[2], 2 * kTile, kTile, 2, true);
+    build_bwd_schedule(&v, &p->bsched_res, kTile, kTile);
     p->dview = static_cast<int32_t>(p->dilation);
     const int64_t nkb_res = (v.T + kTile - 1) / kTile;
     cudaError_t e = dev_alloc(&p->d_colmask_res, size_t(nkb_res) * 4);
@@ -643,6 +644,7 @@ spattn_status spattn_plan_create(const spattn_mask_spec* spec, int64_t T, int32_
   {
     spattn_status us = upload_schedule(&p->bsched);
     if (us == SPATTN_OK) us = upload_schedule(&p->bsched_tc);
+    if (us == SPATTN_OK) us = upload_schedule(&p->bsched_res);
     if (us != SPATTN_OK) return bail(us);
     std::vector<int32_t> colidx(size_t(T), -1);
     for (int32_t c = 0; c < p->n_cols; ++c) colidx[p->cols[c]] = c;
@@ -914,6 +916,19 @@ spattn_status spattn_bwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
     t.u_entries = p->bsched_tc.d_entries;
     t.n_packed_units = p->bsched_tc.n_packed_units;
     t.n_units = static_cast<int32_t>(p->bsched_tc.items.size() / 4);
+    if (p->dview > 1) {  // a dilated window on its residue classes, as the forward walks it
+      t.mask = p->mask_dev_res();
+      t.colmask = p->d_colmask_res;
+      t.n_cols = 0;
+      t.items = p->sched[2].d_items;
+      t.entries = p->sched[2].d_entries;
+      t.n_items = static_cast<int32_t>(p->sched[2].items.size() / 4);
+      t.units = p->bsched_res.d_items;
+      t.u_entries = p->bsched_res.d_entries;
+      t.n_packed_units = 0;
+      t.n_units = static_cast<int32_t>(p->bsched_res.items.size() / 4);
+      t.dview = p->dview;
+    }
     const char* why = "";
     e = spattn::launch_bwd_dq_tc(p->d, t, stream, &why);
     if (e != cudaSuccess)
