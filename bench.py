@@ -1,6 +1,12 @@
 """Benchmark: allowed-pair TFLOP/s of the block-sparse masked attention forward pass.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--pass fwd|bwd|decode] [--decode-workload NAME]
+
+--pass fwd (default) is the headline described below.  --pass bwd times one spattn_bwd
+over the whole batch (10 d pairs flops per step, against the bf16 peak); --pass decode
+times one generation step (ring-buffer append + decode) and reports GB/s of cached K/V
+read per step against the measured HBM bandwidth.
 
 One step = one spattn_fwd call over the whole batch (every (batch, head)) of the
 workload, inputs already resident in HBM.  value = 4 d B H pairs_per_head / t_step
