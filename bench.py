@@ -6,7 +6,8 @@
 --pass fwd (default) is the headline described below.  --pass bwd times one spattn_bwd
 over the whole batch (10 d pairs flops per step, against the bf16 peak); --pass decode
 times one generation step (ring-buffer append + decode) and reports GB/s of cached K/V
-read per step against the measured HBM bandwidth.
+read per step against the measured HBM bandwidth; its timed steps are captured once into a
+CUDA graph and replayed (each step still appends, decodes at its own position and merges).
 
 One step = one spattn_fwd call over the whole batch (every (batch, head)) of the
 workload, inputs already resident in HBM.  value = 4 d B H pairs_per_head / t_step
@@ -52,8 +53,8 @@ TRAFFIC = {"kernel_sha": "9618899bf5ccef92", "bytes_per_launch": 998.6e6, "workl
 # decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
 BWD_TRAFFIC = {"kernel_sha": "988fd762c2c34052", "bytes_per_launch": 1348.9e6,
                "workload": "t32k_w4096", "file": "bwd_tc.cu"}
-DEC_TRAFFIC = {"kernel_sha": "1500b47262601fb8", "file": "decode.cu",
-               "bytes_per_launch": {"decode_b8_w4096": 138.1e6, "decode_b32_w4096": 552.6e6}}
+DEC_TRAFFIC = {"kernel_sha": "0bdc470aa24527e5", "file": "decode.cu",
+               "bytes_per_launch": {"decode_b8_w4096": 140.9e6, "decode_b32_w4096": 563.4e6}}
 
 
 def kernel_sha(name: str = "fwd_tc.cu") -> str:
@@ -509,19 +510,25 @@ def run_decode(args):
         step(s)
     stream.synchronize()
     c.check(stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # The timed steps run as one captured CUDA graph, the way a generation loop
+    # launches its steps: every step still appends its rows, decodes at its own
+    # position and merges the splits (three kernels), with no host work in between.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for s in range(args.steps):
+            step(args.warmup + s)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
         ev[0].record(stream)
-        for s in range(args.steps):
-            step(args.warmup + s)
-            ev[s + 1].record(stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        ev[1].record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
     c.check(stream)
-    per = [ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps)]
-    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world) / args.steps
+    ms = max_over_ranks(ev[0].elapsed_time(ev[1]), world) / args.steps
     value = world * step_bytes / (ms / 1e3) / 1e9
 
     # end to end: this step's q, k, v from pinned host memory, append + decode, the
@@ -543,7 +550,7 @@ def run_decode(args):
     e2e = world * step_bytes * e2e_steps / e2e_s / 1e9
     if rank == 0:
         peaks, src = load_peaks()
-        step_ms = statistics.mean(per)
+        step_ms = ev[0].elapsed_time(ev[1]) / args.steps
         achieved = step_bytes / (step_ms / 1e3) / 1e9
         line = {
             "metric": DECODE_METRIC, "pass": "decode", "value": value, "unit": "GB/s",
@@ -552,6 +559,7 @@ def run_decode(args):
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.decode_workload, **cfg,
                        "tokens_per_step": B,
+                       "launch": "timed steps replayed from one captured CUDA graph",
                        "l2": f"cache larger than L2 ({kv_bytes / 1e6:.0f} MB of K/V)"},
             "tokens_per_s": world * B / (ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
