@@ -1,0 +1,84 @@
+"""The benchmark's output on a B300: each pass prints exactly one JSON line that carries
+every key of its contract, with numbers that agree with one another (throughput against
+the step time and the work, the roofline fraction against its parts, end-to-end bytes
+counted from the copied tensors)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+pytestmark = pytest.mark.gpu
+
+KEYS = ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+        "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
+        "e2e", "gpu_launches", "clocks"]
+ROOFLINE = ["bound", "achieved", "peak", "unit", "frac", "traffic"]
+
+
+def _run(*args):
+    out = subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True,
+                         text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout[-3000:]
+    return json.loads(lines[0])
+
+
+def _check_common(line, steps):
+    for k in KEYS:
+        assert k in line, k
+    roof = line["roofline"]
+    for k in ROOFLINE:
+        assert k in roof, k
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    assert line["n_gpus"] == 1 and line["steps"] == steps and line["warmup"] >= 3
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["gpu_launches"] >= steps
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert "workload" in line["config"]
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    clk = line["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+
+
+def test_forward_line():
+    line = _run("--workload", "t2048_w256_s64", "--steps", "4", "--warmup", "3",
+                "--cpu-budget", "2")
+    _check_common(line, 4)
+    c = line["config"]
+    flops = 4.0 * c["d"] * c["B"] * c["H"] * c["pairs_per_head"]
+    assert line["value"] == pytest.approx(flops / (line["ms_per_step"] / 1e3) / 1e12, rel=1e-6)
+    assert line["roofline"]["bound"] == "tensor"
+    # inputs in, output and LSE out: bf16 q, k, v and O, fp32 LSE
+    elems = c["B"] * c["H"] * c["T"] * c["d"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 3 * 2 * elems
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["cores"] >= 1 and cpu["sample"]
+
+
+def test_backward_line():
+    line = _run("--pass", "bwd", "--workload", "t2048_w256_s64", "--steps", "4", "--warmup", "3")
+    _check_common(line, 4)
+    c = line["config"]
+    flops = 10.0 * c["d"] * c["B"] * c["H"] * c["pairs_per_head"]
+    assert line["value"] == pytest.approx(flops / (line["ms_per_step"] / 1e3) / 1e12, rel=1e-6)
+    elems = c["B"] * c["H"] * c["T"] * c["d"]
+    # q, k, v, O, dO (bf16) and LSE (fp32) in; dQ, dK, dV out
+    assert line["e2e"]["h2d_bytes_per_step"] == 5 * 2 * elems + 4 * c["B"] * c["H"] * c["T"]
+    assert line["e2e"]["d2h_bytes_per_step"] == 3 * 2 * elems
+
+
+def test_decode_line():
+    line = _run("--pass", "decode", "--decode-workload", "decode_b8_w4096", "--steps", "5",
+                "--warmup", "3")
+    _check_common(line, 5)
+    c = line["config"]
+    assert line["roofline"]["bound"] == "hbm" and line["unit"] == "GB/s"
+    kv = c["B"] * c["Hkv"] * c["window"] * c["d"] * 2 * 2
+    assert line["value"] * line["ms_per_step"] / 1e3 * 1e9 >= kv  # at least the cache is counted
+    assert line["gpu_launches"] == 3 * 5
