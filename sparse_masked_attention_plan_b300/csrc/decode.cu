@@ -12,11 +12,13 @@
 // The step is HBM-bound: every cached key and value row is read once per step and
 // used by the G query heads of its group.  The slot range [0, cap) of each (batch,
 // key/value head) is split across CTAs; a CTA streams 64-slot sub-chunks of K and V
-// into shared memory with bulk asynchronous copies (a ring of stages, an mbarrier per
-// stage), runs an online softmax over them for the G query heads, and leaves (max,
-// sum, unnormalised output) per head; a second kernel merges the splits.  The valid
-// slots of a step are one circular interval of slot space (up to two linear ones), so
-// a CTA copies only valid rows and needs no per-element mask.
+// into shared memory through a ring of stages with an mbarrier per stage (TMA boxes
+// for bf16, bulk copies of the valid rows for fp32), runs an online softmax over them
+// for the G query heads, and leaves (max, sum, unnormalised output) per head; a second
+// kernel merges the splits.  The valid slots of a step are one circular interval of
+// slot space (up to two linear ones), so a sub-chunk is a run of consecutive slots and
+// only its ragged end needs a mask.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -24,9 +26,11 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace spattn {
 namespace {
@@ -62,21 +66,10 @@ __device__ __forceinline__ void unpack(const uint4& v, uint64_t* out, const floa
   out[0] = (static_cast<uint64_t>(v.y) << 32) | v.x;
   out[1] = (static_cast<uint64_t>(v.w) << 32) | v.z;
 }
-__device__ __forceinline__ void unpack(const uint4& v, uint64_t* out, const __nv_bfloat16*) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k)  // bf16 -> fp32 is a 16-bit shift of the bit pattern
-    out[k] = (static_cast<uint64_t>(w[k] & 0xffff0000u) << 32) | (w[k] << 16);
-}
 __device__ __forceinline__ uint64_t ld2p(const float* p) {
   return *reinterpret_cast<const uint64_t*>(p);
 }
-__device__ __forceinline__ uint64_t ld2p(const __nv_bfloat16* p) {
-  const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-  return (static_cast<uint64_t>(w & 0xffff0000u) << 32) | (w << 16);
-}
 __device__ __forceinline__ float ld1(const float* p) { return *p; }
-__device__ __forceinline__ float ld1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st1(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
@@ -135,6 +128,7 @@ __device__ __forceinline__ void sub_chunk(const Ranges& r, int o, int64_t& s0, i
   rows = static_cast<int>(min(static_cast<int64_t>(kSub), r.b[k] - s0));
 }
 
+// fp32 decode on the FP32 FMA units (the bf16 kernel is decode_mma_kernel below).
 // Online softmax over the CTA's slots, one 64-slot sub-chunk (its K and V rows, one
 // copy each) at a time through a ring of kStages buffers.  Scores run in log2 units:
 // q is pre-multiplied by scale * log2(e), the weights are exp2 of the differences,
@@ -328,6 +322,275 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
   }
 }
 
+// bf16 decode with the dot products on the warp-level tensor cores.  The scores of a
+// group's G query heads against a sub-chunk of keys are S^T = K q^T (an m16n8k16 MMA:
+// 16 slots x 8 heads, the heads past G zero), and the output is O^T += V^T P^T (16 value
+// columns x 8 heads per MMA).  That takes the dot products off the FP32 and issue paths,
+// which bound the plain version, so the step is left to the memory system.  Each of the
+// 4 warps owns 16 slots of every 64-slot sub-chunk and keeps its own running max, sum
+// and output (in the MMA fragment layout a lane holds heads 2 (l % 4) and 2 (l % 4) + 1
+// in S^T and O^T alike, so its running max rescales its own outputs); the warps merge
+// once at the end.  A sub-chunk's K and V rows arrive as TMA boxes of 64 rows x 64
+// columns with the 128-byte swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)),
+// which keeps the eight rows of every 8 x 8 matrix load in distinct banks.
+constexpr int kMmaWarps = 4;
+constexpr int kMmaThreads = 32 * kMmaWarps;
+constexpr int kMmaStages = 2;
+
+template <int D>
+struct MmaCfg {
+  static constexpr int kBoxBytes = kSub * 128;           // 64 rows x 64 bf16 columns
+  static constexpr int kBoxes = D / 64;                   // boxes per row block
+  static constexpr int kTensorBytes = kBoxes * kBoxBytes;  // K or V rows of one sub-chunk
+  static constexpr int kStageBytes = 2 * kTensorBytes;    // K then V
+  static constexpr int kSteps = D / 16;                   // 16-wide steps over d (k or m tiles)
+  // shared layout (1024-byte aligned): stages [kMmaStages] of K, V | per-warp max and
+  // sum [2][warps][8] | barriers full [kMmaStages], empty [kMmaStages]
+  static constexpr int kOffStats = kMmaStages * kStageBytes;
+  static constexpr int kOffBar = kOffStats + 2 * kMmaWarps * 8 * 4;
+  static constexpr int kSmemBytes = kOffBar + 16 * kMmaStages + 1024;
+  static_assert(kSub == 16 * kMmaWarps, "16 slots per warp");
+  static_assert(kMmaWarps * 8 * D * 4 <= kMmaStages * kStageBytes, "warp partials fit");
+  static_assert(kOffBar % 8 == 0, "alignment");
+};
+
+// Shared address of 16-byte chunk c (8 columns) of row r in a swizzled row block.
+__device__ __forceinline__ uint32_t swz(uint32_t block, int r, int c) {
+  return block + (c >> 3) * (kSub * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMmaThreads)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const DecParams p) {
+  using Cfg = MmaCfg<D>;
+  constexpr float kRescale = 8.0f;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s0addr = smem_addr(smem);                      // stage st at + st * kStageBytes
+  float* wm = reinterpret_cast<float*>(smem + Cfg::kOffStats);  // [warps][8] max
+  float* wl = wm + kMmaWarps * 8;                               // [warps][8] sum
+  const uint32_t full0 = smem_addr(smem + Cfg::kOffBar);
+  const uint32_t empty0 = full0 + 8 * kMmaStages;
+
+  const int split = blockIdx.x % p.nsplit;
+  const int bk = blockIdx.x / p.nsplit;  // b * Hkv + kv head
+  const int b = bk / p.Hkv, hk = bk % p.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int64_t t = p.pos[b];
+  const int64_t lo = static_cast<int64_t>(split) * p.span;
+  const Ranges rg = valid_ranges(t, p.cap, p.window, lo, min(p.cap, lo + p.span));
+  int n_sub = 0;
+  for (int k = 0; k < rg.n; ++k) n_sub += static_cast<int>((rg.b[k] - rg.a[k] + kSub - 1) / kSub);
+
+  // thread 0 copies sub-chunk o: 64 rows from its first slot, K then V, one box per 64
+  // columns (rows past the slot range are read too, and masked; past cap they are zero)
+  auto issue = [&](int o) {
+    int64_t s0;
+    int rows;
+    sub_chunk(rg, o, s0, rows);
+    const int st = o % kMmaStages;
+    const uint32_t bar = full0 + 8 * st, dst = s0addr + st * Cfg::kStageBytes;
+    mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+#pragma unroll
+    for (int c = 0; c < Cfg::kBoxes; ++c) {
+      tma_load_4d(dst + c * Cfg::kBoxBytes, &tmK, bar, 64 * c, 0, static_cast<int>(s0), bk);
+      tma_load_4d(dst + Cfg::kTensorBytes + c * Cfg::kBoxBytes, &tmV, bar, 64 * c, 0,
+                  static_cast<int>(s0), bk);
+    }
+  };
+  int issued = 0;  // copies issued so far: counted alike by every lane of warp 0
+  if (warp == 0) {  // the first copies start before anything else
+    if (lane == 0) {
+      for (int k = 0; k < kMmaStages; ++k) {
+        mbar_init(full0 + 8 * k, 1);
+        mbar_init(empty0 + 8 * k, kMmaWarps);
+      }
+      fence_barrier_init();
+    }
+    for (; issued < kMmaStages && issued < n_sub; ++issued)
+      if (lane == 0) issue(issued);
+    __syncwarp();
+  }
+  // q as the B operand of S^T = K q^T: lane holds elements 16 kk + 2 tig (+1) and
+  // (+8) of head grp; heads past G are zero
+  uint32_t qb[Cfg::kSteps][2];
+  {
+    const __nv_bfloat16* qg =
+        static_cast<const __nv_bfloat16*>(p.q) + (static_cast<int64_t>(b) * p.Hq + hk * G) * D;
+#pragma unroll
+    for (int kk = 0; kk < Cfg::kSteps; ++kk) {
+      qb[kk][0] = 0u;
+      qb[kk][1] = 0u;
+      if (grp < G) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(qg + grp * D + 16 * kk + 2 * tig);
+        qb[kk][0] = src[0];
+        qb[kk][1] = src[4];
+      }
+    }
+  }
+  __syncthreads();  // barrier initialisation is visible
+
+  const float c2 = p.scale * 1.4426950408889634f;  // scores in log2 units
+  float m[2] = {-INFINITY, -INFINITY}, lp[2] = {0.f, 0.f};  // heads 2 tig, 2 tig + 1
+  float o[Cfg::kSteps][4];  // O^T: value column 16 mt + grp (+8), heads 2 tig (+1)
+#pragma unroll
+  for (int mt = 0; mt < Cfg::kSteps; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+  // this lane's rows in the 8 x 8 matrix loads: K as the A operand of S^T, V as the
+  // (transposed) A operand of O^T
+  const int k0 = warp * 16;  // this warp's slots [k0, k0 + 16) of every sub-chunk
+  const int rk = k0 + (lane & 7) + 8 * ((lane >> 3) & 1), ck = lane >> 4;
+  const int rv = k0 + (lane & 7) + 8 * ((lane >> 4) & 1), cv = (lane >> 3) & 1;
+  bool ok = true;
+  for (int sc = 0; sc < n_sub; ++sc) {
+    const int st = sc % kMmaStages;
+    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * st, (sc / kMmaStages) & 1, kWaitBudget,
+                                           p.err, kErrTimeout))) {
+      ok = false;
+      break;
+    }
+    int64_t s0;
+    int rows;
+    sub_chunk(rg, sc, s0, rows);
+    if (k0 < rows) {  // (slot k0 valid: every max below is finite)
+      const uint32_t kst = s0addr + st * Cfg::kStageBytes, vst = kst + Cfg::kTensorBytes;
+      if (k0 + 16 > rows) {
+        // rows past the slot range hold other slots' values; zero them so that
+        // 0-weight slots add exact zeros (whatever those rows hold)
+        uint8_t* vblk = smem + st * Cfg::kStageBytes + Cfg::kTensorBytes;
+        for (int x = lane; x < (k0 + 16 - rows) * Cfg::kBoxes * 8; x += 32) {
+          const int r = rows + x / (Cfg::kBoxes * 8), c = x % (Cfg::kBoxes * 8);
+          *reinterpret_cast<uint4*>(vblk + (c >> 3) * Cfg::kBoxBytes + r * 128 + 16 * (c & 7)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // ordered before the copies that later refill the stage
+        __syncwarp();
+      }
+      // S^T (16 slots x 8 heads) = K q^T, over d in 16-wide steps
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < Cfg::kSteps; ++kk) {
+        uint32_t a[4];
+        ldmatrix_x4(swz(kst, rk, 2 * kk + ck), a);
+        mma_16816_bf16(s, a, qb[kk][0], qb[kk][1]);
+      }
+      // lane: slots k0 + grp (s[0], s[1]) and k0 + grp + 8 (s[2], s[3]), heads 2 tig (+1)
+      const bool va = k0 + grp < rows, vb = k0 + grp + 8 < rows;
+      const float x[4] = {va ? s[0] * c2 : -INFINITY, va ? s[1] * c2 : -INFINITY,
+                          vb ? s[2] * c2 : -INFINITY, vb ? s[3] * c2 : -INFINITY};
+      // per head, the max over the warp's 16 slots (the 8 lanes sharing tig); the
+      // running max moves (and the outputs rescale) only when it grows by more than 2^8
+      float corr[2];
+      bool need = false;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(x[j], x[2 + j]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        corr[j] = 1.f;
+        if (mx > m[j] + kRescale) {
+          corr[j] = exp2f(m[j] - mx);  // 0 while m[j] is -inf
+          lp[j] *= corr[j];
+          m[j] = mx;
+          need = true;
+        }
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int mt = 0; mt < Cfg::kSteps; ++mt) {
+          o[mt][0] *= corr[0];
+          o[mt][1] *= corr[1];
+          o[mt][2] *= corr[0];
+          o[mt][3] *= corr[1];
+        }
+      }
+      float pw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pw[e] = exp2f(x[e] - m[e & 1]);  // 0 for slots past the rows
+      lp[0] += pw[0] + pw[2];
+      lp[1] += pw[1] + pw[3];
+      // P^T as the B operand: the transposes of P's two 8 x 8 blocks (slots x heads)
+      const uint32_t b0 = movmatrix_trans(pack_bf16x2(pw[0], pw[1]));
+      const uint32_t b1 = movmatrix_trans(pack_bf16x2(pw[2], pw[3]));
+      // O^T (d x heads) += V^T (d x slots) P^T (slots x heads), 16 value columns a step
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kSteps; ++mt) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(swz(vst, rv, 2 * mt + cv), a);
+        mma_16816_bf16(o[mt], a, b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);  // this warp has left the stage
+    if (warp == 0 && issued < n_sub) {            // refill it once every warp has left
+      if (__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * st, (sc / kMmaStages) & 1, kWaitBudget,
+                                            p.err, kErrTimeout))) {
+        if (lane == 0) issue(issued);
+        ++issued;
+      } else {
+        ok = false;
+      }
+      __syncwarp();
+    }
+  }
+  // drain: the last copies issued into each stage have landed (at once when consumed)
+  if (tid == 0)
+    for (int x = max(0, issued - kMmaStages); x < issued; ++x)
+      mbar_wait(full0 + 8 * (x % kMmaStages), (x / kMmaStages) & 1, kWaitBudget, p.err,
+                kErrTimeout);
+  if (!__syncthreads_and(ok)) return;
+
+  // merge the warps (in the now idle stage buffers) and write this split's partial
+  float* red = reinterpret_cast<float*>(smem);  // [warps][8][D]
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {  // the warp's sum: the 8 lanes sharing tig
+    lp[j] += __shfl_xor_sync(0xffffffffu, lp[j], 4);
+    lp[j] += __shfl_xor_sync(0xffffffffu, lp[j], 8);
+    lp[j] += __shfl_xor_sync(0xffffffffu, lp[j], 16);
+  }
+#pragma unroll
+  for (int mt = 0; mt < Cfg::kSteps; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      red[(warp * 8 + 2 * tig + (e & 1)) * D + 16 * mt + grp + 8 * (e >> 1)] = o[mt][e];
+  if (grp == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      wm[warp * 8 + 2 * tig + j] = m[j];
+      wl[warp * 8 + 2 * tig + j] = lp[j];
+    }
+  }
+  __syncthreads();
+  float* out = p.part + (static_cast<int64_t>(b) * p.Hq + hk * G) * p.nsplit * (D + 2);
+  for (int x = tid; x < G * D; x += kMmaThreads) {
+    const int g = x / D, c = x % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, wm[w * 8 + g]);
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w)
+      if (wm[w * 8 + g] > -INFINITY) a = fmaf(red[(w * 8 + g) * D + c], exp2f(wm[w * 8 + g] - M), a);
+    out[(static_cast<int64_t>(g) * p.nsplit + split) * (D + 2) + c] = a;
+  }
+  if (tid < G) {
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w)
+      if (wm[w * 8 + tid] > -INFINITY) L = fmaf(wl[w * 8 + tid], exp2f(wm[w * 8 + tid] - M), L);
+    float* row = out + (static_cast<int64_t>(tid) * p.nsplit + split) * (D + 2);
+    row[D] = M;
+    row[D + 1] = L;
+  }
+}
+
 // Merge the splits of every (batch, query head): one warp each.  Maxima are in log2
 // units; LSE is returned in natural-log units.
 template <typename In, int D>
@@ -374,18 +637,33 @@ __global__ void kv_append_kernel(In* Kc, In* Vc, const In* kn, const In* vn, con
   }
 }
 
+// bf16 runs on the warp-level tensor cores; fp32 (products that must stay within 1e-5)
+// on the FP32 FMA units.
 template <typename In, int D, int G>
 cudaError_t launch_decode_g(const DecParams& p, cudaStream_t st) {
-  using Cfg = DecCfg<In, D, G>;
+  constexpr bool kMma = std::is_same<In, __nv_bfloat16>::value;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_kernel<In, D, G>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if constexpr (kMma)
+      attr_err = cudaFuncSetAttribute(decode_mma_kernel<D, G>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      MmaCfg<D>::kSmemBytes);
+    else
+      attr_err = cudaFuncSetAttribute(decode_kernel<In, D, G>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      DecCfg<In, D, G>::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int64_t ctas = static_cast<int64_t>(p.B) * p.Hkv * p.nsplit;
-  decode_kernel<In, D, G><<<static_cast<unsigned>(ctas), kThreads, Cfg::kSmemBytes, st>>>(p);
+  const unsigned ctas = static_cast<unsigned>(static_cast<int64_t>(p.B) * p.Hkv * p.nsplit);
+  if constexpr (kMma) {
+    CUtensorMap mK, mV;  // the caches as [B * Hkv][cap][D], boxes of 64 slots x 64 columns
+    const long long bh = static_cast<long long>(p.B) * p.Hkv;
+    if (!make_map(&mK, p.Kc, D, p.cap, bh, 1, kSub) || !make_map(&mV, p.Vc, D, p.cap, bh, 1, kSub))
+      return cudaErrorInvalidValue;
+    decode_mma_kernel<D, G><<<ctas, kMmaThreads, MmaCfg<D>::kSmemBytes, st>>>(mK, mV, p);
+  } else
+    decode_kernel<In, D, G><<<ctas, kThreads, DecCfg<In, D, G>::kSmemBytes, st>>>(p);
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq;
   decode_combine_kernel<In, D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(p);
   return cudaGetLastError();
@@ -406,11 +684,10 @@ cudaError_t launch_decode_typed(const DecParams& p, cudaStream_t st) {
 
 int decode_splits(int64_t B, int64_t Hkv, int64_t cap) {
   // One wave: the (b, kv head) pairs times the splits fill at most the CTAs that are
-  // resident at once (two per SM for d = 128, G = 4, bounded by registers).  A single
-  // wave of long CTAs streams the cache faster than several waves of short ones: less
-  // per-CTA set-up and no partly filled last wave (B = 8: 45.5 us at 4 splits against
-  // 53.8 us at 14; B = 32: 1 split is as fast as 4).
-  constexpr int64_t kResidentCtas = 2 * 148;
+  // resident at once (three per SM for the bf16 kernel, bounded by its shared memory).
+  // A single wave of long CTAs streams the cache faster than several waves of short
+  // ones: less per-CTA set-up and no partly filled last wave.
+  constexpr int64_t kResidentCtas = 3 * 148;
   const int64_t per = kResidentCtas / (B * Hkv);
   const int64_t most = (cap + kSub - 1) / kSub;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(per, std::min<int64_t>(most, 64))));

@@ -33,7 +33,7 @@ EncodeTiledFn get_encode_fn() {
 }  // namespace
 
 bool make_map(CUtensorMap* map, const void* base, int D, long long rows, long long BH,
-              long long dview) {
+              long long dview, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   if (rows < 1) rows = 1;
@@ -42,7 +42,7 @@ bool make_map(CUtensorMap* map, const void* base, int D, long long rows, long lo
                         static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[3] = {row_bytes, row_bytes * static_cast<cuuint64_t>(dview),
                            row_bytes * static_cast<cuuint64_t>(dview) * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
