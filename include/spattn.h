@@ -241,8 +241,9 @@ spattn_status spattn_bwd(const spattn_plan* plan, int32_t B, int32_t H, spattn_d
  * generation.  Position p lives in slot p % cap of the cache.
  *
  * Layouts (device memory, contiguous, 16-byte aligned):
- *   K_cache, V_cache: [B, Hkv, cap, d] of `dtype` (caller-owned; slots never written
- *                     are never read while pos[b] < cap);
+ *   K_cache, V_cache: [B, Hkv, cap, d] of `dtype` (caller-owned; slots outside the
+ *                     window never affect the result, whatever they hold: bf16 reads
+ *                     whole 64-slot blocks and masks the slots past the window);
  *   q, out:           [B, Hq, d] of `dtype`; lse: [B, Hq] fp32 natural log (or NULL);
  *   k_new, v_new:     [B, Hkv, d] of `dtype`;
  *   pos:              [B] int64, device memory: the position of the token each batch
@@ -271,7 +272,9 @@ spattn_status spattn_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, 
  * head h / (Hq/Hkv), the allowed positions being max(0, pos[b]-window+1) .. pos[b]
  * (window = 0 means window = cap; 1 <= window <= cap).  The caller appends the
  * step's own key and value (spattn_kv_append) before calling, as the token reads
- * itself.  Asynchronous on cuda_stream; fp32 accumulation; bf16 out rounded once.
+ * itself.  Asynchronous on cuda_stream; fp32 accumulation.  bf16: products on the
+ * tensor cores with the softmax weights rounded to bf16 for the weighted sum (as the
+ * forward pass), out rounded once; fp32: FP32 products throughout.
  * Device-side waits are bounded: one that runs out sets the workspace's error word
  * (reported by spattn_decode_check as SPATTN_ERR_TIMEOUT).
  * Errors: NULL, ALIGN, SHAPE (also a workspace smaller than
