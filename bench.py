@@ -53,8 +53,8 @@ TRAFFIC = {"kernel_sha": "9618899bf5ccef92", "bytes_per_launch": 998.6e6, "workl
 # decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
 BWD_TRAFFIC = {"kernel_sha": "988fd762c2c34052", "bytes_per_launch": 1348.9e6,
                "workload": "t32k_w4096", "file": "bwd_tc.cu"}
-DEC_TRAFFIC = {"kernel_sha": "5f521481acc76771", "file": "decode.cu",
-               "bytes_per_launch": {"decode_b8_w4096": 140.4e6, "decode_b32_w4096": 561.7e6}}
+DEC_TRAFFIC = {"kernel_sha": "759ec790e0e58505", "file": "decode.cu",
+               "bytes_per_launch": {"decode_b8_w4096": 140.4e6, "decode_b32_w4096": 561.5e6}}
 
 
 def kernel_sha(name: str = "fwd_tc.cu") -> str:

@@ -683,11 +683,12 @@ cudaError_t launch_decode_typed(const DecParams& p, cudaStream_t st) {
 }  // namespace
 
 int decode_splits(int64_t B, int64_t Hkv, int64_t cap) {
-  // One wave: the (b, kv head) pairs times the splits fill at most the CTAs that are
-  // resident at once (three per SM for the bf16 kernel, bounded by its shared memory).
-  // A single wave of long CTAs streams the cache faster than several waves of short
-  // ones: less per-CTA set-up and no partly filled last wave.
-  constexpr int64_t kResidentCtas = 3 * 148;
+  // At most 2 x 148 CTAs in all (the bf16 kernel keeps three per SM resident, so this
+  // is a single wave): few, long CTAs amortise each CTA's start-up and final merge over
+  // many sub-chunks.  Measured on the bf16 kernel (graph-replayed steps): B = 8 (64 kv
+  // heads) 31.7 us at 4 splits against 34.1 at 6 and 38.0 at 2; B = 32 (256 kv heads)
+  // 88.7 us at 1 split against 93.6 at 3.
+  constexpr int64_t kResidentCtas = 2 * 148;
   const int64_t per = kResidentCtas / (B * Hkv);
   const int64_t most = (cap + kSub - 1) / kSub;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(per, std::min<int64_t>(most, 64))));
