@@ -114,3 +114,26 @@ def test_null_arguments_are_rejected(built):
                             None) == sp.ERR_NULL
     built.spattn_plan_destroy(None)
     assert built.spattn_last_error()
+
+
+def test_decode_workspace_bytes_without_gpu(built):
+    """The workspace holds a 256-byte header (error word) and one (d + 2)-float partial per
+    (batch, query head, split); the split count keeps B * Hkv * splits within 2 * 148
+    CTAs, at most 64 splits and one 64-slot sub-chunk per split at least."""
+    import ctypes
+    n = ctypes.c_size_t()
+
+    def ws(B, Hq, Hkv, cap, d):
+        assert built.spattn_decode_workspace_bytes(B, Hq, Hkv, cap, d, ctypes.byref(n)) == sp.OK
+        return n.value
+
+    def expect(B, Hq, Hkv, cap, d, splits):
+        return 256 + B * Hq * splits * (d + 2) * 4
+
+    assert ws(8, 32, 8, 4096, 128) == expect(8, 32, 8, 4096, 128, 4)      # 296 // 64
+    assert ws(32, 32, 8, 4096, 128) == expect(32, 32, 8, 4096, 128, 1)    # 296 // 256
+    assert ws(64, 32, 8, 4096, 128) == expect(64, 32, 8, 4096, 128, 1)    # never below 1
+    assert ws(1, 8, 1, 100000, 64) == expect(1, 8, 1, 100000, 64, 64)     # at most 64
+    assert ws(1, 8, 2, 100, 64) == expect(1, 8, 2, 100, 64, 2)            # ceil(100 / 64)
+    assert built.spattn_decode_workspace_bytes(1, 8, 3, 100, 64, ctypes.byref(n)) == sp.ERR_SHAPE
+    assert built.spattn_decode_workspace_bytes(1, 8, 2, 100, 64, None) == sp.ERR_NULL
