@@ -17,7 +17,9 @@ Under torchrun each rank runs its own copy of the workload on its GPU (heads are
 independent; there is no collective on the data path), and value sums over ranks.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this method) on a
-bounded sample of query rows of the same workload, on the host cores.
+bounded sample of the same workload, on the host cores: query rows of one head for the
+forward, dQ of sampled rows for --pass bwd, sampled (batch, kv head) groups for --pass
+decode, each in its pass's metric and unit.
 """
 from __future__ import annotations
 
@@ -283,6 +285,114 @@ def run_reference(args, cfg, p):
                          "sample": f"{args.steps} steps x {n} rows of head (0,0), "
                                    f"{done} allowed pairs"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_reference_bwd(args, cfg, p):
+    """The backward's reference arm: the oracle's dQ of seeded sampled rows of one head
+    (each row's dQ needs only its own allowed set), bounded per step.  It is credited
+    with the full backward's 10 d flops per pair although it computes only dQ, so the
+    arm is if anything overstated."""
+    world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    oracle.build()
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    g = torch.Generator().manual_seed(0)
+    Q, K, V, dO = (torch.randn(T, d, generator=g).to(torch.bfloat16) for _ in range(4))
+    m = oracle.Mask.from_params(T, p)
+    q, k, v, do = (oracle.bf16_bits(x) for x in (Q, K, V, dO))
+    scale = 1.0 / math.sqrt(d)
+    rows = W.sample_rows(T, 16, 11)
+    t0 = time.perf_counter()
+    oracle.attention_bwd_dq(m, q, k, v, do, scale, rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(T, max(16, 16 * 2.0 / dt)))
+    samples = [W.sample_rows(T, n, 100 + s) for s in range(args.warmup + args.steps)]
+    pairs = [sum(len(m.row_set(int(r))) for r in rs) for rs in samples]
+    for s in range(args.warmup):
+        oracle.attention_bwd_dq(m, q, k, v, do, scale, samples[s])
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        oracle.attention_bwd_dq(m, q, k, v, do, scale, samples[s])
+    secs = time.perf_counter() - t0
+    done = sum(pairs[args.warmup:])
+    value = 10 * d * done / secs / 1e12
+    line = {
+        "impl": "reference", "metric": BWD_METRIC, "pass": "bwd", "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d,
+                   "mask": mask_desc(p),
+                   "step": f"dQ of {n} seeded query rows of one head per step (bounded "
+                           f"sample, credited with 10 d flops per pair)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} steps x dQ of {n} rows, {done} allowed pairs"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_reference_decode(args):
+    """The decode step's reference arm: the oracle's decode of every query head of
+    seeded sampled (batch, kv head) groups, bounded per step; the bytes are each
+    group's cached K/V rows of the window, counted once for its G heads (as the GPU
+    arm counts them)."""
+    world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    oracle.build()
+    cfg = W.DECODE_WORKLOADS[args.decode_workload]
+    B, Hq, Hkv, cap, w, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["cap"], cfg["window"], cfg["d"]
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(0)
+    Kc, Vc = (oracle.bf16_bits(torch.randn(cap, d, generator=g).to(torch.bfloat16))
+              for _ in range(2))
+    qs = [oracle.bf16_bits(torch.randn(d, generator=g).to(torch.bfloat16)) for _ in range(G)]
+    pos = W.decode_positions(B, cap, 0)
+    scale = 1.0 / math.sqrt(d)
+    group_bytes = w * d * 2 * 2
+
+    def groups(n, s):  # n groups: every head of the group at its sequence's position
+        for i in range(n):
+            t = int(pos[(s * n + i) % B]) + s
+            for h in range(G):
+                oracle.decode(qs[h], Kc, Vc, t, w, scale)
+
+    t0 = time.perf_counter()
+    groups(1, 0)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(1, min(B * Hkv, 1.0 / dt)))
+    for s in range(args.warmup):
+        groups(n, s)
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        groups(n, s)
+    secs = time.perf_counter() - t0
+    value = group_bytes * n * args.steps / secs / 1e9
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "pass": "decode", "value": value,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.decode_workload, **cfg,
+                   "step": f"{n} of the {B * Hkv} (batch, kv head) groups per step, all "
+                           f"{G} query heads each (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} steps x {n} groups x {G} heads, window {w}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -672,6 +782,10 @@ def main():
         cfg["H"] = args.heads
     p = W.mask_params(args.workload)
     if args.impl == "reference":
+        if args.which == "bwd":
+            return run_reference_bwd(args, cfg, p)
+        if args.which == "decode":
+            return run_reference_decode(args)
         return run_reference(args, cfg, p)
     if args.which == "bwd":
         return run_ours_bwd(args, cfg, p)

@@ -63,3 +63,24 @@ def test_reference_arm_under_torchrun_prints_one_line(oracle_mod):
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("args", [
+    ["--pass", "bwd", "--workload", "t512_w128_s0"],
+    ["--pass", "decode", "--decode-workload", "decode_b8_w4096"],
+], ids=["bwd", "decode"])
+def test_reference_arms_of_the_other_passes(oracle_mod, args):
+    """The oracle arm of the backward and decode passes prints one line with the same
+    metric and unit as the GPU arm of that pass."""
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", *args], cwd=ROOT, capture_output=True, text=True,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    sys.path.insert(0, ROOT)
+    import bench
+    want = bench.BWD_METRIC if args[1] == "bwd" else bench.DECODE_METRIC
+    assert line["impl"] == "reference" and line["metric"] == want and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["value"] == line["value"]
