@@ -60,6 +60,8 @@ CASES = [
     (2, 2, 1, 130, 65, 128, [-1, 129]),
     (4, 16, 8, 1000, 999, 64, [998, 999, 1500, 3]),
     (1, 2, 2, 5000, 4000, 128, [4999]),
+    (2, 16, 2, 200, 150, 64, [199, 1000]),  # G = 8 at d = 64
+    (1, 8, 2, 512, 0, 64, [600]),           # G = 4 at d = 64, full window, wrapped
 ]
 
 
