@@ -63,6 +63,10 @@ def _configure(lib):
         _i64, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_double, _vp, _i64,
         ctypes.POINTER(ctypes.c_double)]
     lib.oracle_attention_bwd_dq_rows.restype = None
+    lib.oracle_attention_bwd_dkdv_keys.argtypes = spec + [
+        _i64, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_double, _vp, _i64,
+        ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    lib.oracle_attention_bwd_dkdv_keys.restype = None
     lib.oracle_decode.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp,
                                   ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                   ctypes.POINTER(ctypes.c_double)]
@@ -246,6 +250,26 @@ def attention_bwd_dq(mask: Mask, Q, K, V, dO, scale: float, rows):
         dO.ctypes.data, float(scale), rr.ctypes.data, int(rr.size),
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return out
+
+
+def attention_bwd_dkdv(mask: Mask, Q, K, V, dO, scale: float, keys):
+    """fp64 (dK, dV), each [len(keys), d], of the listed keys only: every row that
+    reads a listed key contributes, with its softmax taken over its whole set."""
+    T, d = Q.shape
+    assert T == mask.T
+    dt = 0 if Q.dtype == np.float32 else 1
+    Q, K, V, dO = (np.ascontiguousarray(x) for x in (Q, K, V, dO))
+    kk = np.ascontiguousarray(np.asarray(keys, dtype=np.int64))
+    assert kk.size == 0 or (kk.min() >= 0 and kk.max() < T)
+    assert np.unique(kk).size == kk.size, "keys must be distinct"
+    dK = np.zeros((kk.size, d), np.float64)
+    dV = np.zeros((kk.size, d), np.float64)
+    pd = ctypes.POINTER(ctypes.c_double)
+    _load().oracle_attention_bwd_dkdv_keys(
+        *mask._args(), int(d), dt, Q.ctypes.data, K.ctypes.data, V.ctypes.data,
+        dO.ctypes.data, float(scale), kk.ctypes.data, int(kk.size),
+        dK.ctypes.data_as(pd), dV.ctypes.data_as(pd))
+    return dK, dV
 
 
 def decode(q, Kc, Vc, t: int, window: int, scale: float):

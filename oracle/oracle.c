@@ -46,7 +46,9 @@
  *   unchanged.
  *
  *   Gradients.  oracle_attention_bwd_head: dQ, dK, dV of the same y given dO, by the
- *   chain rule through the softmax over S_i (see the function).
+ *   chain rule through the softmax over S_i (see the function);
+ *   oracle_attention_bwd_dq_rows and oracle_attention_bwd_dkdv_keys: the same
+ *   gradients for listed query rows or listed keys only.
  *
  *   Decode.  oracle_decode: one new token against a ring-buffer KV cache that keeps
  *   the last cap tokens (see the function).
@@ -347,16 +349,6 @@ int64_t oracle_attention_head(int causal, int64_t window, int64_t radius, int64_
 
 /* ---- gradients of the attention over the allowed sets ------------------------- */
 
-/* One head: given dO (the gradient of a loss with respect to y), the gradients with
- * respect to Q, K and V of y_i = sum_{j in S_i} alpha_ij v_j, alpha_ij =
- * softmax_{j in S_i}(scale q_i . k_j).  By the chain rule through the softmax over S_i:
- *   dV_j = sum_{i : j in S_i} alpha_ij dO_i
- *   dalpha_ij = dO_i . v_j,   D_i = sum_{j in S_i} alpha_ij dalpha_ij  (= dO_i . y_i)
- *   ds_ij = alpha_ij (dalpha_ij - D_i)            (softmax Jacobian over S_i)
- *   dQ_i = scale sum_{j in S_i} ds_ij k_j,   dK_j = scale sum_{i : j in S_i} ds_ij q_i
- * Every row is recomputed from its definition in fp64 (no saved forward state).
- * Q, K, V, dO: [T][d], dtype 0 = fp32, 1 = bf16 bits.  dQ, dK, dV: [T][d] fp64,
- * overwritten.  Sequential over rows (dK and dV gather from every row). */
 /* One row i of the gradient: recomputes alpha_ij over S_i, adds row i's share to
  * dK and dV (when they are not NULL) and writes dQ_i to dq_row.  set, a, da: [T]. */
 static void bwd_row(const omask* m, int64_t i, int64_t d, int dtype, const void* Q,
@@ -447,6 +439,98 @@ void oracle_attention_bwd_dq_rows(int causal, int64_t window, int64_t radius, in
     free(a);
     free(da);
   }
+}
+
+/* dK and dV of the listed keys only.  Key j takes a share from every row i whose
+ * allowed set holds it (the transposed set {i : j in S_i}), and each share needs row
+ * i's whole softmax: its logit maximum, its normaliser and D_i, all over S_i.  So:
+ * (1) mark the rows that read at least one listed key; (2) compute those rows'
+ * softmax statistics over their allowed sets, as bwd_row does; (3) for each listed
+ * key, visit the rows in ascending order and add
+ *   dV_j += alpha_ij dO_i,   dK_j += scale alpha_ij (dO_i . v_j - D_i) q_i
+ * (the same chain rule as oracle_attention_bwd_head, read key by key).
+ * keys: n_keys distinct indices in [0, T).  dK_keys, dV_keys: [n_keys][d] fp64. */
+void oracle_attention_bwd_dkdv_keys(int causal, int64_t window, int64_t radius,
+                                    int64_t dilation, int64_t stride, int64_t offset,
+                                    int64_t n_global, const int32_t* gpos, int64_t T,
+                                    int64_t rand_block, int64_t n_rand,
+                                    const int32_t* rand_pairs, int64_t d, int dtype,
+                                    const void* Q, const void* K, const void* V,
+                                    const void* dO, double scale, const int64_t* keys,
+                                    int64_t n_keys, double* dK_keys, double* dV_keys) {
+  omask m = {causal,     window,  radius, dilation, stride, offset,
+               n_global,   gpos,    T,      rand_block, n_rand, rand_pairs};
+  unsigned char* need = (unsigned char*)calloc((size_t)T, 1);
+  double* rmax = (double*)malloc(sizeof(double) * (size_t)T);
+  double* rsum = (double*)malloc(sizeof(double) * (size_t)T);
+  double* rD = (double*)malloc(sizeof(double) * (size_t)T);
+  /* (1) rows that read a listed key */
+#pragma omp parallel for schedule(dynamic, 256)
+  for (int64_t i = 0; i < T; i++)
+    for (int64_t a = 0; a < n_keys; a++)
+      if (allowed(&m, i, keys[a])) {
+        need[i] = 1;
+        break;
+      }
+  /* (2) their softmax statistics over S_i */
+#pragma omp parallel
+  {
+    int32_t* set = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+    double* s = (double*)malloc(sizeof(double) * (size_t)T);
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t i = 0; i < T; i++) {
+      if (!need[i]) continue;
+      const int64_t n = row_set_union(&m, i, set);
+      double mx = -INFINITY;
+      for (int64_t t = 0; t < n; t++) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; k++)
+          acc += load_elem(Q, dtype, i * d + k) * load_elem(K, dtype, set[t] * d + k);
+        s[t] = scale * acc;
+        if (s[t] > mx) mx = s[t];
+      }
+      double l = 0.0;
+      for (int64_t t = 0; t < n; t++) l += exp(s[t] - mx);
+      double D = 0.0;
+      for (int64_t t = 0; t < n; t++) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; k++)
+          acc += load_elem(dO, dtype, i * d + k) * load_elem(V, dtype, set[t] * d + k);
+        D += exp(s[t] - mx) / l * acc;
+      }
+      rmax[i] = mx;
+      rsum[i] = l;
+      rD[i] = D;
+    }
+    free(set);
+    free(s);
+  }
+  /* (3) each listed key gathers the shares of the rows that read it */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t a = 0; a < n_keys; a++) {
+    const int64_t j = keys[a];
+    double* dk = dK_keys + a * d;
+    double* dv = dV_keys + a * d;
+    for (int64_t k = 0; k < d; k++) dk[k] = dv[k] = 0.0;
+    for (int64_t i = 0; i < T; i++) {
+      if (!allowed(&m, i, j)) continue;
+      double qk = 0.0, gv = 0.0;
+      for (int64_t k = 0; k < d; k++) {
+        qk += load_elem(Q, dtype, i * d + k) * load_elem(K, dtype, j * d + k);
+        gv += load_elem(dO, dtype, i * d + k) * load_elem(V, dtype, j * d + k);
+      }
+      const double alpha = exp(scale * qk - rmax[i]) / rsum[i];
+      const double ds = alpha * (gv - rD[i]);
+      for (int64_t k = 0; k < d; k++) {
+        dv[k] += alpha * load_elem(dO, dtype, i * d + k);
+        dk[k] += scale * ds * load_elem(Q, dtype, i * d + k);
+      }
+    }
+  }
+  free(need);
+  free(rmax);
+  free(rsum);
+  free(rD);
 }
 
 /* ---- decode with a capped KV cache ------------------------------------------------ */

@@ -595,6 +595,47 @@ def check_bwd_invariants():
     return bad
 
 
+def check_bwd_key_subset(seed=23):
+    """dK and dV of listed keys only, against torch's fp64 autograd through SDPA with
+    the independent numpy mask (the same library pin as the full gradient), on masks
+    with every rule (dilated, strided, global, random blocks), the edge keys 0 and
+    T - 1 always among the listed ones; and equal to the full evaluation's rows."""
+    bad = []
+    specs = [dict(T=37, causal=1, window=5, radius=-1, stride=4, offset=1, global_pos=[3, 30],
+                  dilation=1),
+             dict(T=45, causal=0, window=0, radius=3, stride=0, offset=0, global_pos=[0],
+                  dilation=2)] + small_specs(seed, n=14)
+    rng = np.random.default_rng(seed)
+    for n, e in enumerate(specs):
+        T = e["T"]
+        d = 8
+        g = torch.Generator().manual_seed(700 + n)
+        Q, K, V, dO = (torch.randn(T, d, generator=g) for _ in range(4))
+        sc = 0.5 / math.sqrt(d)
+        keys = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=min(T, 5),
+                                                                replace=False)])).astype(np.int64)
+        rng.shuffle(keys)
+        D = torch.from_numpy(dense_of(e))
+        q, k, v = (x.double().requires_grad_(True) for x in (Q, K, V))
+        y = torch.nn.functional.scaled_dot_product_attention(
+            q[None, None], k[None, None], v[None, None], attn_mask=D[None, None],
+            scale=sc)[0, 0]
+        y.backward(dO.double())
+        m = mask_of(e)
+        dK, dV = oracle.attention_bwd_dkdv(m, Q.numpy(), K.numpy(), V.numpy(), dO.numpy(), sc,
+                                           keys)
+        for name, a, b in (("dK", dK, k.grad), ("dV", dV, v.grad)):
+            ref = b.numpy()[keys]
+            if not np.allclose(a, ref, rtol=0, atol=1e-11):
+                bad.append(f"{name} of keys {keys.tolist()} vs autograd for {e}: "
+                           f"{np.abs(a - ref).max():.3g}")
+        _, fK, fV = _oracle_bwd(m, Q, K, V, dO, sc)
+        if not (np.allclose(dK, fK[keys], rtol=0, atol=1e-12) and
+                np.allclose(dV, fV[keys], rtol=0, atol=1e-12)):
+            bad.append(f"key-subset dK/dV differ from the full evaluation for {e}")
+    return bad
+
+
 # ---------------------------------------------------------------- decode pins
 
 def ring_fill(K, t, cap):
@@ -653,7 +694,8 @@ def check_decode_special():
 
 DECODE_CHECKS = [check_decode_matches_sequence_rows, check_decode_special]
 
-BWD_CHECKS = [check_bwd_autograd, check_bwd_finite_differences, check_bwd_invariants]
+BWD_CHECKS = [check_bwd_autograd, check_bwd_finite_differences, check_bwd_invariants,
+              check_bwd_key_subset]
 
 COUNT_CHECKS = [check_page_counts, check_row_sets, check_reach, check_edge_formula,
                 check_dilated_counts, check_causal_equivalences, check_against_numpy_rules,

@@ -59,6 +59,17 @@ BWD_MUTANTS = {
                            "    a[t] = acc;\n    if (a[t] > mx)"),
     "bwd_dV_to_query_row": ("dV[j * d + k] +=", "dV[i * d + k] +="),
     "bwd_rows_subset_shifted": ("bwd_row(&m, rows[r], d,", "bwd_row(&m, rows[r] / 2, d,"),
+    # the same slips in the key-subset gradient, and ones of its own
+    "bwd_keys_rule_transposed": ("if (!allowed(&m, i, j)) continue;",
+                                 "if (!allowed(&m, j, i)) continue;"),
+    "bwd_keys_D_unweighted": ("D += exp(s[t] - mx) / l * acc;", "D += acc;"),
+    "bwd_keys_dK_no_scale": ("dk[k] += scale * ds *", "dk[k] += ds *"),
+    "bwd_keys_dV_uses_value": ("dv[k] += alpha * load_elem(dO, dtype, i * d + k);",
+                               "dv[k] += alpha * load_elem(V, dtype, i * d + k);"),
+    "bwd_keys_normaliser_of_key_row": ("exp(scale * qk - rmax[i]) / rsum[i];",
+                                       "exp(scale * qk - rmax[j]) / rsum[j];"),
+    "bwd_keys_first_key_rows_missed": ("for (int64_t a = 0; a < n_keys; a++)\n      if (allowed",
+                                       "for (int64_t a = 1; a < n_keys; a++)\n      if (allowed"),
 }
 
 
