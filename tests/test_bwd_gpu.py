@@ -2,9 +2,10 @@
 the GPU) against the fp64 oracle's gradients on the same seeded inputs.
 
 Small and mid-size cases compare every element of every (or of chosen) heads.  At
-the benchmark's full sizes the oracle computes dQ of sampled rows exactly (a row's
-dQ needs only its own allowed set), and dK, dV are checked through identities that
-hold at any size (sums over keys of a softmax over each row's set):
+the benchmark's full sizes the oracle computes dQ of sampled rows and dK, dV of
+sampled keys exactly (a row's dQ needs only its own allowed set; a key's dK, dV need
+the rows that read it), element by element; identities that hold at any size (sums
+over keys of a softmax over each row's set) are checked on every head besides:
   sum_j dV_j = sum_i dO_i,  sum_j dK_j = 0,
   sum_i q_i . dQ_i = sum_j k_j . dK_j,  sum_j v_j . dV_j = sum_i dO_i . O_i.
 """
@@ -94,19 +95,46 @@ def _identities(Q, K, V, dO, res, dtype):
             assert abs(c1 - c2) <= tol * ref, f"v.dV != dO.O in head {(b, h)}: {c1} {c2}"
 
 
-@pytest.mark.parametrize("name", ["t32k_w4096", "t16k_r256_s16_g128", "t32k_w512_d2"])
-def test_full_size_sampled_rows_and_identities(oracle_mod, name):
+def sample_keys(T, p, n, seed):
+    """Keys whose dK/dV the full-size tests check: the sequence ends, tile and window
+    edges, the first strided and global columns (packed columns of the kernels) and
+    the keys of a random block, plus n seeded ones."""
+    keys = set(edge_rows(T, p)[:40])
+    s = p.get("stride", 0)
+    if s:
+        keys.update(range(p.get("offset", 0), min(T, 4 * s), s))
+    g = np.asarray(p.get("global_pos", ()), dtype=np.int64)
+    keys.update(int(x) for x in g[:4])
+    keys.update(int(x) for x in g[-2:])
+    rp = np.asarray(p.get("rand_pairs", ()), dtype=np.int64).reshape(-1, 2)
+    if len(rp):
+        b = p["rand_block"]
+        k0 = int(rp[len(rp) // 2, 1]) * b
+        keys.update({k0, k0 + 1, min(T - 1, k0 + b - 1)})
+    return W.sample_rows(T, n, seed=seed, must=sorted(x for x in keys if 0 <= x < T))
+
+
+@pytest.mark.parametrize("name", ["t32k_w4096", "t16k_r256_s16_g128", "t32k_w512_d2",
+                                  "t4096_bigbird"])
+def test_full_size_sampled_rows_keys_and_identities(oracle_mod, name):
+    """At the benchmark's sizes and launch configuration: dQ of sampled rows and dK, dV
+    of sampled keys element by element against the oracle, and the identities on
+    every head."""
     cfg, p = workload(name)
     B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
     (Q, K, V, dO), _, res, scale = run_bwd(B, H, T, d, p, "bf16", seed=0)
     _identities(Q, K, V, dO, res, "bf16")
-    dq = res[2]
+    dq, dk, dv = res[2], res[3], res[4]
     m = oracle_mask(T, p)
     rows = W.sample_rows(T, 24, seed=5, must=edge_rows(T, p)[:40])
+    keys = sample_keys(T, p, 16, seed=6)
     for (b, h) in [(0, 0), (B - 1, H - 1)]:
-        ref = oracle.attention_bwd_dq(m, host_view(Q[b, h]), host_view(K[b, h]),
-                                      host_view(V[b, h]), host_view(dO[b, h]), scale, rows)
+        args = [host_view(x[b, h]) for x in (Q, K, V, dO)]
+        ref = oracle.attention_bwd_dq(m, *args, scale, rows)
         check_grad("dQ", dq[b, h][rows], ref, "bf16", where=f" head {(b, h)}")
+        rk, rv = oracle.attention_bwd_dkdv(m, *args, scale, keys)
+        check_grad("dK", dk[b, h][keys], rk, "bf16", where=f" head {(b, h)}")
+        check_grad("dV", dv[b, h][keys], rv, "bf16", where=f" head {(b, h)}")
 
 
 def test_identities_fp32_mid_size(oracle_mod):

@@ -92,7 +92,7 @@ def test_t2048_workloads(oracle_mod, name):
 
 
 @pytest.mark.parametrize("name", ["t32k_w4096", "t16k_r256_s16_g128", "t8k_full_causal",
-                                  "t128k_w4096_s1024"])
+                                  "t128k_w4096_s1024", "t4096_bigbird", "t32k_w512_d2"])
 def test_large_workloads_sampled_rows(oracle_mod, name):
     cfg, p = workload(name)
     T = cfg["T"]

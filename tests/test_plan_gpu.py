@@ -2,6 +2,9 @@
 (block, count, class) and the compacted column list must match bit for bit; the
 execution schedule must compute only non-empty tiles and cover every allowed pair
 exactly once."""
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -203,6 +206,42 @@ def test_schedule_covers_each_allowed_pair_once(oracle_mod, k):
             grow = i in set(gpos.tolist())
             got = sorted(covered_keys(sched, cols, T, group_rows, qtile_rows, i, grow, e))
             assert got == m.row_set(i).tolist(), (which, i)
+
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_counts.json")))
+
+
+def _spec(e):
+    return {k: e[k] for k in ("causal", "window", "radius", "stride", "offset", "global_pos")}
+
+
+@pytest.mark.parametrize("k", range(len(GOLDEN["pair_counts"])))
+def test_page_printed_counts_through_gpu_plan(oracle_mod, k):
+    """The pages' own small masks (six tokens with w = 2 and full causal; sixteen
+    tokens full, causal, w = 4, w = 2 + stride 4, radius 2 + global token 0) built by
+    spattn_plan_create: the pair count equals the printed integer, and the tile list
+    equals the oracle's."""
+    e = GOLDEN["pair_counts"][k]
+    plan, _ = check_plan(e["T"], _spec(e))
+    assert plan.info()["pairs_per_head"] == e["pairs"], e["source"]
+
+
+@pytest.mark.parametrize("k", range(len(GOLDEN["row_sets"])))
+def test_page_printed_row_sets_through_gpu_schedule(oracle_mod, k):
+    """The keys the GPU plan's forward schedule lets the printed query read are the
+    printed set (query 12 of the sixteen-token examples, query 0 when global, the
+    sixth of six tokens, token 8000 of an 8192-token window of 512)."""
+    e = GOLDEN["row_sets"][k]
+    T, i = e["T"], e["row"]
+    spec = _spec(e)
+    plan, _ = check_plan(T, spec)
+    want = e["set"] if "set" in e else list(range(e["range"][0], e["range"][1] + 1))
+    spec["global_pos_sorted"] = np.sort(np.asarray(spec["global_pos"], dtype=np.int64))
+    grow = i in set(spec["global_pos"])
+    for which, (group_rows, qtile_rows) in enumerate([(256, 128), (64, 64)]):
+        got = sorted(covered_keys(plan.schedule(which), plan.columns(), T, group_rows,
+                                  qtile_rows, i, grow, spec))
+        assert got == want, (which, e["source"])
 
 
 def test_walk_counter_counts_scheduled_products(oracle_mod):
