@@ -16,6 +16,12 @@ O(E (d_k + d_v)) cost, "Sparse attention", section "When the cost is linear").
 Under torchrun each rank runs its own copy of the workload on its GPU (heads are
 independent; there is no collective on the data path), and value sums over ranks.
 
+At N = 1 the default run also times, after the headline, the other forward workloads
+(the 128K / 8K pair that shows density-proportional cost, the 16K long-document mask,
+the dilated and BigBird masks, and the short 2048- and 512-token configs on the HBM
+roofline) on device-drawn seeded inputs, each with its own clock record, under the
+line's "secondary" key; --no-secondary skips them.
+
 --impl reference times the fp64 CPU oracle (the reference arm of this method) on a
 bounded sample of the same workload, on the host cores: query rows of one head for the
 forward, dQ of sampled rows for --pass bwd, sampled (batch, kv head) groups for --pass
@@ -191,6 +197,89 @@ class StepTimer:
 
     def per_step_ms(self):
         return [a.elapsed_time(b) for a, b in zip(self.t0, self.t1)]
+
+
+# Configurations whose forward is bound by HBM traffic and launch latency rather than the
+# tensor cores (arithmetic intensity below the ridge point): the 512- and 2048-token
+# shapes.  Their roofline is GB/s of algorithmic bytes against the measured HBM bandwidth.
+HBM_BOUND = ("t512_w128_s0", "t512_w128_s64", "t512_full_causal", "t2048_w256_s0",
+             "t2048_w256_s64")
+
+SECONDARY = ["t128k_w4096_s1024", "t8k_full_causal", "t16k_r256_s16_g128", "t32k_w512_d2",
+             "t4096_bigbird", "t2048_w256_s0", "t2048_w256_s64", "t512_w128_s0"]
+
+
+def fwd_algo_bytes(B, H, T, d, elem=2):
+    """Algorithmic bytes of one forward launch: Q, K, V read and O written (d elements
+    each per token per head) plus the fp32 LSE."""
+    return B * H * T * (4 * d * elem + 4)
+
+
+def fwd_roofline(name, cfg, flops, ms, peaks):
+    """(bound, achieved, peak, unit) of a forward step taking `ms`."""
+    if name in HBM_BOUND:
+        gbs = fwd_algo_bytes(cfg["B"], cfg["H"], cfg["T"], cfg["d"]) / (ms / 1e3) / 1e9
+        return "hbm", gbs, peaks["hbm_gbs"], "GB/s"
+    return "tensor", flops / (ms / 1e3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+
+
+def time_secondary(torch, sp, names, steps, warmup, dev, stream):
+    """Time one forward step of each named workload (whole batch, inputs resident, the
+    same per-step CUDA events and L2 rule as the headline), each with its own clocks.
+    Inputs are seeded N(0,1) bf16 drawn on the device (these lines are throughput only;
+    the parity tests use the host-drawn inputs)."""
+    peaks, _ = load_peaks()
+    out = {}
+    for name in names:
+        cfg = W.WORKLOADS[name]
+        p = W.mask_params(name)
+        B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+        g = torch.Generator(device=dev).manual_seed(1)
+        with torch.cuda.stream(stream):
+            q, k, v = (torch.randn(B, H, T, d, generator=g, device=dev, dtype=torch.float32)
+                       .to(torch.bfloat16) for _ in range(3))
+            o = torch.empty_like(q)
+            lse = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+        plan = sp.Plan(T, d, **p, stream=stream)
+        info = plan.info()
+        flops = 4.0 * d * B * H * info["pairs_per_head"]
+        scale = 1.0 / math.sqrt(d)
+
+        def step():
+            sp.fwd(plan, q, k, v, scale, out=o, lse=lse, stream=stream)
+
+        for _ in range(warmup):
+            step()
+        stream.synchronize()
+        timer = StepTimer(torch, dev, stream, steps, 3 * q.numel() * q.element_size(), "Q/K/V")
+        with ClockSampler(dev.index or 0) as clk:
+            torch.cuda.synchronize(dev)
+            timer.run(step)
+            torch.cuda.synchronize(dev)
+        plan.check_device(stream)
+        ms = statistics.mean(timer.per_step_ms())
+        bound, achieved, peak, unit = fwd_roofline(name, cfg, flops, ms, peaks)
+        packing = plan.columns().size > 0 or len(p["global_pos"]) > 0
+        out[name] = {"B": B, "H": H, "T": T, "d": d, "mask": mask_desc(p),
+                     "pairs_per_head": info["pairs_per_head"], "ms_per_step": ms,
+                     "tflops": flops / (ms / 1e3) / 1e12,
+                     "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak,
+                     "step": "k_pack + fwd_tc" if packing else "fwd_tc",
+                     "l2": timer.l2, "clocks": clk.summary()}
+        plan.close()
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    a, b = out.get("t128k_w4096_s1024"), out.get("t8k_full_causal")
+    if a and b:
+        pr = (a["pairs_per_head"] * a["B"] * a["H"]) / (b["pairs_per_head"] * b["B"] * b["H"])
+        ma, mb = a["clocks"]["sm_mhz"], b["clocks"]["sm_mhz"]
+        out["density"] = {
+            "pairs_ratio_128k_over_8k": pr,
+            "time_ratio": a["ms_per_step"] / b["ms_per_step"],
+            "cycles_ratio": (a["ms_per_step"] * ma) / (b["ms_per_step"] * mb) if ma and mb else None,
+            "note": "cycles_ratio = (time x median SM MHz) of the 128K step over the 8K step"}
+    return out
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -464,10 +553,14 @@ def run_ours(args, cfg, p):
     e2e_value = world * flops_step * e2e_steps / e2e_s / 1e12
 
     peaks, peak_src = load_peaks()
-    kernel_ms = statistics.mean(per) if not packing else None
     line = None
+    secondary = None
+    if world == 1 and not args.no_secondary and not args.heads:
+        secondary = time_secondary(torch, sp, [n for n in SECONDARY if n != args.workload],
+                                   args.steps, args.warmup, dev, stream)
     if rank == 0:
-        achieved = flops_step / (kernel_ms / 1e3) / 1e12 if kernel_ms else value / world
+        bound, achieved, peak, r_unit = fwd_roofline(args.workload, cfg, flops_step,
+                                                     statistics.mean(per), peaks)
         traffic = (TRAFFIC["bytes_per_launch"]
                    if TRAFFIC["kernel_sha"] == kernel_sha() and
                    TRAFFIC["workload"] == args.workload and not args.heads else None)
@@ -492,13 +585,15 @@ def run_ours(args, cfg, p):
                        "l2": timer.l2,
                        "plan_build_ms": round(1e3 * t_plan, 2)},
             "pct_of_bf16_peak": 100.0 * (value / world) / peaks["bf16_tflops"],
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": r_unit, "frac": achieved / peak,
                          "traffic": traffic,
-                         "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "kernel": "fwd_tc_kernel<%d>" % d,
-                         "kernel_ms": kernel_ms},
+                         "peak_source": (f"{peak_src} hbm_gbs" if bound == "hbm" else
+                                         f"{peak_src} bf16_tflops (burst)"),
+                         "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                               if bound == "tensor" else None),
+                         "kernel": "fwd_tc_kernel<%d>" % d + (" (with k_pack)" if packing else ""),
+                         "kernel_ms": statistics.mean(per)},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
                     "d2h_bytes_per_step": out_bytes,
                     "api": "spattn_fwd_host (pinned host buffers)"},
@@ -506,6 +601,8 @@ def run_ours(args, cfg, p):
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
+        if secondary is not None:
+            line["secondary"] = secondary
         print(json.dumps(line))
     plan.close()
     if world > 1:
@@ -772,6 +869,8 @@ def main():
                          "one decode step")
     ap.add_argument("--decode-workload", default="decode_b32_w4096",
                     choices=sorted(W.DECODE_WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="time the named workload only (no secondary forward workloads)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (smaller profiling captures; the line then names it)")
     args = ap.parse_args()

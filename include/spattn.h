@@ -314,8 +314,10 @@ spattn_status spattn_fwd_host(const spattn_plan* plan, int32_t B, int32_t H,
  * until the process exits, so the call allocates nothing.  The scratch needed is
  * B*H*(2*n_columns + n_global)*d*element_size bytes; above 16 MiB the call returns
  * SPATTN_ERR_SHAPE and launches nothing.  The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture.  All calls share the array:
+ * the array's device address (cudaGetSymbolAddress, with that device current) and
+ * remembers it with the current CUDA context; a call made in a new context on that
+ * device (after cudaDeviceReset, say) looks it up again.  Make the first call on a
+ * device, and the first after any such reset, before any stream capture.  All calls share the array:
  * calls that may overlap on the GPU (unordered streams) race and give wrong results.
  */
 spattn_status spattn_fwd_static_scratch(const spattn_plan* plan, int32_t B, int32_t H,

@@ -13,11 +13,13 @@
 // that loads the library holds it until the process exits.  In host code its name
 // is only a stand-in for the symbol, not a device address: the first call on each
 // device looks the address up with cudaGetSymbolAddress (with that device current)
-// and caches it; that first call should therefore come before any stream capture.
+// and caches it with the context it belongs to (a call in a new context on that device
+// looks it up again); that first call should therefore come before any stream capture.
 // All calls share the one array and it keeps the last call's contents; nothing in
 // it has to start at zero, because the packing kernel overwrites every byte the
 // forward kernel reads.  Two calls whose work overlaps on the GPU (different
 // streams, no ordering between them) race on the array and give wrong results.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -34,20 +36,48 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
+// The array's device address per device, remembered together with the CUDA context
+// it was looked up in: a new context on the device (after cudaDeviceReset, or when the
+// primary context was released and made again) loads the module afresh, and the
+// array may then sit at another address, so the lookup is repeated.
+struct AddrCache {
+  CUcontext ctx;
+  void* addr;
+};
 std::mutex g_addr_mu;
-void* g_addr[kMaxDevices] = {};
+AddrCache g_addr[kMaxDevices] = {};
 
-// Device address of g_static_scratch on `dev` (the current device), looked up once.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  });
+  return fn;
+}
+
+// Device address of g_static_scratch on `dev` (the current device) in the current
+// context, looked up once per (device, context).
 cudaError_t static_scratch_address(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_addr_mu);
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_addr[dev]) {
+  CUcontext ctx = nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
+  if (!g_addr[dev].addr || g_addr[dev].ctx != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
+    g_addr[dev] = {ctx, p};
   }
-  *out = g_addr[dev];
+  *out = g_addr[dev].addr;
   return cudaSuccess;
 }
 
@@ -96,21 +126,11 @@ extern "C" spattn_status spattn_fwd_static_scratch(const spattn_plan* p, int32_t
                             static_cast<int32_t>(row_bytes), stream);
     if (e != cudaSuccess) return err(SPATTN_ERR_CUDA, cudaGetErrorString(e));
   }
+  // the same launch arguments as spattn_fwd (test hooks and wait budget included),
+  // with the packing scratch in the static array
   spattn::TcArgs a;
-  a.Q = Q;
-  a.K = K;
-  a.V = V;
-  a.Kc = base ? base : K;
-  a.Vc = base ? base + kc_bytes : V;
-  a.Qg = base ? base + 2 * kc_bytes : Q;
-  a.O = O;
-  a.LSE = LSE;
-  a.BH = static_cast<int32_t>(BH);
-  a.scale = scale;
-  a.walk = p->walk_enabled ? p->d_walk : nullptr;
-  a.err = p->d_err;
-  a.wait_budget_cycles = p->wait_budget_cycles;
-  spattn::select_schedule(p, dtype == SPATTN_BF16, &a);
+  spattn::fill_fwd_args(p, dtype == SPATTN_BF16, BH, Q, K, V, base, base ? base + kc_bytes : nullptr,
+                        base ? base + 2 * kc_bytes : nullptr, O, LSE, scale, &a);
   cudaError_t e;
   if (dtype == SPATTN_BF16) {
     const char* why = "";

@@ -307,6 +307,13 @@ cudaError_t launch_kv_append(bool bf16, void* Kc, void* Vc, const void* kn, cons
 // spattn_api.cu: schedule, mask view and column data a forward launch of `dtype` uses.
 void select_schedule(const spattn_plan* p, bool bf16, TcArgs* a);
 
+// spattn_api.cu: every field of a forward launch's arguments from the plan, the
+// caller's buffers and the packing scratch (Kc, Vc, Qg; NULL when nothing is packed),
+// the schedule included.  Both forward entry points fill their launches with it.
+void fill_fwd_args(const spattn_plan* p, bool bf16, int64_t BH, const void* Q, const void* K,
+                   const void* V, void* Kc, void* Vc, void* Qg, void* O, float* LSE, float scale,
+                   TcArgs* a);
+
 // spattn_api.cu: set the calling thread's spattn_last_error() message.
 void set_last_error(const char* msg);
 

@@ -384,6 +384,27 @@ void spattn::select_schedule(const spattn_plan* p, bool bf16, TcArgs* a) {
   a->dview = view ? p->dview : 1;
 }
 
+void spattn::fill_fwd_args(const spattn_plan* p, bool bf16, int64_t BH, const void* Q,
+                           const void* K, const void* V, void* Kc, void* Vc, void* Qg, void* O,
+                           float* LSE, float scale, TcArgs* a) {
+  a->Q = Q;
+  a->K = K;
+  a->V = V;
+  a->Kc = Kc ? Kc : K;
+  a->Vc = Vc ? Vc : V;
+  a->Qg = Qg ? Qg : Q;
+  a->O = O;
+  a->LSE = LSE;
+  a->BH = static_cast<int32_t>(BH);
+  a->n_cols = p->n_cols;
+  a->scale = scale;
+  a->walk = p->walk_enabled ? p->d_walk : nullptr;
+  a->err = p->d_err;
+  a->wait_budget_cycles = p->wait_budget_cycles;
+  a->inject_timeout = p->inject_timeout;
+  select_schedule(p, bf16, a);
+}
+
 extern "C" {
 
 const char* spattn_last_error(void) { return g_last_error.c_str(); }
@@ -770,22 +791,7 @@ spattn_status spattn_fwd(const spattn_plan* cp, int32_t B, int32_t H, spattn_dty
                                  static_cast<int32_t>(ng), BH, p->T, static_cast<int32_t>(row_bytes),
                                  stream));
   spattn::TcArgs a;
-  a.Q = Q;
-  a.K = K;
-  a.V = V;
-  a.Kc = Kc ? Kc : K;
-  a.Vc = Vc ? Vc : V;
-  a.Qg = Qg ? Qg : Q;
-  a.O = O;
-  a.LSE = LSE;
-  a.BH = static_cast<int32_t>(BH);
-  a.n_cols = p->n_cols;
-  a.scale = scale;
-  a.walk = p->walk_enabled ? p->d_walk : nullptr;
-  a.err = p->d_err;
-  a.wait_budget_cycles = p->wait_budget_cycles;
-  a.inject_timeout = p->inject_timeout;
-  spattn::select_schedule(p, dtype == SPATTN_BF16, &a);
+  spattn::fill_fwd_args(p, dtype == SPATTN_BF16, BH, Q, K, V, Kc, Vc, Qg, O, LSE, scale, &a);
   if (dtype == SPATTN_BF16) {
     const char* why = "";
     cudaError_t e = spattn::launch_fwd_tc(p->d, a, stream, &why);

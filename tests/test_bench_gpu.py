@@ -48,17 +48,42 @@ def _check_common(line, steps):
 
 def test_forward_line():
     line = _run("--workload", "t2048_w256_s64", "--steps", "4", "--warmup", "3",
-                "--cpu-budget", "2")
+                "--cpu-budget", "2", "--no-secondary")
     _check_common(line, 4)
     c = line["config"]
     flops = 4.0 * c["d"] * c["B"] * c["H"] * c["pairs_per_head"]
     assert line["value"] == pytest.approx(flops / (line["ms_per_step"] / 1e3) / 1e12, rel=1e-6)
-    assert line["roofline"]["bound"] == "tensor"
+    # a 2048-token step is bound by HBM traffic: GB/s of Q, K, V, O and LSE bytes
+    roof = line["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    algo = c["B"] * c["H"] * c["T"] * (4 * c["d"] * 2 + 4)
+    assert roof["achieved"] == pytest.approx(algo / (line["ms_per_step"] / 1e3) / 1e9, rel=1e-6)
+    assert "secondary" not in line
     # inputs in, output and LSE out: bf16 q, k, v and O, fp32 LSE
     elems = c["B"] * c["H"] * c["T"] * c["d"]
     assert line["e2e"]["h2d_bytes_per_step"] == 3 * 2 * elems
     cpu = line["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["cores"] >= 1 and cpu["sample"]
+
+
+def test_forward_line_secondary_workloads():
+    """The default forward run also times the other workloads, each with its own clocks,
+    and compares the 128K / 8K cost ratio with their pair ratio."""
+    line = _run("--workload", "t512_w128_s64", "--steps", "3", "--warmup", "3",
+                "--no-cpu-baseline")
+    sec = line["secondary"]
+    for name in ["t128k_w4096_s1024", "t8k_full_causal", "t16k_r256_s16_g128",
+                 "t2048_w256_s0", "t4096_bigbird", "t32k_w512_d2"]:
+        e = sec[name]
+        assert e["ms_per_step"] > 0 and 0 < e["frac"] == pytest.approx(e["achieved"] / e["peak"])
+        assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(e["clocks"])
+        flops = 4.0 * e["d"] * e["B"] * e["H"] * e["pairs_per_head"]
+        assert e["tflops"] == pytest.approx(flops / (e["ms_per_step"] / 1e3) / 1e12, rel=1e-6)
+    assert sec["t2048_w256_s0"]["bound"] == "hbm" and sec["t16k_r256_s16_g128"]["bound"] == "tensor"
+    dens = sec["density"]
+    assert dens["pairs_ratio_128k_over_8k"] == pytest.approx(536_420_352 / 33_558_528)
+    # density-proportional cost: the 128K step costs about its pair ratio in SM cycles
+    assert 0.5 * dens["pairs_ratio_128k_over_8k"] < dens["cycles_ratio"] < 2 * dens["pairs_ratio_128k_over_8k"]
 
 
 def test_backward_line():

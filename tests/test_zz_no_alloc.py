@@ -56,6 +56,51 @@ def test_static_scratch_matches_allocating_entry(name, dtype):
         close(o, o_ref, l, l_ref, dtype)
 
 
+def test_queued_calls_with_different_plans_each_finish_correctly():
+    """Two static-scratch calls with different plans and shapes queued on one stream
+    before a single sync: the second call's packing overwrites the shared array only
+    after the first call's kernels have read it (stream order), so both outputs match
+    spattn_fwd."""
+    runs = []
+    for name, seed in (("t16k_r256_s16_g128", 21), ("t512_w128_s64", 22)):
+        cfg = W.WORKLOADS[name]
+        B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+        plan = sp.Plan(T, d, **W.mask_params(name))
+        q, k, v = (x.cuda() for x in W.qkv(B, H, T, d, seed, torch.bfloat16))
+        runs.append((plan, q, k, v, 1.0 / math.sqrt(d)))
+    torch.cuda.synchronize()
+    outs = [sp.fwd_static_scratch(plan, q, k, v, sc) for plan, q, k, v, sc in runs]
+    torch.cuda.synchronize()
+    for (plan, q, k, v, sc), (o, l) in zip(runs, outs):
+        plan.check_device()
+        o_ref, l_ref = sp.fwd(plan, q, k, v, sc)
+        torch.cuda.synchronize()
+        close(o, o_ref, l, l_ref, torch.bfloat16)
+
+
+def test_wait_timeout_is_reported_through_this_entry():
+    """The plan's device-wait test hook and budget apply to this entry point too: a
+    wait that runs out is reported as SPATTN_ERR_TIMEOUT, and the next call is right."""
+    name = "t512_w128_s64"
+    cfg = W.WORKLOADS[name]
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    plan = sp.Plan(T, d, **W.mask_params(name))
+    q, k, v = (x.cuda() for x in W.qkv(B, H, T, d, 31, torch.bfloat16))
+    plan.set_wait_budget(200_000)
+    plan.test_wait_timeout(True)
+    sp.fwd_static_scratch(plan, q, k, v, 0.125)
+    with pytest.raises(sp.SpattnError) as ei:
+        plan.check_device()
+    assert ei.value.status == sp.ERR_TIMEOUT
+    plan.test_wait_timeout(False)
+    plan.set_wait_budget(8_000_000_000)
+    o, l = sp.fwd_static_scratch(plan, q, k, v, 0.125)
+    o_ref, l_ref = sp.fwd(plan, q, k, v, 0.125)
+    torch.cuda.synchronize()
+    plan.check_device()
+    close(o, o_ref, l, l_ref, torch.bfloat16)
+
+
 def test_oversize_request_is_rejected():
     # T=16384, stride 16: 1024 packed columns; d=128, B*H=64 bf16 needs
     # 64 * 2 * 1024 * 256 B = 32 MiB > 16 MiB
