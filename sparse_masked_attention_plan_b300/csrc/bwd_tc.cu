@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::kBarQ), 1);
     mbar_init(BAR(C::kBarS + 0), 1);
     mbar_init(BAR(C::kBarS + 1), 1);
-    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 128);
+    // chunk hand-off: one arrival per warp of the warpgroup (128 arrivals on one
+    // barrier word would serialise on the critical path)
+    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 4);
     mbar_init(BAR(C::kBarDone), 1);
     fence_barrier_init();
   }
@@ -372,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(lane_base + 128 * h + 16 * qq, pk);  // over this half's own S
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
+        __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
+        if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
       }
       }
       ++n_done;
@@ -594,9 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::kBarS + 0), 1);
     mbar_init(BAR(C::kBarS + 1), 1);
-    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 128);
+    // one arrival per warp of the warpgroup on the chunk hand-off and on the per-query
+    // vector exchange
+    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 4);
     mbar_init(BAR(C::kBarDone), 1);
-    for (int k = 0; k < 4; ++k) mbar_init(BAR(C::kBarVec + k), 128);
+    for (int k = 0; k < 4; ++k) mbar_init(BAR(C::kBarVec + k), 4);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -776,7 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_lse[kk] = lse_cur;
         s_dd[kk] = dd_cur;
       }
-      mbar_arrive(BAR(C::kBarVec + wg * 2 + (n & 1)));
+      __syncwarp();  // this warp's LSE and D values are written before lane 0 arrives
+      if (lane == 0) mbar_arrive(BAR(C::kBarVec + wg * 2 + (n & 1)));
       if (kk < 64 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next);
       if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + wg * 2 + (n & 1)), (n >> 1) & 1,
                                              p.budget, p.err, kErrTimeout)))
@@ -829,7 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(lane_base + 128 * hh + 64 + 16 * qq, pg);  // over this half's own dP^T
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(BAR(C::kBarP + q));  // queries 32q .. 32q+31 of P^T and dS^T are in TMEM
+        __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
+        if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // queries 32q .. 32q+31 of P^T and dS^T are in TMEM
       }
       }
       ++n_done;

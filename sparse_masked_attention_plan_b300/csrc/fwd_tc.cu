@@ -173,12 +173,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::kBarQ), 1);
     mbar_init(BAR(C::kBarS + 0), 1);
     mbar_init(BAR(C::kBarS + 1), 1);
-    mbar_init(BAR(C::kBarP + 0), 128);
-    mbar_init(BAR(C::kBarP + 1), 128);
+    // p_full and s_free: one arrival per softmax warp (a single arrive per warp keeps the
+    // hand-off off the critical path: 128 arrivals on one barrier word serialise)
+    mbar_init(BAR(C::kBarP + 0), 4);
+    mbar_init(BAR(C::kBarP + 1), 4);
     mbar_init(BAR(C::kBarO), 1);
     mbar_init(BAR(C::kBarNever), 1);
-    mbar_init(BAR(C::kBarSfree + 0), 128);
-    mbar_init(BAR(C::kBarSfree + 1), 128);
+    mbar_init(BAR(C::kBarSfree + 0), 4);
+    mbar_init(BAR(C::kBarSfree + 1), 4);
     mbar_init(BAR(C::kBarPVdone + 0), 1);
     mbar_init(BAR(C::kBarPVdone + 1), 1);
     fence_barrier_init();
@@ -459,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld128(lane_base + colS, sr);
       if constexpr (C::kSepP) {  // S_t is in registers: the next S_t may overwrite it
         tc_fence_before();
-        mbar_arrive(BAR(C::kBarSfree + wg));
+        __syncwarp();  // every lane's load is complete before lane 0 arrives for the warp
+        if (lane == 0) mbar_arrive(BAR(C::kBarSfree + wg));
       }
       if (!(e.y & (kFull0 << wg))) {
         uint32_t w[4];
@@ -534,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(BAR(C::kBarP + wg));
+      __syncwarp();  // every lane's P and O stores are complete before lane 0 arrives
+      if (lane == 0) mbar_arrive(BAR(C::kBarP + wg));
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
