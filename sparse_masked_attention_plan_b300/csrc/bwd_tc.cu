@@ -138,12 +138,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rank = (blockIdx.x / p.BH) >> 1;
   const int t = (blockIdx.x / p.BH) & 1;
   const int4 item = p.items[rank];
-  const int n_ent = item.z;
+  // a split item of the forward schedule (both query tiles hold the same global rows,
+  // alternate key tiles): the tile-0 CTA takes every entry of it, the tile-1 CTA nothing
+  const bool split = (item.w & kItemSplit) != 0;
+  const bool idle = split && t == 1;
+  const int n_ent = idle ? 0 : item.z;
   const int4* ents = p.entries + item.y;
   const bool gathered = (item.w & kItemGathered) != 0;
   const MaskDev& m = p.mask;
-  const int qrow0 = item.x + t * kTile;  // first row (or gathered index) of the tile
-  const int active_bit = kActive0 << t, full_bit = kFull0 << t;
+  const int qrow0 = item.x + (split ? 0 : t * kTile);  // first row (or gathered index) of the tile
+  const int active_bit = split ? (kActive0 | kActive1) : kActive0 << t;
+  const int full_bit = split ? (kFull0 | kFull1) : kFull0 << t;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
-    const bool write = valid && (gathered || !m.rowglobal[i]);
+    const bool write = !idle && valid && (gathered || !m.rowglobal[i]);
     bool have = false;
     if (n_done > 0) {
       have = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarDone), 0, p.budget, p.err, kErrTimeout));

@@ -68,7 +68,9 @@ struct TcCfg {
                        kBarO = 2 * kStages + 5, kBarNever = 2 * kStages + 6,
                        kBarSfree = 2 * kStages + 7, kBarPVdone = 2 * kStages + 9,
                        kNumBars = 2 * kStages + 11;
-  static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
+  // split items: the two query tiles' row maxima and sums, [tile][2][row] fp32
+  static constexpr int kSmemX = 2 * 2 * kTile * 4;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + kSmemX + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
   // d = 128: S_t [128t, 128t+128), P_t over the first 64 columns of S_t, O_t at 256 + d t.
@@ -134,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_addr(smem);
   const uint32_t sKV = sQ + C::kSmemQ;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemQ + C::kSmemKV);
+  float* xch = reinterpret_cast<float*>(smem + C::kSmemQ + C::kSmemKV);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemQ + C::kSmemKV + C::kSmemX);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   const uint32_t bar0 = smem_addr(bars);
 #define BAR(k) (bar0 + 8u * static_cast<uint32_t>(k))
@@ -163,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_ent = item.z;
   const int4* ents = p.entries + item.y;
   const bool gathered = (item.w & kItemGathered) != 0;
+  const bool split = (item.w & kItemSplit) != 0;  // both tiles hold the same rows
   const MaskDev& m = p.mask;
 
   if (threadIdx.x == 0) {
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(sQ + t * C::kTileBytes + c * C::kChunkBytes, mapQ, BAR(C::kBarQ), c * 64,
-                      res, item.x + t * kTile, bh);
+                      res, item.x + (split ? 0 : t * kTile), bh);
     }
     __syncwarp();
     int issued = 0;
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t colS = wg ? C::kColS1 : C::kColS0, colO = wg ? C::kColO1 : C::kColO0;
     const uint32_t colP = wg ? C::kColP1 : C::kColP0;
     uint32_t pvph = 0;  // d = 64: phase of this tile's pv_done
-    const int local = wg * kTile + r;
+    const int local = (split ? 0 : wg * kTile) + r;
     int i;
     bool valid;
     if (gathered) {
@@ -542,7 +546,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
-    if (n_done > 0) {
+    if (split) {
+      // both tiles walked alternate key tiles for the same rows: merge the two partial
+      // states, m = max(m0, m1), l = l0 2^(m0 - m) + l1 2^(m1 - m), O likewise; tile t's
+      // thread of row r writes columns t d / 2 .. of the row (both O_t are in its lanes)
+      xch[wg * 2 * kTile + r] = mrow;
+      xch[wg * 2 * kTile + kTile + r] = lrow;
+      bar_sync(1, 256);
+      const float m0 = xch[r], l0 = xch[kTile + r];
+      const float m1 = xch[2 * kTile + r], l1 = xch[3 * kTile + r];
+      const float mm = fmaxf(m0, m1);
+      const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mm);
+      const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mm);
+      const float lsum = l0 * a0 + l1 * a1;
+      const bool got = mbar_wait(BAR(C::kBarO), 0, p.budget, p.err, kErrTimeout);
+      if (__all_sync(0xffffffffu, got)) {
+        tc_fence_after();
+        const bool write = valid;
+        const float inv = (write && lsum > 0.f) ? 1.f / lsum : 0.f;
+        const float w0 = a0 * inv, w1 = a1 * inv;
+        const size_t row = static_cast<size_t>(bh) * p.T_out + static_cast<size_t>(i) * p.dview + res;
+        uint4* dst = reinterpret_cast<uint4*>(p.O + row * D + wg * (D / 2));
+#pragma unroll
+        for (int q = 0; q < D / 64; ++q) {
+          const uint32_t c = wg * (D / 2) + 32 * q;
+          uint32_t o0[32], o1[32];
+          tmem_ld32(lane_base + C::kColO0 + c, o0);
+          tmem_ld32(lane_base + C::kColO1 + c, o1);
+          if (write) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              float f[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                f[k] = __uint_as_float(o0[8 * v4 + k]) * w0 + __uint_as_float(o1[8 * v4 + k]) * w1;
+              uint4 w;
+              w.x = pack_bf16x2(f[0], f[1]);
+              w.y = pack_bf16x2(f[2], f[3]);
+              w.z = pack_bf16x2(f[4], f[5]);
+              w.w = pack_bf16x2(f[6], f[7]);
+              dst[4 * q + v4] = w;
+            }
+          }
+        }
+        if (write && wg == 0 && p.LSE) p.LSE[row] = (mm + log2f(lsum)) * 0.69314718055994531f;
+      }
+    } else if (n_done > 0) {
       const bool got = mbar_wait(BAR(C::kBarO), 0, p.budget, p.err, kErrTimeout);
       if (__all_sync(0xffffffffu, got)) {
         tc_fence_after();

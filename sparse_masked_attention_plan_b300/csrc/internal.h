@@ -15,6 +15,10 @@ constexpr int kActive0 = 1, kActive1 = 2, kFull0 = 4, kFull1 = 8;
 constexpr int kKindShift = 4;
 constexpr int kKindBand = 0, kKindPacked = 1, kKindDense = 2, kKindRandom = 3;
 constexpr int kItemGathered = 1;
+// A gathered item whose global rows fit in one query tile: both query tiles hold the
+// same rows and walk alternate key tiles (entry n is active for tile n % 2 only); the
+// two partial softmax states are merged at the end.
+constexpr int kItemSplit = 2;
 
 // Key-major (backward) schedule: a unit is 64 consecutive keys, either natural key
 // rows (k0 .. k0+63) or packed sparse columns (C[c0] .. C[c0+63]); its entries are

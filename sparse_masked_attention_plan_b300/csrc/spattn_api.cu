@@ -222,19 +222,24 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
     const int32_t cnt = static_cast<int32_t>(s->entries.size() / 4) - off;
     if (cnt > 0) items.push_back({static_cast<int32_t>(r0), off, cnt, 0});
   }
-  // global rows: every key that causality permits
+  // global rows: every key that causality permits.  A group whose rows fit in one
+  // query tile is split (d = 64 only, where the kernel's separate P columns let the two
+  // query tiles overlap): both tiles hold its rows and take alternate key tiles, so the
+  // dense walk that every global row needs runs at two tiles per entry pair.
   const int64_t ng = static_cast<int64_t>(p->gpos.size());
   for (int64_t q0 = 0; q0 < ng; q0 += group_rows) {
     const int32_t off = static_cast<int32_t>(s->entries.size() / 4);
     const int64_t last = p->gpos[std::min<int64_t>(q0 + group_rows, ng) - 1];
     const int64_t kb_hi = (p->causal ? last : T - 1) / kTile;
+    const bool split = n_qtiles == 2 && p->d == 64 && ng - q0 <= qtile_rows && kb_hi >= 1;
     for (int64_t kb = 0; kb <= kb_hi; ++kb) {
       const int64_t k0 = kb * kTile, k1 = std::min<int64_t>(k0 + kTile, T) - 1;
       const bool ragged = k0 + kTile > T;
       int32_t flags = kKindDense << kKindShift;
       for (int t = 0; t < n_qtiles; ++t) {
-        const int64_t a = q0 + int64_t(t) * qtile_rows;
+        const int64_t a = q0 + (split ? 0 : int64_t(t) * qtile_rows);
         if (a >= ng) continue;
+        if (split && t != (kb & 1)) continue;
         const int64_t b = std::min<int64_t>(a + qtile_rows, ng) - 1;
         const int64_t rmin = p->gpos[a], rmax = p->gpos[b];
         if (p->causal && k0 > rmax) continue;
@@ -244,7 +249,8 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
       if (flags & (kActive0 | kActive1)) push(static_cast<int32_t>(k0), flags, static_cast<int32_t>(kb), 0);
     }
     const int32_t cnt = static_cast<int32_t>(s->entries.size() / 4) - off;
-    if (cnt > 0) items.push_back({static_cast<int32_t>(q0), off, cnt, kItemGathered});
+    if (cnt > 0)
+      items.push_back({static_cast<int32_t>(q0), off, cnt, kItemGathered | (split ? kItemSplit : 0)});
   }
   if (longest_first)
     std::stable_sort(items.begin(), items.end(),
