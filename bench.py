@@ -5,7 +5,7 @@
 
 --pass fwd (default) is the headline described below.  --pass bwd times one spattn_bwd
 over the whole batch (10 d pairs flops per step, against the bf16 peak); --pass decode
-times one generation step (ring-buffer append + decode) and reports GB/s of cached K/V
+times one generation step (ring-buffer append + decode, spattn_decode_append) and reports GB/s of cached K/V
 read per step against the measured HBM bandwidth; its timed steps are captured once into a
 CUDA graph and replayed (each step still appends, decodes at its own position and merges).
 
@@ -765,9 +765,8 @@ def run_decode(args):
     step_bytes = kv_bytes + (2 * q.numel() + 2 * kn.numel()) * 2 + lse.numel() * 4
     scale = 1.0 / math.sqrt(d)
 
-    def step(s):
-        c.append(kn, vn, pos_all[s], stream=stream)
-        c.step(q, pos_all[s], scale, out=out, lse=lse, stream=stream)
+    def step(s):  # append the step's rows and decode, one call (two launches for bf16)
+        c.append_step(kn, vn, q, pos_all[s], scale, out=out, lse=lse, stream=stream)
 
     for s in range(args.warmup):
         step(s)
@@ -775,7 +774,8 @@ def run_decode(args):
     c.check(stream)
     # The timed steps run as one captured CUDA graph, the way a generation loop
     # launches its steps: every step still appends its rows, decodes at its own
-    # position and merges the splits (three kernels), with no host work in between.
+    # position and merges the splits (two kernels: the decode kernel appends), with no
+    # host work in between.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for s in range(args.steps):
@@ -838,13 +838,14 @@ def run_decode(args):
                                      else None),
                          "traffic_kernel": "decode_mma_kernel",
                          "peak_source": f"{src} hbm_gbs",
-                         "kernel": "kv_append + decode + combine (whole step)",
+                         "kernel": "decode (with the append) + combine (whole step)",
                          "kernel_ms": step_ms},
             "e2e": {"value": e2e, "unit": "GB/s",
                     "h2d_bytes_per_step": (q.numel() + 2 * kn.numel()) * 2,
                     "d2h_bytes_per_step": out.numel() * 2,
-                    "api": "DecodeCache.append/step with pinned host q/k/v and output"},
-            "gpu_launches": 3 * args.steps,
+                    "api": "DecodeCache.append_step (spattn_decode_append) with pinned host "
+                           "q/k/v and output"},
+            "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line))

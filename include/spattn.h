@@ -285,6 +285,23 @@ spattn_status spattn_decode(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap, int
                             float scale, void* out, float* lse, void* workspace,
                             size_t workspace_bytes, void* cuda_stream);
 
+/* spattn_kv_append followed by spattn_decode, as one step: k_new, v_new ([B][Hkv]
+ * [head_dim], 16-byte aligned, the dtype of the cache) are written to slot pos[b] % cap
+ * and the step's query reads them, as the token reads itself ("Sparse and
+ * sliding-window attention", section "Sliding window attention": position t reads
+ * t - W + 1 .. t, with the cache capped at W).  For bf16 the decode kernel does the
+ * append (the CTA that reads slot pos[b] % cap writes the rows to the cache and uses
+ * them directly), so a step is two launches (decode, merge) instead of three; the
+ * results are identical to the two calls.  For fp32 it launches the append kernel
+ * first.  Same arguments, layouts, workspace and errors as spattn_decode, plus NULL /
+ * ALIGN for k_new and v_new. */
+spattn_status spattn_decode_append(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap,
+                                   int64_t window, int32_t head_dim, spattn_dtype dtype,
+                                   const void* q, void* K_cache, void* V_cache,
+                                   const void* k_new, const void* v_new, const int64_t* pos,
+                                   float scale, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* cuda_stream);
+
 /* Synchronise cuda_stream, then report (and clear) the decode workspace's error word:
  * SPATTN_ERR_TIMEOUT if a device-side wait ran out, else SPATTN_OK. */
 spattn_status spattn_decode_check(void* workspace, void* cuda_stream);

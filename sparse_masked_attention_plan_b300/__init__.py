@@ -29,7 +29,8 @@ EXPORTS = ("spattn_mask_validate", "spattn_plan_create", "spattn_plan_info",
            "spattn_plan_copy_tiles", "spattn_plan_copy_columns", "spattn_plan_copy_schedule",
            "spattn_plan_set_walk_counter", "spattn_plan_walk_count", "spattn_fwd",
            "spattn_bwd", "spattn_kv_append", "spattn_decode_workspace_bytes",
-           "spattn_decode", "spattn_decode_check", "spattn_fwd_host", "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
+           "spattn_decode", "spattn_decode_append", "spattn_decode_check", "spattn_fwd_host",
+           "spattn_fwd_static_scratch", "spattn_plan_set_wait_budget",
            "spattn_plan_test_wait_timeout", "spattn_plan_check_device", "spattn_plan_destroy",
            "spattn_last_error", "spattn_version")
 
@@ -95,6 +96,11 @@ def lib():
                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                         ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
                                         _vp, _vp, ctypes.c_size_t, _vp]
+            L.spattn_decode_append.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                               ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                               ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t,
+                                               _vp]
             L.spattn_decode_check.argtypes = [_vp, _vp]
             L.spattn_bwd.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, _vp,
                                      _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
@@ -329,6 +335,21 @@ class DecodeCache:
                                    self.V.data_ptr(), pos.data_ptr(), float(scale),
                                    out.data_ptr(), lse.data_ptr(), self.workspace.data_ptr(),
                                    self.workspace.numel(), _stream_handle(stream)))
+        return out, lse
+
+    def append_step(self, k_new, v_new, q, pos, scale, out=None, lse=None, stream=None):
+        """append(k_new, v_new, pos) then step(q, pos, scale) as one call
+        (spattn_decode_append).  Returns (out, lse)."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=q.device)
+        _check(lib().spattn_decode_append(
+            self.B, self.Hq, self.Hkv, self.cap, self.window, self.d, _dtype_code(q),
+            q.data_ptr(), self.K.data_ptr(), self.V.data_ptr(), k_new.data_ptr(),
+            v_new.data_ptr(), pos.data_ptr(), float(scale), out.data_ptr(), lse.data_ptr(),
+            self.workspace.data_ptr(), self.workspace.numel(), _stream_handle(stream)))
         return out, lse
 
     def check(self, stream=None):

@@ -82,6 +82,8 @@ struct DecParams {
   float* lse;       // [B][Hq] or null
   float* part;      // [B*Hq][nsplit][D + 2]: unnormalised output, max (log2 units), sum
   int* err;
+  const void* kn;   // [B][Hkv][D] the step's own key/value rows to append first, or null
+  const void* vn;
   int32_t B, Hq, Hkv, G, nsplit;
   int64_t cap, window, span;
   float scale;
@@ -384,6 +386,25 @@ __global__ void __launch_bounds__(kMmaThreads)
   const Ranges rg = valid_ranges(t, p.cap, p.window, lo, min(p.cap, lo + p.span));
   int n_sub = 0;
   for (int k = 0; k < rg.n; ++k) n_sub += static_cast<int>((rg.b[k] - rg.a[k] + kSub - 1) / kSub);
+  // With the step's own rows given (spattn_decode_append), the CTA whose slot range
+  // holds slot t % cap appends them: it writes them to the cache for later steps and
+  // puts them into its shared tile of that slot after the copy has landed, so this step
+  // reads them without waiting for the global write.  No other CTA reads that slot.
+  const int64_t s_new = (p.kn && t >= 0) ? t % p.cap : -1;
+  const bool owner = s_new >= lo && s_new < min(p.cap, lo + p.span);
+  const uint4* kn_row = owner ? reinterpret_cast<const uint4*>(
+                                    static_cast<const __nv_bfloat16*>(p.kn) + static_cast<int64_t>(bk) * D)
+                              : nullptr;
+  const uint4* vn_row = owner ? reinterpret_cast<const uint4*>(
+                                    static_cast<const __nv_bfloat16*>(p.vn) + static_cast<int64_t>(bk) * D)
+                              : nullptr;
+  if (owner && threadIdx.x >= 64 && threadIdx.x < 64 + 2 * (D / 8)) {  // warps 2-3: global rows
+    const int c = threadIdx.x - 64;  // 16-byte chunk c % (D / 8) of K (c < D / 8) or V
+    const int64_t off = (static_cast<int64_t>(bk) * p.cap + s_new) * D;
+    uint4* dst = reinterpret_cast<uint4*>(
+        const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(c < D / 8 ? p.Kc : p.Vc)) + off);
+    dst[c % (D / 8)] = (c < D / 8 ? kn_row : vn_row)[c % (D / 8)];
+  }
 
   // thread 0 copies sub-chunk o: 64 rows from its first slot, K then V, one box per 64
   // columns (rows past the slot range are read too, and masked; past cap they are zero)
@@ -456,6 +477,20 @@ __global__ void __launch_bounds__(kMmaThreads)
     int64_t s0;
     int rows;
     sub_chunk(rg, sc, s0, rows);
+    if (owner && s_new >= s0 && s_new < s0 + rows && (s_new - s0) / 16 == warp) {
+      // this warp's rows hold the appended slot: the step's own K and V rows replace
+      // whatever the copy read there (lane l: 16-byte chunk l % (D / 8) of K or V)
+      const int r = static_cast<int>(s_new - s0);
+      uint8_t* blk = smem + st * Cfg::kStageBytes;
+      for (int x = lane; x < 2 * (D / 8); x += 32) {
+        const int c = x % (D / 8);
+        uint8_t* tile = blk + (x < D / 8 ? 0 : Cfg::kTensorBytes);
+        *reinterpret_cast<uint4*>(tile + (c >> 3) * Cfg::kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+            (x < D / 8 ? kn_row : vn_row)[c];
+      }
+      fence_proxy_async_smem();  // ordered before the copies that later refill the stage
+      __syncwarp();
+    }
     if (k0 < rows) {  // (slot k0 valid: every max below is finite)
       const uint32_t kst = s0addr + st * Cfg::kStageBytes, vst = kst + Cfg::kTensorBytes;
       if (k0 + 16 > rows) {
@@ -718,6 +753,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   p.window = a.window;
   p.span = decode_span(a.cap, a.nsplit);
   p.scale = a.scale;
+  p.kn = a.kn;
+  p.vn = a.vn;
   if (a.bf16) {
     if (a.d == 64) return launch_decode_typed<__nv_bfloat16, 64>(p, st);
     if (a.d == 128) return launch_decode_typed<__nv_bfloat16, 128>(p, st);

@@ -301,6 +301,8 @@ struct DecodeArgs {
   int32_t B, Hq, Hkv, d, nsplit, bf16;
   int64_t cap, window;
   float scale;
+  const void* kn = nullptr;  // bf16 only: the step's own rows, appended by the kernel
+  const void* vn = nullptr;
 };
 int decode_splits(int64_t B, int64_t Hkv, int64_t cap);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);

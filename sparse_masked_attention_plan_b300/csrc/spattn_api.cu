@@ -1039,6 +1039,60 @@ spattn_status spattn_decode(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap, int
   return SPATTN_OK;
 }
 
+spattn_status spattn_decode_append(int32_t B, int32_t Hq, int32_t Hkv, int64_t cap,
+                                   int64_t window, int32_t head_dim, spattn_dtype dtype,
+                                   const void* q, void* Kc, void* Vc, const void* k_new,
+                                   const void* v_new, const int64_t* pos, float scale, void* out,
+                                   float* lse, void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream) {
+  spattn_status st = decode_shape(B, Hq, Hkv, cap, window, head_dim, dtype);
+  if (st != SPATTN_OK) return st;
+  if ((st = check_ptr(q, "q")) || (st = check_ptr(Kc, "K_cache")) ||
+      (st = check_ptr(Vc, "V_cache")) || (st = check_ptr(out, "out")) ||
+      (st = check_ptr(workspace, "workspace")) || (st = check_ptr(k_new, "k_new")) ||
+      (st = check_ptr(v_new, "v_new")))
+    return st;
+  if (!pos) return fail(SPATTN_ERR_NULL, "pos is NULL");
+  if (reinterpret_cast<uintptr_t>(pos) % 8) return fail(SPATTN_ERR_ALIGN, "pos misaligned");
+  if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return fail(SPATTN_ERR_ALIGN, "lse misaligned");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(SPATTN_ERR_INVALID_SPEC, "scale must be positive and finite");
+  size_t need = 0;
+  spattn_decode_workspace_bytes(B, Hq, Hkv, cap, head_dim, &need);
+  if (workspace_bytes < need)
+    return fail(SPATTN_ERR_SHAPE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  spattn::DecodeArgs a;
+  a.q = q;
+  a.Kc = Kc;
+  a.Vc = Vc;
+  a.pos = pos;
+  a.out = out;
+  a.lse = lse;
+  a.err = static_cast<int*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kDecodeHeader);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = head_dim;
+  a.nsplit = spattn::decode_splits(B, Hkv, cap);
+  a.bf16 = dtype == SPATTN_BF16;
+  a.cap = cap;
+  a.window = window ? window : cap;
+  a.scale = scale;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = cudaSuccess;
+  if (a.bf16) {  // the decode kernel appends the rows itself
+    a.kn = k_new;
+    a.vn = v_new;
+  } else {  // fp32: the append kernel first, as spattn_kv_append
+    e = spattn::launch_kv_append(false, Kc, Vc, k_new, v_new, pos, B, Hkv, cap, head_dim, stream);
+    if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
+  }
+  e = spattn::launch_decode(a, stream);
+  if (e != cudaSuccess) return fail(SPATTN_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return SPATTN_OK;
+}
+
 spattn_status spattn_decode_check(void* workspace, void* cuda_stream) {
   if (!workspace) return fail(SPATTN_ERR_NULL, "workspace is NULL");
   CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));

@@ -1,6 +1,8 @@
 """Decode parity: one generation step against a ring-buffer KV cache (spattn_kv_append +
 spattn_decode through the C ABI) against the fp64 oracle's decode step, and a whole
-generation loop against rows of the forward oracle on the full sequence."""
+generation loop against rows of the forward oracle on the full sequence.  The fused
+step (spattn_decode_append, the append done by the decode kernel for bf16) must give
+exactly the results and cache contents of the two calls."""
 import math
 
 import numpy as np
@@ -104,7 +106,58 @@ def test_append_writes_the_ring_slot():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_generation_loop_matches_sequence_rows(oracle_mod, dtype):
+@pytest.mark.parametrize("k", range(len(CASES)))
+def test_fused_append_step_equals_append_then_step(k, dtype):
+    B, Hq, Hkv, cap, window, d, pos = CASES[k]
+    g = torch.Generator().manual_seed(700 + k)
+    K, V = _fill_cache(B, Hkv, cap, d, pos, window, dtype, g)
+    q = torch.randn(B, Hq, d, generator=g).to(torch_dtype(dtype)).cuda()
+    kn = torch.randn(B, Hkv, d, generator=g).to(torch_dtype(dtype)).cuda()
+    vn = torch.randn(B, Hkv, d, generator=g).to(torch_dtype(dtype)).cuda()
+    p = torch.tensor(pos, dtype=torch.int64, device="cuda")
+    caches = [sp.DecodeCache(B, Hq, Hkv, cap, d, window=window, dtype=torch_dtype(dtype))
+              for _ in range(2)]
+    for c in caches:
+        c.K.copy_(K.cuda())
+        c.V.copy_(V.cuda())
+    caches[0].append(kn, vn, p)
+    o1, l1 = caches[0].step(q, p, 0.11)
+    o2, l2 = caches[1].append_step(kn, vn, q, p, 0.11)
+    for c in caches:
+        c.check()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(caches[0].K, caches[1].K) and torch.equal(caches[0].V, caches[1].V)
+
+
+def test_fused_append_full_size_equals_two_calls():
+    """B = 8 sequences of the benchmark's shape (Hq 32, Hkv 8, cap = W = 4096, d = 128):
+    several fused steps in a row equal the two-call steps, outputs and caches."""
+    B, Hq, Hkv, cap, d = 8, 32, 8, 4096, 128
+    g = torch.Generator().manual_seed(23)
+    K = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16).cuda()
+    V = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16).cuda()
+    pos0 = torch.from_numpy(np.random.default_rng(4).integers(cap, 10 ** 6, size=B)).cuda()
+    caches = [sp.DecodeCache(B, Hq, Hkv, cap, d) for _ in range(2)]
+    for c in caches:
+        c.K.copy_(K)
+        c.V.copy_(V)
+    for s in range(3):
+        q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).cuda()
+        kn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).cuda()
+        vn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).cuda()
+        p = pos0 + s
+        caches[0].append(kn, vn, p)
+        o1, l1 = caches[0].step(q, p, 1 / math.sqrt(d))
+        o2, l2 = caches[1].append_step(kn, vn, q, p, 1 / math.sqrt(d))
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for c in caches:
+        c.check()
+    assert torch.equal(caches[0].K, caches[1].K) and torch.equal(caches[0].V, caches[1].V)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_generation_loop_matches_sequence_rows(oracle_mod, dtype, fused):
     """Append + decode token by token with a cache smaller than the sequence; every
     step must equal row t of the forward oracle over the whole sequence with the
     causal window."""
@@ -120,8 +173,12 @@ def test_generation_loop_matches_sequence_rows(oracle_mod, dtype):
     outs, lses = [], []
     for t in range(T):
         p = torch.tensor([t], dtype=torch.int64, device="cuda")
-        c.append(Kd[None, :, t].contiguous(), Vd[None, :, t].contiguous(), p)
-        o, l = c.step(Qd[None, :, t].contiguous(), p, scale)
+        if fused:
+            o, l = c.append_step(Kd[None, :, t].contiguous(), Vd[None, :, t].contiguous(),
+                                 Qd[None, :, t].contiguous(), p, scale)
+        else:
+            c.append(Kd[None, :, t].contiguous(), Vd[None, :, t].contiguous(), p)
+            o, l = c.step(Qd[None, :, t].contiguous(), p, scale)
         outs.append(o[0].float().cpu())
         lses.append(l[0].cpu())
     c.check()
