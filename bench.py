@@ -54,15 +54,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the tensor-core forward kernel on the
 # 32K / W=4096 workload, from the ncu capture summarised in
-# the forward kernel's profile summary (captured with H=8, 249.6 MB, scaled by 32/8 heads),
+# the forward kernel's profile summary (captured with H=8, 250.7 MB, scaled by 32/8 heads),
 # valid only for the kernel source with this hash; any other source reports null.
-TRAFFIC = {"kernel_sha": "9618899bf5ccef92", "bytes_per_launch": 998.6e6, "workload": "t32k_w4096"}
+TRAFFIC = {"kernel_sha": "5a48c620f380e51a", "bytes_per_launch": 1002.6e6, "workload": "t32k_w4096"}
 # The same for the backward's dominant kernel (bwd_dkdv_tc, H=4 capture x 8) and the
 # decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
 BWD_TRAFFIC = {"kernel_sha": "988fd762c2c34052", "bytes_per_launch": 1348.9e6,
                "workload": "t32k_w4096", "file": "bwd_tc.cu"}
-DEC_TRAFFIC = {"kernel_sha": "759ec790e0e58505", "file": "decode.cu",
-               "bytes_per_launch": {"decode_b8_w4096": 140.4e6, "decode_b32_w4096": 561.5e6}}
+DEC_TRAFFIC = {"kernel_sha": "f291ef942120fdbd", "file": "decode.cu",
+               "bytes_per_launch": {"decode_b8_w4096": 140.1e6, "decode_b32_w4096": 560.2e6}}
 
 
 def kernel_sha(name: str = "fwd_tc.cu") -> str:
