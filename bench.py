@@ -10,7 +10,10 @@ read per step against the measured HBM bandwidth; its timed steps are captured o
 CUDA graph and replayed (each step still appends, decodes at its own position and merges).
 
 One step = one spattn_fwd call over the whole batch (every (batch, head)) of the
-workload, inputs already resident in HBM.  value = 4 d B H pairs_per_head / t_step
+workload, inputs already resident in HBM.  Warm-up: at least W steps, and for steps
+shorter than 0.2 ms at least 0.2 s of back-to-back steps before the timed region (a kernel
+of tens of microseconds would otherwise be timed while the GPU ramps up from the idle of
+the host-side legs).  value = 4 d B H pairs_per_head / t_step
 (2d flops for q.k and 2d for the weighted values per allowed pair: the glossary's
 O(E (d_k + d_v)) cost, "Sparse attention", section "When the cost is linear").
 Under torchrun each rank runs its own copy of the workload on its GPU (heads are
@@ -248,9 +251,7 @@ def time_secondary(torch, sp, names, steps, warmup, dev, stream):
         def step():
             sp.fwd(plan, q, k, v, scale, out=o, lse=lse, stream=stream)
 
-        for _ in range(warmup):
-            step()
-        stream.synchronize()
+        warm_up(torch, stream, step, warmup)
         timer = StepTimer(torch, dev, stream, steps, 3 * q.numel() * q.element_size(), "Q/K/V")
         with ClockSampler(dev.index or 0) as clk:
             torch.cuda.synchronize(dev)
@@ -280,6 +281,33 @@ def time_secondary(torch, sp, names, steps, warmup, dev, stream):
             "cycles_ratio": (a["ms_per_step"] * ma) / (b["ms_per_step"] * mb) if ma and mb else None,
             "note": "cycles_ratio = (time x median SM MHz) of the 128K step over the 8K step"}
     return out
+
+
+MIN_WARM_S = 0.2  # warm-up wall time before the timed region of a short step
+SHORT_STEP_S = 2e-4  # steps shorter than this get MIN_WARM_S of warm-up
+
+
+def warm_up(torch, stream, step, steps):
+    """Run `steps` untimed steps; while the steps are short (< SHORT_STEP_S each) go on
+    until MIN_WARM_S of wall time has passed, so a kernel of tens of microseconds is not
+    timed while the GPU is still ramping up from idle (after the host-side legs of the
+    run: measured, 30 ms of such steps were not enough, 0.2 s was).  Longer steps stop at
+    `steps`: their own warm-up already brings the clocks up, and more of it would only
+    heat the chip into its power limit."""
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        step()
+        n += 1
+        if n % 8 == 0 or n >= steps:
+            stream.synchronize()
+        if n < steps:
+            continue
+        el = time.perf_counter() - t0
+        if el >= MIN_WARM_S or el / n >= SHORT_STEP_S:
+            break
+    stream.synchronize()
+    return n
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -523,9 +551,7 @@ def run_ours(args, cfg, p):
     def step():
         sp.fwd(plan, q, k, v, scale, out=o, lse=lse, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
+    warm_up(torch, stream, step, args.warmup)
     plan.check_device(stream)
     timer = StepTimer(torch, dev, stream, args.steps, in_bytes, "Q/K/V")
     with ClockSampler(local) as clk:
@@ -649,9 +675,7 @@ def run_ours_bwd(args, cfg, p):
     def step():
         sp.bwd(plan, q, k, v, o, lse, do, scale, dq, dk, dv, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
+    warm_up(torch, stream, step, args.warmup)
     timer = StepTimer(torch, dev, stream, args.steps,
                       5 * q.numel() * q.element_size() + lse.numel() * 4, "q, k, v, O, dO, LSE")
     with ClockSampler(local) as clk:
@@ -780,9 +804,15 @@ def run_decode(args):
     with torch.cuda.graph(graph, stream=stream):
         for s in range(args.steps):
             step(args.warmup + s)
-    with torch.cuda.stream(stream):
-        graph.replay()  # the graph's first launch (upload); the timed launch repeats it
-    stream.synchronize()
+    # the graph's first launches (upload, and the clocks up from idle); replaying it
+    # again rewrites the same rows at the same positions, so the timed launch repeats it
+    t_w = time.perf_counter()
+    while True:
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        if time.perf_counter() - t_w >= 0.2:
+            break
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with ClockSampler(local) as clk:
         barrier(world)
