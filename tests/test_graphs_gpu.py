@@ -117,3 +117,36 @@ def test_decode_step_graph_replay():
 
     _replay_matches(capture, direct, refill)
     c.check()
+
+
+def test_fused_decode_step_graph_replay():
+    """The same generation loop through spattn_decode_append (the decode kernel appends
+    the step's rows): each replay's output equals a direct decode of the cache the replay
+    left behind, at the advanced positions."""
+    B, Hq, Hkv, cap, d = 4, 8, 2, 256, 128
+    c = sp.DecodeCache(B, Hq, Hkv, cap, d, window=200)
+    g = torch.Generator().manual_seed(6)
+    c.K.copy_(torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16).cuda())
+    c.V.copy_(torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16).cuda())
+    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).cuda()
+    kn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).cuda()
+    vn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).cuda()
+    pos = torch.tensor(np.array([7, 255, 256, 999]), dtype=torch.int64, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(B, Hq, device="cuda")
+
+    def capture():
+        c.append_step(kn, vn, q, pos, 0.09, out=out, lse=lse)
+        return [out, lse]
+
+    def direct():
+        return list(c.step(q, pos, 0.09))
+
+    def refill(r):
+        pos.add_(1)
+        q.copy_(torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).cuda())
+        kn.copy_(torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).cuda())
+        vn.copy_(torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).cuda())
+
+    _replay_matches(capture, direct, refill)
+    c.check()
