@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+import spattn_workloads as W
 import sparse_masked_attention_plan_b300 as sp
 from gpu_cases import TOL, host_view, torch_dtype
 
@@ -194,26 +195,38 @@ def test_generation_loop_matches_sequence_rows(oracle_mod, dtype, fused):
         assert np.abs(lse[h] - L).max() <= tol["lse"], f"head {h}: LSE"
 
 
-def test_full_size_sampled_heads(oracle_mod):
-    """The benchmark's decode configuration (B=32, Hq=32, Hkv=8, cap=W=4096, d=128)
-    with every row past the cap at its own position; sampled (b, h) against the oracle."""
-    B, Hq, Hkv, cap, d = 32, 32, 8, 4096, 128
-    g = torch.Generator().manual_seed(17)
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("name", ["decode_b32_w4096", "decode_b8_w4096"])
+def test_full_size_every_head(oracle_mod, name, fused):
+    """The benchmark's decode configurations (cap = W = 4096, Hq = 32, Hkv = 8, d = 128)
+    with every batch row past the cap at its own position: every (b, h) of the step,
+    element by element, against the oracle at the bf16 tolerances (max-abs, rel-L2,
+    LSE).  With `fused` the step's rows go in through spattn_decode_append, so the
+    oracle reads the cache with those rows written into their ring slots."""
+    cfg = W.DECODE_WORKLOADS[name]
+    B, Hq, Hkv, cap, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["cap"], cfg["d"]
+    g = torch.Generator().manual_seed(17 + B)
     K = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16)
     V = torch.randn(B, Hkv, cap, d, generator=g).to(torch.bfloat16)
     q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16)
-    pos = np.random.default_rng(3).integers(cap, 10 ** 6, size=B)
+    kn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16)
+    pos = np.random.default_rng(3 + B).integers(cap, 10 ** 6, size=B)
     c = sp.DecodeCache(B, Hq, Hkv, cap, d)
     c.K.copy_(K.cuda())
     c.V.copy_(V.cuda())
-    out, lse = c.step(q.cuda(), torch.tensor(pos, device="cuda"), 1 / math.sqrt(d))
+    pos_d = torch.tensor(pos, device="cuda")
+    scale = 1 / math.sqrt(d)
+    if fused:
+        out, lse = c.append_step(kn.cuda(), vn.cuda(), q.cuda(), pos_d, scale)
+        for b in range(B):
+            K[b, :, pos[b] % cap] = kn[b]
+            V[b, :, pos[b] % cap] = vn[b]
+    else:
+        out, lse = c.step(q.cuda(), pos_d, scale)
     c.check()
-    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
-    for b, h in [(0, 0), (5, 13), (31, 31), (17, 2)]:
-        ref, ref_lse = oracle.decode(host_view(q[b, h]), host_view(K[b, h // 4]),
-                                     host_view(V[b, h // 4]), int(pos[b]), cap, 1 / math.sqrt(d))
-        assert np.abs(out[b, h] - ref).max() <= 1e-2
-        assert abs(lse[b, h] - ref_lse) <= 1e-4
+    _compare(out.float().cpu().numpy(), lse.cpu().numpy(), q, K, V, pos, cap, scale, "bf16",
+             Hq // Hkv)
 
 
 def test_bad_arguments():
