@@ -333,14 +333,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dsc2 = f32x2(dsc, dsc), dterm2 = f32x2(dterm, dterm);
     uint32_t sph = 0;
     int n_done = 0;
+    // entries two ahead and the tile's column-mask words one ahead, so that no global
+    // load's latency sits between one tile's hand-off and the next tile's mask
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
+    int4 e_next2 = n_ent > 1 ? ents[1] : make_int4(0, 0, 0, 0);
+    uint4 cm_next = n_ent ? colmask_words(p.colmask, e_next) : make_uint4(0u, 0u, 0u, 0u);
     for (int n = 0; n < n_ent; ++n) {
       const int4 e = e_next;
-      if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead, consumed next iteration
+      const uint4 cm = cm_next;
+      e_next = e_next2;
+      if (n + 2 < n_ent) e_next2 = ents[n + 2];
+      if (n + 1 < n_ent) cm_next = colmask_words(p.colmask, e_next);
       if (!(e.y & active_bit)) continue;
-      // the row's mask words, computed before the wait so their loads overlap the products
+      // the row's mask words, computed before the wait so that they overlap the products
       uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (!(e.y & full_bit)) row_mask(make_predicate(m, p.colmask, e, i), w);
+      if (!(e.y & full_bit)) row_mask(make_predicate(m, cm, e, i), w);
       const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
@@ -350,15 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // time; the bf16 result of chunk qq lands over this half's S, already loaded
       {
         const int h = wg;
-        uint32_t sv64[64], dv64[64];  // S and dP of key half h (columns 64h .. 64h+63)
-        tmem_ld64x2(lane_base + 128 * h, sv64, lane_base + 128 * h + 64, dv64);
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * h + qq;
-        const uint32_t* sv = sv64 + 32 * qq;
-        const uint32_t* dv = dv64 + 32 * qq;
+        // S and dP of the chunk's 32 keys (dS of chunk 0 lands over columns 0-15 of S,
+        // which chunk 1 does not read)
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2(lane_base + 128 * h + 32 * qq, sv, lane_base + 128 * h + 64 + 32 * qq, dv);
         uint32_t pk[16];
-        const bool all = w[q] == 0xffffffffu;
+        const uint32_t wq = h ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
+        const bool all = wq == 0xffffffffu;
 #pragma unroll
         for (int b = 0; b < 16; ++b) {
           const int c0 = 2 * b;
@@ -367,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 nl2x2), x0, x1);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           if (!all) {
-            if (!((w[q] >> c0) & 1u)) p0 = 0.f;
-            if (!((w[q] >> (c0 + 1)) & 1u)) p1 = 0.f;
+            if (!((wq >> c0) & 1u)) p0 = 0.f;
+            if (!((wq >> (c0 + 1)) & 1u)) p1 = 0.f;
           }
           const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
                                         dsc2, dterm2);
@@ -505,11 +513,33 @@ __device__ __forceinline__ void add_span(int a, int b, uint32_t (&w)[4]) {
   for (int k = 0; k < 4; ++k) w[k] |= span_bits(a, b, 32 * k);
 }
 
+// What the mask says about key j whatever the query tile: whether it is a strided or
+// global column, and its range in the transposed random-block list.  Loaded once per
+// CTA, so no global load sits on the per-tile path.
+struct KeyInfo {
+  bool colbit;
+  int rt_lo, rt_hi;
+};
+
+__device__ __forceinline__ KeyInfo key_info(const KvParams& p, int j) {
+  const MaskDev& m = p.mask;
+  KeyInfo k;
+  const uint32_t cw = p.colmask[(j / kTile) * 4 + (j % kTile) / 32];
+  k.colbit = (cw >> (j & 31)) & 1u;
+  k.rt_lo = k.rt_hi = 0;
+  if (m.rand_block) {
+    const int kb = j / m.rand_block;
+    k.rt_lo = p.rt_off[kb];
+    k.rt_hi = p.rt_off[kb + 1];
+  }
+  return k;
+}
+
 // The query columns of the tile at row q0 that may read key j (packed index c_pk for
 // packed units), for an entry of `kind`; rows that are not rows of the tile are
 // removed separately (LSE = +inf).
 __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, int q0, int j,
-                                         int c_pk, uint32_t (&w)[4]) {
+                                         int c_pk, const KeyInfo& ki, uint32_t (&w)[4]) {
   const MaskDev& m = p.mask;
   w[0] = w[1] = w[2] = w[3] = 0u;
   if (kind == kKindPacked) {
@@ -533,11 +563,9 @@ __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, in
   const int jc = j - q0;  // the key's own column
   const int cut = m.causal ? jc : 0;
   uint32_t extra[4] = {0u, 0u, 0u, 0u};
-  const uint32_t cw = p.colmask[(j / kTile) * 4 + (j % kTile) / 32];
-  const bool colbit = (cw >> (j & 31)) & 1u;
+  const bool colbit = ki.colbit;
   if (m.rand_block && !(kind == kKindRandom && colbit)) {
-    const int kb = j / m.rand_block;
-    for (int x = p.rt_off[kb]; x < p.rt_off[kb + 1]; ++x) {
+    for (int x = ki.rt_lo; x < ki.rt_hi; ++x) {
       const int r0 = p.rt_qb[x] * m.rand_block - q0;
       add_span(max(r0, cut), r0 + m.rand_block - 1, extra);
     }
@@ -753,27 +781,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto seq = [&](int x) { return static_cast<size_t>(x) * p.dview + res; };
     uint32_t sph = 0;
     int n_done = 0;
+    const KeyInfo ki = key_info(p, j);
     // LSE and D of query column 64 wg + kk of an entry (threads kk < 64 of each
     // warpgroup load their half's columns), one entry ahead so the global loads overlap
-    // the previous tile's work
-    auto column_values = [&](const int4& e, float& lse_v, float& dd_v) {
-      int i = -1;
+    // the previous tile's work.  The loads are issued unconditionally (a row outside
+    // the sequence reads row 0) and whether the column is a row of the tile (`keep`:
+    // inside the sequence and not a global row, whose gradient comes from its gathered
+    // tile) is decided when the values are used, so nothing waits for them here
+    auto column_values = [&](const int4& e, float& lse_v, float& dd_v, uint32_t& keep) {
       const int a = e.x + 64 * wg + kk;
-      if (e.y & kEntryGathered) {
-        if (a < m.n_global) i = m.gpos[a];
-      } else if (a < m.T && !m.rowglobal[a]) {
-        i = a;
+      size_t at;
+      if (e.y & kEntryGathered) {  // the row's position comes from the global list
+        const int i = a < m.n_global ? m.gpos[a] : -1;
+        keep = i >= 0;
+        at = head + static_cast<size_t>(max(i, 0));
+      } else {
+        const int i = a < m.T ? a : 0;
+        keep = static_cast<uint32_t>(a < m.T) & (static_cast<uint32_t>(m.rowglobal[i]) ^ 1u);
+        at = head + seq(i);
       }
-      const size_t at = head + ((e.y & kEntryGathered) ? static_cast<size_t>(i) : seq(i));
-      lse_v = i >= 0 ? p.LSE[at] * 1.4426950408889634f : INFINITY;
-      dd_v = i >= 0 ? p.Dvec[at] * dsc : 0.f;
+      lse_v = p.LSE[at];
+      dd_v = p.Dvec[at];
     };
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     float lse_next = 0.f, dd_next = 0.f;
-    if (n_ent && kk < 64) column_values(e_next, lse_next, dd_next);
+    uint32_t keep_next = 0u;
+    if (n_ent && kk < 64) column_values(e_next, lse_next, dd_next, keep_next);
     for (int n = 0; n < n_ent; ++n) {
       const int4 e = e_next;
-      const float lse_cur = lse_next, dd_cur = dd_next;
+      const float lse_cur = keep_next ? lse_next * 1.4426950408889634f : INFINITY;
+      const float dd_cur = keep_next ? dd_next * dsc : 0.f;
       if (n + 1 < n_ent) e_next = ents[n + 1];
       const int kind = (e.y >> kKindShift) & 3;
       // this warpgroup's 64 query columns' LSE and D, double-buffered per warpgroup:
@@ -788,12 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();  // this warp's LSE and D values are written before lane 0 arrives
       if (lane == 0) mbar_arrive(BAR(C::kBarVec + wg * 2 + (n & 1)));
-      if (kk < 64 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next);
+      if (kk < 64 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next, keep_next);
       if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + wg * 2 + (n & 1)), (n >> 1) & 1,
                                              p.budget, p.err, kErrTimeout)))
         break;
       uint32_t w[4];
-      key_mask(p, kind, e, e.x, j, key, w);
+      key_mask(p, kind, e, e.x, j, key, ki, w);
       if (!key_valid) w[0] = w[1] = w[2] = w[3] = 0u;
       const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -801,15 +838,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       {
         const int hh = wg;
-        uint32_t sv64[64], dv64[64];  // S^T and dP^T of query half hh (columns 64hh ..)
-        tmem_ld64x2(lane_base + 128 * hh, sv64, lane_base + 128 * hh + 64, dv64);
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * hh + qq;
-        const uint32_t* sv = sv64 + 32 * qq;
-        const uint32_t* dv = dv64 + 32 * qq;
+        // S^T and dP^T of the chunk's 32 queries (P^T and dS^T of chunk 0 land over
+        // columns 0-15 of S^T and dP^T, which chunk 1 does not read)
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2(lane_base + 128 * hh + 32 * qq, sv, lane_base + 128 * hh + 64 + 32 * qq, dv);
         uint32_t pp[16], pg[16];
-        const bool all = w[q] == 0xffffffffu;
+        const uint32_t wq = hh ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
+        const bool all = wq == 0xffffffffu;
 #pragma unroll
         for (int b = 0; b < 16; b += 2) {  // four columns per step: one vector load each
           const int c0 = 32 * qq + 2 * b;  // column within this warpgroup's 64
@@ -825,8 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   f32x2(-la, -lb)), x0, x1);
             float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             if (!all) {
-              if (!((w[q] >> x) & 1u)) p0 = 0.f;
-              if (!((w[q] >> (x + 1)) & 1u)) p1 = 0.f;
+              if (!((wq >> x) & 1u)) p0 = 0.f;
+              if (!((wq >> (x + 1)) & 1u)) p1 = 0.f;
             }
             const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1])),
                                           dsc2, f32x2(-da, -db));

@@ -52,8 +52,18 @@ struct RowPredicate {
   uint32_t bits[4];
 };
 
-__device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const uint32_t* colmask,
-                                                       int4 e, int i) {
+// The column-mask words of an entry's key tile (band and random entries; zero for the
+// other kinds, which do not read them).  Loaded apart from make_predicate so that a
+// kernel can fetch them one entry ahead.
+__device__ __forceinline__ uint4 colmask_words(const uint32_t* colmask, int4 e) {
+  const int kind = (e.y >> kKindShift) & 3;
+  if (kind == kKindBand || kind == kKindRandom)
+    return *reinterpret_cast<const uint4*>(colmask + 4 * e.z);
+  return make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The predicate of row i in the entry's tile, with the tile's column-mask words `w`.
+__device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, uint4 w, int4 e, int i) {
   RowPredicate p;
   const int kind = (e.y >> kKindShift) & 3;
   const int k0 = e.x;
@@ -80,7 +90,6 @@ __device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const u
     p.lo = lo - k0;
     p.hi = hi - k0;
     p.hb = hb - k0;
-    const uint4 w = *reinterpret_cast<const uint4*>(colmask + 4 * e.z);
     p.bits[0] = w.x;
     p.bits[1] = w.y;
     p.bits[2] = w.z;
@@ -95,7 +104,6 @@ __device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const u
     p.lo = 1;  // no local span
     p.hi = 0;
     p.hb = (m.causal ? min(i, m.T - 1) : m.T - 1) - k0;
-    const uint4 w = *reinterpret_cast<const uint4*>(colmask + 4 * e.z);
     uint32_t r[4];
     random_bits(m, i, k0, r);
     p.bits[0] = r[0] & ~w.x;
@@ -110,6 +118,11 @@ __device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const u
     p.hi = (m.causal ? min(i, m.T - 1) : m.T - 1) - k0;
   }
   return p;
+}
+
+__device__ __forceinline__ RowPredicate make_predicate(const MaskDev& m, const uint32_t* colmask,
+                                                       int4 e, int i) {
+  return make_predicate(m, colmask_words(colmask, e), e, i);
 }
 
 // Bits b of a 32-bit word with lo <= base + b <= hi.
@@ -135,7 +148,14 @@ __device__ __forceinline__ void row_mask(const RowPredicate& p, uint32_t (&w)[4]
   int c = max(p.lo, 0);
   c += ((p.res - c) % p.dil + p.dil) % p.dil;
   const int last = min(p.hi, kTile - 1);
-  for (; c <= last; c += p.dil) w[c >> 5] |= 1u << (c & 31);
+  for (; c <= last; c += p.dil) {  // word selected by value: w stays in registers
+    const uint32_t bit = 1u << (c & 31);
+    const int k = c >> 5;
+    w[0] |= k == 0 ? bit : 0u;
+    w[1] |= k == 1 ? bit : 0u;
+    w[2] |= k == 2 ? bit : 0u;
+    w[3] |= k == 3 ? bit : 0u;
+  }
 }
 
 __device__ __forceinline__ bool pred_allowed(const RowPredicate& p, int c) {
