@@ -456,6 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int4 e = e_next;
       if (n + 1 < n_ent) e_next = ents[n + 1];
       if (!(e.y & (kActive0 << wg))) continue;
+      // the row's allowed columns, computed before the wait (they do not depend on S, and
+      // the column-mask load overlaps the product)
+      const bool partial = !(e.y & (kFull0 << wg));
+      uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (partial) row_mask(make_predicate(m, p.colmask, e, i), w);
       const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
@@ -468,9 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // every lane's load is complete before lane 0 arrives for the warp
         if (lane == 0) mbar_arrive(BAR(C::kBarSfree + wg));
       }
-      if (!(e.y & (kFull0 << wg))) {
-        uint32_t w[4];
-        row_mask(make_predicate(m, p.colmask, e, i), w);
+      if (partial) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
           if (!((w[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
