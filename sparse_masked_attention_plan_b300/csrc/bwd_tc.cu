@@ -588,7 +588,7 @@ __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, in
   pr.hi = min(pr.hi, kTile - 1);
   pr.hb = kTile - 1;
   pr.dil = d;
-  pr.res = ((jc % d) + d) % d;
+  pr.res = d == 1 ? 0 : ((jc % d) + d) % d;  // no division when d = 1
 #pragma unroll
   for (int k = 0; k < 4; ++k) pr.bits[k] = extra[k];
   row_mask(pr, w);
