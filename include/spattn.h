@@ -308,11 +308,17 @@ spattn_status spattn_decode_check(void* workspace, void* cuda_stream);
 
 /*
  * The same forward pass from HOST buffers: copies Q/K/V host -> device, runs
- * spattn_fwd, copies O and LSE device -> host, all on `cuda_stream`, and returns
- * after the stream is synchronised.  Host buffers should be pinned for full copy
- * bandwidth.  The caller provides the device buffers (same shapes) so that this
- * call allocates nothing beyond spattn_fwd's scratch.  LSE pointers may both be
- * NULL.
+ * spattn_fwd, copies O and LSE device -> host, and returns once everything has
+ * completed.  The (batch, head) units are processed in up to 8 chunks of consecutive
+ * units as a pipeline: the host -> device copy of chunk k+1 (on a copy stream the
+ * plan owns), the forward of chunk k (on `cuda_stream`) and the device -> host copy of
+ * chunk k-1 (a second plan-owned stream) run at the same time; the copies start after
+ * the work already queued on `cuda_stream`.  Results are identical to one spattn_fwd.
+ * Host buffers should be pinned, or the copies neither reach full bandwidth nor
+ * overlap.  The caller provides the device buffers (same shapes) so that this call
+ * allocates nothing beyond spattn_fwd's scratch and, on first use, the plan's two
+ * streams and their events.  LSE pointers may both be NULL.  Not safe to call on one
+ * plan from two host threads at once.
  */
 spattn_status spattn_fwd_host(const spattn_plan* plan, int32_t B, int32_t H,
                               spattn_dtype dtype, const void* Q_host, const void* K_host,

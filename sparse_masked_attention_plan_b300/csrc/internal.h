@@ -126,6 +126,12 @@ struct spattn_plan {
   int* d_err = nullptr;
   uint64_t wait_budget_cycles = 8000000000ull;  // ~4 s at the maximum SM clock
   int32_t inject_timeout = 0;                     // test hook, see spattn_plan_test_wait_timeout
+  // spattn_fwd_host: a copy-in and a copy-out stream and the per-chunk events of its
+  // pipeline (host -> device of chunk k+1, forward of chunk k, device -> host of chunk
+  // k-1), created on first use on the plan's device
+  static constexpr int kHostChunks = 8;
+  cudaStream_t host_in = nullptr, host_out = nullptr;
+  cudaEvent_t host_ev[2 * kHostChunks + 2] = {};
 
   spattn::MaskDev mask_dev() const {
     spattn::MaskDev m;

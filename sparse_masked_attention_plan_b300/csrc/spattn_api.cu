@@ -54,6 +54,10 @@ void free_plan_memory(spattn_plan* p) {
                   p->d_rtoff, p->d_rtqb, p->bsched_res.d_items, p->bsched_res.d_entries};
   for (void* q : ptrs)
     if (q) cudaFree(q);
+  for (cudaEvent_t e : p->host_ev)
+    if (e) cudaEventDestroy(e);
+  if (p->host_in) cudaStreamDestroy(p->host_in);
+  if (p->host_out) cudaStreamDestroy(p->host_out);
 }
 
 // ---- host scheduler ---------------------------------------------------------------
@@ -1115,19 +1119,55 @@ spattn_status spattn_fwd_host(const spattn_plan* p, int32_t B, int32_t H, spattn
   if (B < 1 || H < 1) return fail(SPATTN_ERR_SHAPE, "B and H must be >= 1");
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   const size_t esize = dtype == SPATTN_BF16 ? 2 : 4;
-  const size_t rows = size_t(B) * H * p->T;
-  const size_t bytes = rows * p->d * esize;
   spattn_status st;
   if ((st = check_ptr(Qd, "Q_dev")) || (st = check_ptr(Kd, "K_dev")) || (st = check_ptr(Vd, "V_dev")) ||
       (st = check_ptr(Od, "O_dev")))
     return st;
-  CUDA_TRY(cudaMemcpyAsync(Qd, Qh, bytes, cudaMemcpyHostToDevice, stream));
-  CUDA_TRY(cudaMemcpyAsync(Kd, Kh, bytes, cudaMemcpyHostToDevice, stream));
-  CUDA_TRY(cudaMemcpyAsync(Vd, Vh, bytes, cudaMemcpyHostToDevice, stream));
-  st = spattn_fwd(p, B, H, dtype, Qd, Kd, Vd, scale, Od, LSEd, cuda_stream);
-  if (st != SPATTN_OK) return st;
-  CUDA_TRY(cudaMemcpyAsync(Oh, Od, bytes, cudaMemcpyDeviceToHost, stream));
-  if (LSEh) CUDA_TRY(cudaMemcpyAsync(LSEh, LSEd, rows * 4, cudaMemcpyDeviceToHost, stream));
+  spattn_plan* mp = const_cast<spattn_plan*>(p);  // owns the pipeline's streams and events
+  if (!mp->host_in) {
+    CUDA_TRY(cudaStreamCreateWithFlags(&mp->host_in, cudaStreamNonBlocking));
+    CUDA_TRY(cudaStreamCreateWithFlags(&mp->host_out, cudaStreamNonBlocking));
+    for (cudaEvent_t& e : mp->host_ev) CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  }
+  // Chunks of consecutive (batch, head) units ([B][H][T][d] keeps each chunk contiguous):
+  // the copy-in stream brings chunk k+1 while `stream` computes chunk k and the
+  // copy-out stream returns chunk k-1; every unit is computed independently, so the
+  // results equal one spattn_fwd over all units.
+  const int64_t BH = int64_t(B) * H;
+  const int64_t n_chunks = std::min<int64_t>(BH, spattn_plan::kHostChunks);
+  const int64_t per = (BH + n_chunks - 1) / n_chunks;
+  const size_t unit = size_t(p->T) * p->d * esize;
+  cudaEvent_t* ev = mp->host_ev;
+  cudaEvent_t ev_start = ev[2 * spattn_plan::kHostChunks], ev_done = ev[2 * spattn_plan::kHostChunks + 1];
+  // earlier work on `stream` may still use the device buffers
+  CUDA_TRY(cudaEventRecord(ev_start, stream));
+  CUDA_TRY(cudaStreamWaitEvent(mp->host_in, ev_start, 0));
+  for (int64_t c = 0; c * per < BH; ++c) {
+    const int64_t u0 = c * per, cnt = std::min(per, BH - u0);
+    const size_t off = size_t(u0) * unit, len = size_t(cnt) * unit;
+    auto at = [off](const void* b) { return static_cast<const char*>(b) + off; };
+    auto atw = [off](void* b) { return static_cast<char*>(b) + off; };
+    CUDA_TRY(cudaMemcpyAsync(atw(Qd), at(Qh), len, cudaMemcpyHostToDevice, mp->host_in));
+    CUDA_TRY(cudaMemcpyAsync(atw(Kd), at(Kh), len, cudaMemcpyHostToDevice, mp->host_in));
+    CUDA_TRY(cudaMemcpyAsync(atw(Vd), at(Vh), len, cudaMemcpyHostToDevice, mp->host_in));
+    CUDA_TRY(cudaEventRecord(ev[2 * c], mp->host_in));
+    CUDA_TRY(cudaStreamWaitEvent(stream, ev[2 * c], 0));
+    float* lse_d = LSEd ? LSEd + size_t(u0) * p->T : nullptr;
+    st = spattn_fwd(p, 1, static_cast<int32_t>(cnt), dtype, atw(Qd), atw(Kd), atw(Vd), scale,
+                    atw(Od), lse_d, cuda_stream);
+    if (st != SPATTN_OK) {
+      cudaStreamSynchronize(mp->host_in);
+      return st;
+    }
+    CUDA_TRY(cudaEventRecord(ev[2 * c + 1], stream));
+    CUDA_TRY(cudaStreamWaitEvent(mp->host_out, ev[2 * c + 1], 0));
+    CUDA_TRY(cudaMemcpyAsync(atw(Oh), at(Od), len, cudaMemcpyDeviceToHost, mp->host_out));
+    if (LSEh)
+      CUDA_TRY(cudaMemcpyAsync(LSEh + size_t(u0) * p->T, lse_d, size_t(cnt) * p->T * 4,
+                               cudaMemcpyDeviceToHost, mp->host_out));
+  }
+  CUDA_TRY(cudaEventRecord(ev_done, mp->host_out));
+  CUDA_TRY(cudaStreamWaitEvent(stream, ev_done, 0));
   CUDA_TRY(cudaStreamSynchronize(stream));
   return SPATTN_OK;
 }

@@ -141,3 +141,34 @@ def test_host_buffer_entry_matches_device_entry(oracle_mod):
     sp.fwd_host(plan, hq, hk, hv, 0.125, ho, hl, bufs)
     assert torch.equal(ho, o_dev.cpu())
     assert torch.equal(hl, l_dev.cpu())
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,H,with_lse", [(3, 5, True), (1, 1, True), (2, 8, False), (1, 19, True)])
+def test_host_buffer_pipeline_chunks(B, H, with_lse, dtype):
+    """The host-buffer entry splits the (batch, head) units into up to 8 chunks whose
+    copies overlap the forward of their neighbours: uneven chunk counts (15 units in
+    chunks of 2, 19 in chunks of 3, a single unit), packed strided / global columns
+    (plan scratch reused across chunks), with and without LSE, both dtypes, equal bit
+    for bit to one device call; and a second call on the same plan after work queued
+    on the stream writes the device buffers."""
+    T, d = 700, 64
+    plan = sp.Plan(T, d, causal=1, window=150, stride=48, offset=7, global_pos=[3, 333])
+    Q, K, V = W.qkv(B, H, T, d, 21, dtype)
+    o_dev, l_dev = sp.fwd(plan, Q.cuda(), K.cuda(), V.cuda(), 0.1)
+    torch.cuda.synchronize()  # the plan's scratch is shared with the calls below
+    hq, hk, hv = (x.pin_memory() for x in (Q, K, V))
+    ho = torch.empty_like(Q).pin_memory()
+    hl = torch.empty(B, H, T, dtype=torch.float32).pin_memory() if with_lse else None
+    qd, kd, vd, od = (torch.empty_like(Q, device="cuda") for _ in range(4))
+    ld = torch.empty(B, H, T, dtype=torch.float32, device="cuda") if with_lse else None
+    s = torch.cuda.Stream()
+    for rep in range(2):
+        with torch.cuda.stream(s):
+            for x in (qd, kd, vd, od):  # queued before the call: the copies must follow it
+                x.fill_(7.0)
+        sp.fwd_host(plan, hq, hk, hv, 0.1, ho, hl, (qd, kd, vd, od, ld), stream=s)
+        assert torch.equal(ho, o_dev.cpu()), f"call {rep}"
+        if with_lse:
+            assert torch.equal(hl, l_dev.cpu()), f"call {rep}"
+    plan.check_device()
