@@ -53,12 +53,24 @@ struct DqCfg {
   // kBarP + q: chunk q (keys 32q .. 32q+31) of dS is in TMEM; one barrier per chunk
   // so each completes once per key tile and a waiter can never miss a phase
   // kBarS + h: S and dP of key half h are in TMEM
+  // kBarSfree: every elementwise warp has read its columns of S (whole-tile form)
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
                        kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
-                       kBarDone = 2 * kStages + 7, kNumBars = 2 * kStages + 8;
+                       kBarDone = 2 * kStages + 7, kBarSfree = 2 * kStages + 8,
+                       kNumBars = 2 * kStages + 9;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0, 0);
+  static constexpr uint32_t kIdescFull = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
+  // Whole-tile products: S = Q K^T (TMEM 0) and dP = dO V^T (TMEM 128) of all 128 keys
+  // as two N = 128 products with a barrier each (kBarS + 0, kBarS + 1).  dS (bf16, 64
+  // columns) goes to one of two buffers after dQ (tile k uses buffer k % 2, chunk q at
+  // +16q), so S of the next tile is computed as soon as every warp has read S
+  // (kBarSfree), while the elementwise warps work on this tile; dP of the next tile
+  // follows this tile's dQ products.  A dS buffer is rewritten two tiles later, after
+  // the dP product issued behind that tile's dQ products has completed.
+  static constexpr bool kWhole = true;
+  static constexpr uint32_t kColDS = 256 + D;
   // TMEM: key half h has S at 128h and dP at 128h + 64 (64 columns each); dQ at 256
   static constexpr uint32_t kColDQ = 256;
 };
@@ -93,6 +105,17 @@ __device__ __forceinline__ void issue_half(uint32_t d_tmem, uint64_t a_desc, uin
   }
 }
 constexpr uint32_t kHalfRows16 = (64 * 128) >> 4;  // descriptor offset of a tile's row 64
+
+// A (128 rows) x B^T (128 rows), both K-major over d: a whole-tile S or dP product.
+template <int D>
+__device__ __forceinline__ void issue_tile(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  using C = DqCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, a_desc + off16, b_desc + off16, C::kIdescFull, kk > 0 ? 1u : 0u);
+  }
+}
 
 
 // k-steps 2 chunk, 2 chunk + 1 of an accumulating product over the 128-wide tile
@@ -162,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier word would serialise on the critical path)
     for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 4);
     mbar_init(BAR(C::kBarDone), 1);
+    mbar_init(BAR(C::kBarSfree), 8);  // one arrival per elementwise warp
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -258,17 +282,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
+      // whole tiles: S and dP of the tile whose K and V copies are at `it`
+      auto issue_s = [&](int it) {
+        if (elect_one()) {
+          issue_tile<D>(tmem, q_desc, kv_kdesc + (it % C::kStages) * kSlot16);
+          mma_commit(BAR(C::kBarS + 0));
+        }
+        __syncwarp();
+      };
+      auto issue_dp = [&](int it) {
+        const uint32_t vs = (it + 1) % C::kStages;
+        if (elect_one()) {
+          issue_tile<D>(tmem + 128, do_desc, kv_kdesc + vs * kSlot16);
+          mma_commit(BAR(C::kBarS + 1));
+          mma_commit(BAR(C::kBarEmpty + vs));  // V is no longer needed
+        }
+        __syncwarp();
+      };
       int it = 0, done = 0;
       int n = next_active(0);
       if (n < n_ent) {
         if (!wait_kv(0)) ok = false;
         if (ok) {
           tc_fence_after();
-          issue_sdp(0, 0);
-          issue_sdp(0, 1);
+          if constexpr (C::kWhole) {
+            issue_s(0);
+            issue_dp(0);
+          } else {
+            issue_sdp(0, 0);
+            issue_sdp(0, 1);
+          }
         }
       }
-      while (ok && n < n_ent) {
+      while (C::kWhole && ok && n < n_ent) {
+        const int n1 = next_active(n + 1);
+        const uint32_t ks = it % C::kStages;
+        const uint32_t par = done & 1;
+        if (n1 < n_ent) {  // S of the next tile once every warp has read this tile's S
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarSfree), par, p.budget, p.err,
+                                                 kErrTimeout)) ||
+              !wait_kv(it + 2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(it + 2);
+        }
+        const uint32_t dsb = C::kColDS + 64 * (done & 1);
+        for (int q = 0; q < 4; ++q) {  // dQ += dS K, 32 keys at a time as the chunks arrive
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), par, p.budget, p.err,
+                                                 kErrTimeout))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one())
+            issue_acc_chunk<D>(tmem + C::kColDQ, tmem + dsb + 16 * q, kv_mndesc + ks * kSlot16, q,
+                               done > 0);
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
+        __syncwarp();
+        if (n1 < n_ent) issue_dp(it + 2);  // every chunk has read this tile's dP
+        it += 2;
+        ++done;
+        n = n1;
+      }
+      while (!C::kWhole && ok && n < n_ent) {
         const int n1 = next_active(n + 1);
         const uint32_t ks = it % C::kStages;
         const uint32_t par = done & 1;
@@ -348,6 +429,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row's mask words, computed before the wait so that they overlap the products
       uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (!(e.y & full_bit)) row_mask(make_predicate(m, cm, e, i), w);
+      if constexpr (C::kWhole) {
+        // P of this warpgroup's 64 keys from S (while dP is still being computed), then
+        // dS = scale P (dP - D) chunk by chunk as dP arrives
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 0), sph, p.budget, p.err, kErrTimeout)))
+          break;
+        tc_fence_after();
+        if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
+        float pr[2][32];
+        {
+          uint32_t sa[32], sb[32];  // this warpgroup's 64 columns of S, one wait
+          tmem_ld32x2(lane_base + 64 * wg, sa, lane_base + 64 * wg + 32, sb);
+          tc_fence_before();
+          __syncwarp();  // every lane has read S before lane 0 arrives for the warp
+          if (lane == 0) mbar_arrive(BAR(C::kBarSfree));
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            const uint32_t* sv = qq ? sb : sa;
+            const uint32_t wq = wg ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+              const int c0 = 2 * b;
+              float x0, x1;
+              f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])),
+                                    c2x2, nl2x2), x0, x1);
+              pr[qq][c0] = ((wq >> c0) & 1u) ? fast_exp2(x0) : 0.f;
+              pr[qq][c0 + 1] = ((wq >> (c0 + 1)) & 1u) ? fast_exp2(x1) : 0.f;
+            }
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 1), sph, p.budget, p.err, kErrTimeout)))
+          break;
+        sph ^= 1u;
+        tc_fence_after();
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = 2 * wg + qq;
+          uint32_t dv[32], pk[16];
+          tmem_ld32(lane_base + 128 + 32 * q, dv);
+#pragma unroll
+          for (int b = 0; b < 16; ++b) {
+            const int c0 = 2 * b;
+            const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
+                                          dsc2, dterm2);
+            float g0, g1;
+            f32x2_split(mul_f32x2(f32x2(pr[qq][c0], pr[qq][c0 + 1]), t2), g0, g1);
+            pk[b] = pack_bf16x2(g0, g1);
+          }
+          tmem_st16(lane_base + C::kColDS + 64 * (n_done & 1) + 16 * q, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
+          if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
+        }
+        ++n_done;
+        continue;
+      }
       const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
       if (!__all_sync(0xffffffffu, got)) break;
       sph ^= 1u;
