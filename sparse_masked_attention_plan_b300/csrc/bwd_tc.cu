@@ -17,11 +17,11 @@
 //   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
 //              memory), then dQ += dS K with dS (bf16) from TMEM and the same K tile
 //              read as an MN-major operand
-// TMEM: per key half h (64 keys), S at 128h and dP at 128h + 64; dQ at 256.  dS (bf16)
-// overwrites the half's own S; the tensor pipe runs products in issue order, so the next
-// tile's S (issued after this half's dQ products) cannot overwrite dS before dQ has
-// read it.  The halves ping-pong between the two elementwise warpgroups.  P needs no running maximum:
-// the forward's LSE already normalises it.
+// TMEM: S of the key tile at 0 and dP at 128 (whole 128-key products), dQ at 256, and
+// two dS buffers (bf16, 64 columns each) after it, used by alternate key tiles.  The
+// next tile's S is issued once every elementwise warp has read this tile's S, so it
+// runs while P is computed; the warps compute P from S while dP is still being
+// computed.  P needs no running maximum: the forward's LSE already normalises it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,29 +50,29 @@ struct DqCfg {
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;  // Q and dO
   static constexpr int kSmemKV = kStages * kTileBytes;
+  // kBarS + 0 / + 1: S / dP of the key tile are in TMEM
   // kBarP + q: chunk q (keys 32q .. 32q+31) of dS is in TMEM; one barrier per chunk
   // so each completes once per key tile and a waiter can never miss a phase
-  // kBarS + h: S and dP of key half h are in TMEM
-  // kBarSfree: every elementwise warp has read its columns of S (whole-tile form)
+  // kBarSfree: every elementwise warp has read its columns of S
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
                        kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
                        kBarDone = 2 * kStages + 7, kBarSfree = 2 * kStages + 8,
                        kNumBars = 2 * kStages + 9;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0, 0);
+  static constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0, 0);  // dK/dV kernel
   static constexpr uint32_t kIdescFull = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
   // Whole-tile products: S = Q K^T (TMEM 0) and dP = dO V^T (TMEM 128) of all 128 keys
-  // as two N = 128 products with a barrier each (kBarS + 0, kBarS + 1).  dS (bf16, 64
-  // columns) goes to one of two buffers after dQ (tile k uses buffer k % 2, chunk q at
-  // +16q), so S of the next tile is computed as soon as every warp has read S
-  // (kBarSfree), while the elementwise warps work on this tile; dP of the next tile
-  // follows this tile's dQ products.  A dS buffer is rewritten two tiles later, after
-  // the dP product issued behind that tile's dQ products has completed.
-  static constexpr bool kWhole = true;
-  static constexpr uint32_t kColDS = 256 + D;
-  // TMEM: key half h has S at 128h and dP at 128h + 64 (64 columns each); dQ at 256
+  // as two N = 128 products with a barrier each (64-key halves would run at two thirds
+  // of the tensor rate: with both operands in shared memory a 128x64x16 product takes
+  // 48 cycles against 64 for 128x128x16).  dQ accumulates at 256; dS (bf16, 64 columns)
+  // goes to one of two buffers after dQ (tile k uses buffer k % 2, chunk q at +16q), so
+  // S of the next tile is computed as soon as every warp has read S (kBarSfree), while
+  // the elementwise warps work on this tile; dP of the next tile follows this tile's dQ
+  // products.  A dS buffer is rewritten two tiles later, after the dP product issued
+  // behind that tile's dQ products has completed.
   static constexpr uint32_t kColDQ = 256;
+  static constexpr uint32_t kColDS = 256 + D;
 };
 
 struct DqParams {
@@ -257,9 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout));
     if (ok) {
       tc_fence_after();
-      // Key tiles in halves of 64 keys, ping-pong: S and dP of the next tile's half 0 are
-      // issued as soon as this tile's half 0 has been handed back (dS in TMEM and its dQ
-      // products issued), while the other warpgroup still works on half 1.
+      // Per key tile: S of the next tile once every warp has read this tile's S, the dQ
+      // products chunk by chunk as dS arrives, then dP of the next tile.
       auto next_active = [&](int x) {
         while (x < n_ent && !(ents[x].y & active_bit)) ++x;
         return x;
@@ -272,17 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  ((it + 1) / C::kStages) & 1, p.budget, p.err,
                                                  kErrTimeout));
       };
-      auto issue_sdp = [&](int it, int h) {  // S and dP of key half h of the tile at `it`
-        const uint32_t ks = it % C::kStages, vs = (it + 1) % C::kStages;
-        if (elect_one()) {
-          issue_half<D>(tmem + 128 * h, q_desc, kv_kdesc + ks * kSlot16 + h * kHalfRows16);
-          issue_half<D>(tmem + 128 * h + 64, do_desc, kv_kdesc + vs * kSlot16 + h * kHalfRows16);
-          mma_commit(BAR(C::kBarS + h));
-          if (h == 1) mma_commit(BAR(C::kBarEmpty + vs));  // V is no longer needed
-        }
-        __syncwarp();
-      };
-      // whole tiles: S and dP of the tile whose K and V copies are at `it`
+      // S and dP of the tile whose K and V copies are at `it`
       auto issue_s = [&](int it) {
         if (elect_one()) {
           issue_tile<D>(tmem, q_desc, kv_kdesc + (it % C::kStages) * kSlot16);
@@ -305,16 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_kv(0)) ok = false;
         if (ok) {
           tc_fence_after();
-          if constexpr (C::kWhole) {
-            issue_s(0);
-            issue_dp(0);
-          } else {
-            issue_sdp(0, 0);
-            issue_sdp(0, 1);
-          }
+          issue_s(0);
+          issue_dp(0);
         }
       }
-      while (C::kWhole && ok && n < n_ent) {
+      while (ok && n < n_ent) {
         const int n1 = next_active(n + 1);
         const uint32_t ks = it % C::kStages;
         const uint32_t par = done & 1;
@@ -345,41 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
         __syncwarp();
         if (n1 < n_ent) issue_dp(it + 2);  // every chunk has read this tile's dP
-        it += 2;
-        ++done;
-        n = n1;
-      }
-      while (!C::kWhole && ok && n < n_ent) {
-        const int n1 = next_active(n + 1);
-        const uint32_t ks = it % C::kStages;
-        const uint32_t par = done & 1;
-        for (int h = 0; h < 2 && ok; ++h) {
-          // dQ += dS K over this half's keys, 32 at a time as the chunks arrive
-          for (int c = 0; c < 2; ++c) {
-            const int q = 2 * h + c;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), par, p.budget, p.err,
-                                                   kErrTimeout))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (elect_one())
-              issue_acc_chunk<D>(tmem + C::kColDQ, tmem + 128 * h + 16 * c,
-                                 kv_mndesc + ks * kSlot16, q, done > 0);
-            __syncwarp();
-          }
-          if (!ok) break;
-          if (h == 1 && elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
-          __syncwarp();
-          if (n1 < n_ent) {
-            if (h == 0 && !wait_kv(it + 2)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_sdp(it + 2, h);
-          }
-        }
         it += 2;
         ++done;
         n = n1;
@@ -429,104 +378,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row's mask words, computed before the wait so that they overlap the products
       uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (!(e.y & full_bit)) row_mask(make_predicate(m, cm, e, i), w);
-      if constexpr (C::kWhole) {
-        // P of this warpgroup's 64 keys from S (while dP is still being computed), then
-        // dS = scale P (dP - D) chunk by chunk as dP arrives
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 0), sph, p.budget, p.err, kErrTimeout)))
-          break;
-        tc_fence_after();
-        if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
-        float pr[2][32];
-        {
-          uint32_t sa[32], sb[32];  // this warpgroup's 64 columns of S, one wait
-          tmem_ld32x2(lane_base + 64 * wg, sa, lane_base + 64 * wg + 32, sb);
-          tc_fence_before();
-          __syncwarp();  // every lane has read S before lane 0 arrives for the warp
-          if (lane == 0) mbar_arrive(BAR(C::kBarSfree));
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const uint32_t* sv = qq ? sb : sa;
-            const uint32_t wq = wg ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
-#pragma unroll
-            for (int b = 0; b < 16; ++b) {
-              const int c0 = 2 * b;
-              float x0, x1;
-              f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])),
-                                    c2x2, nl2x2), x0, x1);
-              pr[qq][c0] = ((wq >> c0) & 1u) ? fast_exp2(x0) : 0.f;
-              pr[qq][c0 + 1] = ((wq >> (c0 + 1)) & 1u) ? fast_exp2(x1) : 0.f;
-            }
-          }
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 1), sph, p.budget, p.err, kErrTimeout)))
-          break;
-        sph ^= 1u;
-        tc_fence_after();
+      // P of this warpgroup's 64 keys from S (while dP is still being computed), then
+      // dS = scale P (dP - D) chunk by chunk as dP arrives
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 0), sph, p.budget, p.err, kErrTimeout)))
+        break;
+      tc_fence_after();
+      if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
+      float pr[2][32];
+      {
+        uint32_t sa[32], sb[32];  // this warpgroup's 64 columns of S, one wait
+        tmem_ld32x2(lane_base + 64 * wg, sa, lane_base + 64 * wg + 32, sb);
+        tc_fence_before();
+        __syncwarp();  // every lane has read S before lane 0 arrives for the warp
+        if (lane == 0) mbar_arrive(BAR(C::kBarSfree));
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
-          const int q = 2 * wg + qq;
-          uint32_t dv[32], pk[16];
-          tmem_ld32(lane_base + 128 + 32 * q, dv);
+          const uint32_t* sv = qq ? sb : sa;
+          const uint32_t wq = wg ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
 #pragma unroll
           for (int b = 0; b < 16; ++b) {
             const int c0 = 2 * b;
-            const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
-                                          dsc2, dterm2);
-            float g0, g1;
-            f32x2_split(mul_f32x2(f32x2(pr[qq][c0], pr[qq][c0 + 1]), t2), g0, g1);
-            pk[b] = pack_bf16x2(g0, g1);
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])),
+                                  c2x2, nl2x2), x0, x1);
+            pr[qq][c0] = ((wq >> c0) & 1u) ? fast_exp2(x0) : 0.f;
+            pr[qq][c0 + 1] = ((wq >> (c0 + 1)) & 1u) ? fast_exp2(x1) : 0.f;
           }
-          tmem_st16(lane_base + C::kColDS + 64 * (n_done & 1) + 16 * q, pk);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
-          if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
         }
-        ++n_done;
-        continue;
       }
-      const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
-      if (!__all_sync(0xffffffffu, got)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 1), sph, p.budget, p.err, kErrTimeout)))
+        break;
       sph ^= 1u;
       tc_fence_after();
-      if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
-      // dS = scale P (dP - D) with P = 2^(s scale log2 e - LSE log2 e), 32 columns at a
-      // time; the bf16 result of chunk qq lands over this half's S, already loaded
-      {
-        const int h = wg;
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
-        const int q = 2 * h + qq;
-        // S and dP of the chunk's 32 keys (dS of chunk 0 lands over columns 0-15 of S,
-        // which chunk 1 does not read)
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2(lane_base + 128 * h + 32 * qq, sv, lane_base + 128 * h + 64 + 32 * qq, dv);
-        uint32_t pk[16];
-        const uint32_t wq = h ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
-        const bool all = wq == 0xffffffffu;
+        const int q = 2 * wg + qq;
+        uint32_t dv[32], pk[16];
+        tmem_ld32(lane_base + 128 + 32 * q, dv);
 #pragma unroll
         for (int b = 0; b < 16; ++b) {
           const int c0 = 2 * b;
-          float x0, x1;
-          f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])), c2x2,
-                                nl2x2), x0, x1);
-          float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          if (!all) {
-            if (!((wq >> c0) & 1u)) p0 = 0.f;
-            if (!((wq >> (c0 + 1)) & 1u)) p1 = 0.f;
-          }
           const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
                                         dsc2, dterm2);
           float g0, g1;
-          f32x2_split(mul_f32x2(f32x2(p0, p1), t2), g0, g1);
+          f32x2_split(mul_f32x2(f32x2(pr[qq][c0], pr[qq][c0 + 1]), t2), g0, g1);
           pk[b] = pack_bf16x2(g0, g1);
         }
-        tmem_st16(lane_base + 128 * h + 16 * qq, pk);  // over this half's own S
+        tmem_st16(lane_base + C::kColDS + 64 * (n_done & 1) + 16 * q, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
         if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
-      }
       }
       ++n_done;
     }
