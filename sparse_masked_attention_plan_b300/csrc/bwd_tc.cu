@@ -600,9 +600,25 @@ __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, in
     return;
   }
   const int jc = j - q0;  // the key's own column
+  const bool colbit = ki.colbit;
+  if (kind == kKindBand && m.dilation == 1 && !m.rand_block) {
+    // the common band tile as one span per word: causal, the window [jc, jc + w - 1]
+    // or, for a strided or global key, every later row [jc, 127] (which contains it);
+    // bidirectional, [jc - r, jc + r] or every row
+    int lo = 0, hi = kTile - 1;
+    if (m.causal) {
+      lo = jc;
+      if (!colbit && m.window) hi = jc + static_cast<int>(m.window) - 1;
+    } else if (!colbit && m.radius >= 0) {
+      lo = jc - static_cast<int>(m.radius);
+      hi = jc + static_cast<int>(m.radius);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = span_bits(lo, hi, 32 * k);
+    return;
+  }
   const int cut = m.causal ? jc : 0;
   uint32_t extra[4] = {0u, 0u, 0u, 0u};
-  const bool colbit = ki.colbit;
   if (m.rand_block && !(kind == kKindRandom && colbit)) {
     for (int x = ki.rt_lo; x < ki.rt_hi; ++x) {
       const int r0 = p.rt_qb[x] * m.rand_block - q0;
