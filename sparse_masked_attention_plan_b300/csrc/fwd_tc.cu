@@ -17,15 +17,11 @@
 //   warps 4-7  the same for query tile 1
 //   warp 8     TMA producer: Q tiles once, then K and V tiles into a ring of slots
 //   warp 9     MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V, tcgen05
-// TMEM (512 columns), d = 128: S0 [0,128), S1 [128,256), O0 [256,256+d), O1
-// [256+d,256+2d); P_t (bf16) overwrites the first 64 columns of S_t and feeds the PV
-// product directly from TMEM.  The MMA issue order
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d);
+// P_t (bf16) overwrites the first 64 columns of S_t and feeds the PV product directly
+// from TMEM.  The MMA issue order
 //     S0(n), PV1(n-1), S1(n), PV0(n)
 // lets the softmax of one query tile overlap the other tile's two products.
-// d = 64 leaves room for P_t in columns of its own (S 0-255, P 256-383, O 384-511):
-// the softmax hands S_t back as soon as it has loaded it, so S_t(n+1) runs on the
-// tensor cores while the exponentials of S_t(n) are computed, and the softmax waits for
-// PV_t(n-1) before it overwrites P_t or rescales O_t.
 // Online softmax in fp32 with the exp2 form and a conditional rescale: the running
 // maximum moves (and O is rescaled) only when a row maximum grows by more than
 // 2^8; the final O / l and LSE use the same stale maximum, so the result is exact.
@@ -60,26 +56,24 @@ struct TcCfg {
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
-  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_final, one that
-  // nothing ever arrives on (the wait-timeout test waits on it), and (d = 64 only)
-  // s_free[2] (the softmax has loaded S_t) and pv_done[2] (PV_t has completed)
+  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_final, and one that
+  // nothing ever arrives on (the wait-timeout test waits on it)
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
                        kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
                        kBarO = 2 * kStages + 5, kBarNever = 2 * kStages + 6,
-                       kBarSfree = 2 * kStages + 7, kBarPVdone = 2 * kStages + 9,
-                       kNumBars = 2 * kStages + 11;
+                       kNumBars = 2 * kStages + 7;
   // split items: the two query tiles' row maxima and sums, [tile][2][row] fp32
   static constexpr int kSmemX = 2 * 2 * kTile * 4;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kSmemX + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
-  // d = 128: S_t [128t, 128t+128), P_t over the first 64 columns of S_t, O_t at 256 + d t.
-  // d = 64 (room for separate P): S_t at 128t, P_t [256 + 64t, +64), O_t at 384 + 64t, so
-  // the next tile's S_t can be computed while the softmax still works on P_t.
-  static constexpr bool kSepP = D == 64;
+  // TMEM: S_t [128t, 128t+128), P_t (bf16) over the first 64 columns of S_t, O_t at
+  // 256 + d t.  (At d = 64 a layout with P_t in columns of its own, so that the next S_t
+  // could be computed while the softmax works, was measured slower on the 16K-token
+  // workload: 0.219 against 0.213 ms.)
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;  // S of query tile 0, 1
-  static constexpr uint32_t kColP0 = kSepP ? 256 : kColS0, kColP1 = kSepP ? 320 : kColS1;
-  static constexpr uint32_t kColO0 = kSepP ? 384 : 256, kColO1 = kSepP ? 448 : 256 + D;
+  static constexpr uint32_t kColP0 = kColS0, kColP1 = kColS1;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
 
 struct KParams {
@@ -183,10 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::kBarP + 1), 4);
     mbar_init(BAR(C::kBarO), 1);
     mbar_init(BAR(C::kBarNever), 1);
-    mbar_init(BAR(C::kBarSfree + 0), 4);
-    mbar_init(BAR(C::kBarSfree + 1), 4);
-    mbar_init(BAR(C::kBarPVdone + 0), 1);
-    mbar_init(BAR(C::kBarPVdone + 1), 1);
     fence_barrier_init();
   }
   if (warp == kLoadWarp && lane == 0) {
@@ -267,82 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, !p.inject_timeout ||
                                           mbar_wait(BAR(C::kBarNever), 0, p.budget, p.err, kErrTimeout));
     ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout));
-    if (ok && C::kSepP) {
-      tc_fence_after();
-      // d = 64: S_t(n+1) goes out as soon as the softmax has loaded S_t(n) (s_free), so
-      // it overlaps that softmax; PV_t(n) follows P_t(n) and signals pv_done.
-      uint32_t fph[2] = {0u, 0u}, pph[2] = {0u, 0u};
-      bool s_issued[2] = {false, false};  // an S_t is outstanding (its s_free still due)
-      bool oinit[2] = {false, false};
-      auto issue_s = [&](int n, int t) -> bool {  // S_t of entry n (K slot of entry n)
-        const int kit = 2 * n;
-        if (s_issued[t]) {  // the previous S_t must have been loaded by the softmax
-          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarSfree + t), fph[t], p.budget,
-                                                 p.err, kErrTimeout)))
-            return false;
-          fph[t] ^= 1u;
-        }
-        if (elect_one()) {
-          issue_qk<D>(tmem + (t ? C::kColS1 : C::kColS0), t ? q1_desc : q0_desc,
-                      kv_kdesc + (kit % C::kStages) * kSlot16);
-          mma_commit(BAR(C::kBarS + t));
-        }
-        __syncwarp();
-        s_issued[t] = true;
-        ++walked;
-        return true;
-      };
-      auto wait_full = [&](int it) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + it % C::kStages),
-                                                 (it / C::kStages) & 1, p.budget, p.err,
-                                                 kErrTimeout));
-      };
-      int4 e_cur = ents[0];
-      if (n_ent > 0) {
-        ok = wait_full(0);
-        if (ok) {
-          tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t)
-            if (e_cur.y & (kActive0 << t)) ok = issue_s(0, t);
-          if (ok && elect_one()) mma_commit(BAR(C::kBarEmpty + 0));
-          __syncwarp();
-        }
-      }
-      for (int n = 0; ok && n < n_ent; ++n) {
-        const int4 e_nx = n + 1 < n_ent ? ents[n + 1] : make_int4(0, 0, 0, 0);
-        if (n + 1 < n_ent) {  // the next entry's S products first
-          if (!wait_full(2 * (n + 1))) { ok = false; break; }
-          tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t)
-            if (e_nx.y & (kActive0 << t)) ok = issue_s(n + 1, t);
-          if (!ok) break;
-          if (elect_one()) mma_commit(BAR(C::kBarEmpty + (2 * (n + 1)) % C::kStages));
-          __syncwarp();
-        }
-        const int vit = 2 * n + 1;
-        if (!wait_full(vit)) { ok = false; break; }
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (!(e_cur.y & (kActive0 << t))) continue;
-          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + t), pph[t], p.budget, p.err,
-                                                 kErrTimeout))) { ok = false; break; }
-          pph[t] ^= 1u;
-          tc_fence_after();
-          if (elect_one()) {
-            issue_pv<D>(t ? tmem + C::kColO1 : tmem + C::kColO0,
-                        t ? tmem + C::kColP1 : tmem + C::kColP0,
-                        kv_vdesc + (vit % C::kStages) * kSlot16, oinit[t]);
-            mma_commit(BAR(C::kBarPVdone + t));
-          }
-          __syncwarp();
-          oinit[t] = true;
-        }
-        if (!ok) break;
-        if (elect_one()) mma_commit(BAR(C::kBarEmpty + vit % C::kStages));
-        __syncwarp();
-        e_cur = e_nx;
-      }
-    } else if (ok) {
+    if (ok) {
       tc_fence_after();
       int pend1 = -1;
       uint32_t pend_vs = 0;
@@ -435,7 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
     const uint32_t colS = wg ? C::kColS1 : C::kColS0, colO = wg ? C::kColO1 : C::kColO0;
     const uint32_t colP = wg ? C::kColP1 : C::kColP0;
-    uint32_t pvph = 0;  // d = 64: phase of this tile's pv_done
     const int local = (split ? 0 : wg * kTile) + r;
     int i;
     bool valid;
@@ -468,11 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the whole S row of this thread (one TMEM load), masked where not allowed
       uint32_t sr[kTile];
       tmem_ld128(lane_base + colS, sr);
-      if constexpr (C::kSepP) {  // S_t is in registers: the next S_t may overwrite it
-        tc_fence_before();
-        __syncwarp();  // every lane's load is complete before lane 0 arrives for the warp
-        if (lane == 0) mbar_arrive(BAR(C::kBarSfree + wg));
-      }
       if (partial) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
@@ -499,14 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         lrow *= corr;
       }
       const float msub = (mrow == -INFINITY) ? 0.f : mrow;
-      if constexpr (C::kSepP) {  // P_t and O_t are free once the previous PV_t completed
-        if (n_done > 0) {
-          const bool pv = mbar_wait(BAR(C::kBarPVdone + wg), pvph, p.budget, p.err, kErrTimeout);
-          if (!__all_sync(0xffffffffu, pv)) break;
-          pvph ^= 1u;
-          tc_fence_after();
-        }
-      }
       // P = 2^(s * scale * log2 e - m), stored as bf16 over the first half of S;
       // the scale-and-shift and the row sum run two columns per instruction
       const uint64_t c2x2 = f32x2(c2, c2), nmx2 = f32x2(-msub, -msub);
