@@ -309,7 +309,7 @@ spattn_status spattn_decode_check(void* workspace, void* cuda_stream);
 /*
  * The same forward pass from HOST buffers: copies Q/K/V host -> device, runs
  * spattn_fwd, copies O and LSE device -> host, and returns once everything has
- * completed.  The (batch, head) units are processed in up to 8 chunks of consecutive
+ * completed.  The (batch, head) units are processed in up to 16 chunks of consecutive
  * units as a pipeline: the host -> device copy of chunk k+1 (on a copy stream the
  * plan owns), the forward of chunk k (on `cuda_stream`) and the device -> host copy of
  * chunk k-1 (a second plan-owned stream) run at the same time; the copies start after

@@ -129,7 +129,7 @@ struct spattn_plan {
   // spattn_fwd_host: a copy-in and a copy-out stream and the per-chunk events of its
   // pipeline (host -> device of chunk k+1, forward of chunk k, device -> host of chunk
   // k-1), created on first use on the plan's device
-  static constexpr int kHostChunks = 8;
+  static constexpr int kHostChunks = 16;
   cudaStream_t host_in = nullptr, host_out = nullptr;
   cudaEvent_t host_ev[2 * kHostChunks + 2] = {};
 
