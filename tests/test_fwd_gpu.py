@@ -144,14 +144,15 @@ def test_host_buffer_entry_matches_device_entry(oracle_mod):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("B,H,with_lse", [(3, 5, True), (1, 1, True), (2, 8, False), (1, 19, True)])
+@pytest.mark.parametrize("B,H,with_lse", [(3, 5, True), (1, 1, True), (2, 8, False), (1, 19, True),
+                                           (2, 19, True)])
 def test_host_buffer_pipeline_chunks(B, H, with_lse, dtype):
-    """The host-buffer entry splits the (batch, head) units into up to 8 chunks whose
-    copies overlap the forward of their neighbours: uneven chunk counts (15 units in
-    chunks of 2, 19 in chunks of 3, a single unit), packed strided / global columns
-    (plan scratch reused across chunks), with and without LSE, both dtypes, equal bit
-    for bit to one device call; and a second call on the same plan after work queued
-    on the stream writes the device buffers."""
+    """The host-buffer entry splits the (batch, head) units into chunks whose copies
+    overlap the forward of their neighbours: unit counts that do and do not divide
+    evenly (15, 16, 19, a single unit), packed strided / global columns (plan scratch
+    reused across chunks), with and without LSE, both dtypes, equal bit for bit to one
+    device call; and a second call on the same plan after work queued on the stream
+    writes the device buffers."""
     T, d = 700, 64
     plan = sp.Plan(T, d, causal=1, window=150, stride=48, offset=7, global_pos=[3, 333])
     Q, K, V = W.qkv(B, H, T, d, 21, dtype)
