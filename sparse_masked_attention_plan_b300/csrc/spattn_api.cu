@@ -227,9 +227,9 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
     if (cnt > 0) items.push_back({static_cast<int32_t>(r0), off, cnt, 0});
   }
   // global rows: every key that causality permits.  A group whose rows fit in one
-  // query tile is split (d = 64 only, where the kernel's separate P columns let the two
-  // query tiles overlap): both tiles hold its rows and take alternate key tiles, so the
-  // dense walk that every global row needs runs at two tiles per entry pair.
+  // query tile is split (d = 64 only, where it was measured faster): both tiles hold its
+  // rows and take alternate key tiles, so the dense walk that every global row needs
+  // runs at two tiles per entry pair.
   const int64_t ng = static_cast<int64_t>(p->gpos.size());
   for (int64_t q0 = 0; q0 < ng; q0 += group_rows) {
     const int32_t off = static_cast<int32_t>(s->entries.size() / 4);
