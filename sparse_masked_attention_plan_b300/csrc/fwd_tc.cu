@@ -17,6 +17,8 @@
 //   warps 4-7  the same for query tile 1
 //   warp 8     TMA producer: Q tiles once, then K and V tiles into a ring of slots
 //   warp 9     MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V, tcgen05
+//              (d = 64 schedules whose entries are often read by one query tile only:
+//              warps 9 and 10, one per query tile, 352 threads)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d);
 // P_t (bf16) overwrites the first 64 columns of S_t and feeds the PV product directly
 // from TMEM.  The MMA issue order
@@ -43,12 +45,11 @@
 namespace spattn {
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;  // with two MMA warps: warps 9 and 10 for query tile 0, 1
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+template <int D, int MW = 1>
 struct TcCfg {
   static constexpr int kChunkBytes = kTile * 64 * 2;  // 128 rows x 64 bf16, one swizzle span
   static constexpr int kChunks = D / 64;
@@ -74,6 +75,13 @@ struct TcCfg {
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;  // S of query tile 0, 1
   static constexpr uint32_t kColP0 = kColS0, kColP1 = kColS1;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  // MW = 2 (d = 64, for schedules in which many entries are read by one query tile
+  // only): one MMA-issuing warp per query tile, each running its tile's chain (S, then
+  // PV once P is in TMEM) without waiting on the other tile's hand-offs; K/V slots are
+  // released by both warps.  With one warp the fixed order S0(n), PV1(n-1), S1(n), PV0(n)
+  // staggers the tiles, which is faster when both read every entry.
+  static constexpr int kMmaWarps = MW;
+  static constexpr int kThreads = 32 * (kMmaWarp + MW);
 };
 
 struct KParams {
@@ -118,13 +126,15 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
            (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int MW>
+__global__ void __launch_bounds__(TcCfg<D, MW>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQg,
                   const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
                   const KParams p) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, MW>;
+  static_assert(C::kIdescQK == TcCfg<D>::kIdescQK && C::kIdescPV == TcCfg<D>::kIdescPV,
+                "the issue helpers use the one-warp configuration's shapes");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -166,7 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(BAR(C::kBarFull + s), 1);
-      mbar_init(BAR(C::kBarEmpty + s), 1);
+      // one arrival per MMA-issuing warp: a commit after its products read the slot, or a
+      // plain arrival (after the slot's copy landed) when its query tile skips the entry
+      mbar_init(BAR(C::kBarEmpty + s), C::kMmaWarps);
     }
     mbar_init(BAR(C::kBarQ), 1);
     mbar_init(BAR(C::kBarS + 0), 1);
@@ -175,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // hand-off off the critical path: 128 arrivals on one barrier word serialise)
     mbar_init(BAR(C::kBarP + 0), 4);
     mbar_init(BAR(C::kBarP + 1), 4);
-    mbar_init(BAR(C::kBarO), 1);
+    mbar_init(BAR(C::kBarO), C::kMmaWarps);
     mbar_init(BAR(C::kBarNever), 1);
     fence_barrier_init();
   }
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kErrTimeout);
     mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);  // the Q tiles too
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || (C::kMmaWarps == 2 && warp == kMmaWarp + 1)) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop and waits; one elected lane (always lane 0 of the
     // converged warp, so commits track its own products) issues MMAs and commits.
@@ -257,7 +269,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, !p.inject_timeout ||
                                           mbar_wait(BAR(C::kBarNever), 0, p.budget, p.err, kErrTimeout));
     ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout));
-    if (ok) {
+    if (ok && C::kMmaWarps == 2) {
+      // query tile t = warp - 9: S_t(n), then PV_t(n) once P_t(n) is in TMEM (the next
+      // S_t overwrites P_t, so it follows in issue order)
+      tc_fence_after();
+      const int t = warp - kMmaWarp;
+      const uint64_t q_desc = t ? q1_desc : q0_desc;
+      const uint32_t colS = t ? C::kColS1 : C::kColS0, colO = t ? C::kColO1 : C::kColO0;
+      uint32_t pph = 0u;
+      bool oinit = false;
+      auto wait_full = [&](int it) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + it % C::kStages),
+                                                 (it / C::kStages) & 1, p.budget, p.err,
+                                                 kErrTimeout));
+      };
+      auto release = [&](int it, bool used) {  // this warp's arrival on the slot of `it`
+        if (elect_one()) {
+          if (used) mma_commit(BAR(C::kBarEmpty + it % C::kStages));
+          else mbar_arrive(BAR(C::kBarEmpty + it % C::kStages));
+        }
+        __syncwarp();
+      };
+      int4 e_next = ents[0];
+      for (int n = 0; n < n_ent && ok; ++n) {
+        const int4 e = e_next;
+        if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: global latency off the issue path
+        const bool a = (e.y & (kActive0 << t)) != 0;
+        const int kit = 2 * n, vit = 2 * n + 1;
+        if (!wait_full(kit)) { ok = false; break; }
+        tc_fence_after();
+        if (a) {
+          if (elect_one()) {
+            issue_qk<D>(tmem + colS, q_desc, kv_kdesc + (kit % C::kStages) * kSlot16);
+            mma_commit(BAR(C::kBarS + t));
+          }
+          __syncwarp();
+          ++walked;
+        }
+        release(kit, a);
+        if (!wait_full(vit)) { ok = false; break; }
+        tc_fence_after();
+        if (a) {
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + t), pph, p.budget, p.err,
+                                                 kErrTimeout))) { ok = false; break; }
+          pph ^= 1u;
+          tc_fence_after();
+          if (elect_one())
+            issue_pv<D>(tmem + colO, tmem + colS, kv_vdesc + (vit % C::kStages) * kSlot16, oinit);
+          __syncwarp();
+          oinit = true;
+        }
+        release(vit, a);
+      }
+    } else if (ok) {
       tc_fence_after();
       int pend1 = -1;
       uint32_t pend_vs = 0;
@@ -534,14 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int D>
+template <int D, int MW>
 cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, MW>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::kSmemBytes);
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, MW>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const long long T = a.mask.T;  // rows per residue class
@@ -578,8 +642,8 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
     *why = "too many work items";
     return cudaErrorInvalidValue;
   }
-  fwd_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, st>>>(mQ, mK, mV, mQg,
-                                                                                  mKc, mVc, kp);
+  fwd_tc_kernel<D, MW><<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, st>>>(
+      mQ, mK, mV, mQg, mKc, mVc, kp);
   return cudaGetLastError();
 }
 
@@ -587,8 +651,8 @@ cudaError_t launch_d(const TcArgs& a, cudaStream_t st, const char** why) {
 
 cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why) {
   if (a.n_items == 0) return cudaSuccess;
-  if (d == 64) return launch_d<64>(a, st, why);
-  if (d == 128) return launch_d<128>(a, st, why);
+  if (d == 64) return a.mma_per_tile ? launch_d<64, 2>(a, st, why) : launch_d<64, 1>(a, st, why);
+  if (d == 128) return launch_d<128, 1>(a, st, why);
   *why = "head dim must be 64 or 128";
   return cudaErrorInvalidValue;
 }

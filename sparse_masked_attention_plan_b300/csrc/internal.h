@@ -62,6 +62,10 @@ struct Schedule {
   int64_t tile_products = 0;  // (query tile x key tile) products per (batch, head)
   int32_t n_major = 0;        // leading items (>= 1.5x the median length) launched first
   int32_t n_packed_units = 0;  // key-major schedule: packed units come first
+  // forward at d = 64: fewer than 80 % of the (entry, query tile) slots are products
+  // (entries that one query tile skips, e.g. random blocks): the kernel with one
+  // MMA-issuing warp per query tile is then faster than the one-warp issue order
+  int32_t mma_per_tile = 0;
 };
 
 }  // namespace spattn
@@ -211,6 +215,7 @@ struct TcArgs {
   int32_t inject_timeout = 0;
   int32_t n_major = 0;
   int32_t dview = 1;  // residue classes of a dilated view (mask.T is then T / dview)
+  int32_t mma_per_tile = 0;  // see Schedule::mma_per_tile
 };
 cudaError_t launch_fwd_tc(int d, const TcArgs& a, cudaStream_t st, const char** why);
 

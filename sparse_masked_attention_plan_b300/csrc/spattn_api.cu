@@ -256,6 +256,10 @@ void build_schedule(const spattn_plan* p, spattn::Schedule* s, int group_rows, i
     if (cnt > 0)
       items.push_back({static_cast<int32_t>(q0), off, cnt, kItemGathered | (split ? kItemSplit : 0)});
   }
+  {
+    const int64_t n_ent = static_cast<int64_t>(s->entries.size() / 4);
+    s->mma_per_tile = (p->d == 64 && n_qtiles == 2 && 5 * s->tile_products < 8 * n_ent) ? 1 : 0;
+  }
   if (longest_first)
     std::stable_sort(items.begin(), items.end(),
                      [](const Item& x, const Item& y) { return x.cnt > y.cnt; });
@@ -392,6 +396,7 @@ void spattn::select_schedule(const spattn_plan* p, bool bf16, TcArgs* a) {
   a->colmask = view ? p->d_colmask_res : p->d_colmask;
   a->n_cols = view ? 0 : p->n_cols;
   a->dview = view ? p->dview : 1;
+  a->mma_per_tile = s.mma_per_tile;
 }
 
 void spattn::fill_fwd_args(const spattn_plan* p, bool bf16, int64_t BH, const void* Q,
