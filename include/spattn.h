@@ -165,9 +165,10 @@ spattn_status spattn_plan_copy_columns(const spattn_plan* plan, int32_t* cols, i
  *          unit is packed sparse columns C[key0 .. key0+63] (these come first),
  *          else natural keys key0 .. key0+63.  Its entries are 64-row query groups
  *          {q0, flags, a, b}: flags bits 4-5 kind as above, bit 0: q0 indexes
- *          global_pos (rows gathered from the global list); a packed entry reads
- *          packed columns [a, b) of its unit.  Rows that are global tokens take
- *          part only in gathered entries.
+ *          global_pos (rows gathered from the global list); bit 1: the local
+ *          window alone allows every pair of the group's rows and the unit's keys
+ *          (band entries only); a packed entry reads packed columns [a, b) of its
+ *          unit.  Rows that are global tokens take part only in gathered entries.
  * which = 4: the same at 128-key units and 128-row groups: the schedule of the
  *          bf16 (tensor-core) dK/dV kernel.  Entry kind 3 (both key-major forms and
  *          the forward forms) is a key tile outside the band that only BigBird random

@@ -59,7 +59,6 @@ struct DqCfg {
                        kBarDone = 2 * kStages + 7, kBarSfree = 2 * kStages + 8,
                        kNumBars = 2 * kStages + 9;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0, 0);  // dK/dV kernel
   static constexpr uint32_t kIdescFull = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
   // Whole-tile products: S = Q K^T (TMEM 0) and dP = dO V^T (TMEM 128) of all 128 keys
@@ -91,20 +90,6 @@ struct DqParams {
   int dview;  // residue classes of a dilated view (1: rows are the sequence itself)
   int T_out;  // sequence length (the mask's T times dview)
 };
-
-// A (128 rows) x B^T (64 rows, one half of a 128-row tile), both K-major over d: the
-// S and dP products of one tile half.  The B descriptor points at the half's first row
-// (64 rows x 128 bytes = 8 KB into each 64-column chunk).
-template <int D>
-__device__ __forceinline__ void issue_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
-  using C = DqCfg<D>;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, a_desc + off16, b_desc + off16, C::kIdescHalf, kk > 0 ? 1u : 0u);
-  }
-}
-constexpr uint32_t kHalfRows16 = (64 * 128) >> 4;  // descriptor offset of a tile's row 64
 
 // A (128 rows) x B^T (128 rows), both K-major over d: a whole-tile S or dP product.
 template <int D>
@@ -504,16 +489,23 @@ struct KvCfg {
   static constexpr int kStages = D == 128 ? 2 : 4;  // one stage = the Q and dO tiles
   static constexpr int kSmemKV = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * 2 * kTileBytes;
-  // LSE and D of each warpgroup's 64 query columns, double-buffered: [wg][buf][2][64]
-  static constexpr int kSmemVec = 2 * 2 * 2 * 64 * 4;
-  // kBarP + q: chunk q (queries 32q .. 32q+31) of P^T and dS^T is in TMEM
+  // four elementwise warpgroups (warpgroup q owns query chunk q of every tile), then the
+  // TMA warp and the MMA warp
+  // (18 warps: up to 5 on one SM sub-partition, whose 16K registers leave 96 per thread)
+  static constexpr int kLoadWarp = 16, kMmaWarp = 17, kThreads = 32 * (kMmaWarp + 1);
+  // LSE and D of each elementwise warp's 32 query columns: [warp][2][32]
+  static constexpr int kSmemVec = 16 * 2 * 32 * 4;
+  // kBarS + 0 / + 1: S^T / dP^T of the query tile are in TMEM; kBarP / kBarDS: every
+  // elementwise warp has written its rows of P^T / dS^T (one arrival per warp)
   static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages,
                        kBarS = 1 + 2 * kStages, kBarP = 3 + 2 * kStages,
-                       kBarDone = 7 + 2 * kStages, kBarVec = 8 + 2 * kStages,
-                       kNumBars = 12 + 2 * kStages;  // kBarVec + 2 wg + buf
+                       kBarDS = 4 + 2 * kStages, kBarDone = 5 + 2 * kStages,
+                       kNumBars = 6 + 2 * kStages;
   static constexpr int kSmemBytes = kSmemKV + kSmemRing + kSmemVec + kNumBars * 8 + 16 + 1024;
-  // products use the dQ kernel's issue helpers (same shapes: 128 x 64 and 128 x d).
-  // TMEM: query half h has S^T at 128h and dP^T at 128h + 64; dV, dK after them
+  // products use the dQ kernel's issue helpers (128 x 128 tiles and 128 x d chunks).
+  // TMEM: S^T of the whole query tile at 0 (query q in column q), dP^T at 128; chunk c
+  // (queries 32c .. 32c+31) writes its P^T and dS^T (bf16 pairs) over the first 16 of
+  // its own 32 columns of each; dV, dK after them
   static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 };
 
@@ -574,17 +566,16 @@ __device__ __forceinline__ KeyInfo key_info(const KvParams& p, int j) {
   return k;
 }
 
-// The query columns of the tile at row q0 that may read key j (packed index c_pk for
-// packed units), for an entry of `kind`; rows that are not rows of the tile are
-// removed separately (LSE = +inf).
-__device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, int q0, int j,
-                                         int c_pk, const KeyInfo& ki, uint32_t (&w)[4]) {
+// Word k (rows 32k .. 32k+31) of the query rows of the tile at row q0 that may read key
+// j (packed index c_pk for packed units), for an entry of `kind`; rows that are not rows
+// of the tile are removed separately (LSE = +inf).  The band tile with a contiguous
+// window and no random blocks is one span; other band and random tiles build all four
+// words and return word k.
+__device__ __forceinline__ uint32_t key_word(const KvParams& p, int kind, int4 e, int q0, int j,
+                                             int c_pk, const KeyInfo& ki, int k) {
   const MaskDev& m = p.mask;
-  w[0] = w[1] = w[2] = w[3] = 0u;
-  if (kind == kKindPacked) {
-    if (c_pk >= e.z && c_pk < e.w) w[0] = w[1] = w[2] = w[3] = 0xffffffffu;
-    return;
-  }
+  const int base = 32 * k;
+  if (kind == kKindPacked) return (c_pk >= e.z && c_pk < e.w) ? 0xffffffffu : 0u;
   if (kind == kKindDense) {  // gathered global rows q0 .. : every key j <= their position
     const int nr = min(kTile, m.n_global - q0);
     int r0 = 0;
@@ -596,15 +587,13 @@ __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, in
       }
       r0 = lo;
     }
-    add_span(r0, nr - 1, w);
-    return;
+    return span_bits(r0, nr - 1, base);
   }
   const int jc = j - q0;  // the key's own column
   const bool colbit = ki.colbit;
   if (kind == kKindBand && m.dilation == 1 && !m.rand_block) {
-    // the common band tile as one span per word: causal, the window [jc, jc + w - 1]
-    // or, for a strided or global key, every later row [jc, 127] (which contains it);
-    // bidirectional, [jc - r, jc + r] or every row
+    // causal: the window [jc, jc + w - 1] or, for a strided or global key, every later
+    // row [jc, 127] (which contains it); bidirectional: [jc - r, jc + r] or every row
     int lo = 0, hi = kTile - 1;
     if (m.causal) {
       lo = jc;
@@ -613,10 +602,9 @@ __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, in
       lo = jc - static_cast<int>(m.radius);
       hi = jc + static_cast<int>(m.radius);
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = span_bits(lo, hi, 32 * k);
-    return;
+    return span_bits(lo, hi, base);
   }
+  uint32_t w[4];
   const int cut = m.causal ? jc : 0;
   uint32_t extra[4] = {0u, 0u, 0u, 0u};
   if (m.rand_block && !(kind == kKindRandom && colbit)) {
@@ -627,30 +615,32 @@ __device__ __forceinline__ void key_mask(const KvParams& p, int kind, int4 e, in
   }
   if (kind == kKindRandom) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = extra[k];
-    return;
-  }
-  if (colbit) add_span(cut, kTile - 1, extra);
-  RowPredicate pr;
-  const int d = m.dilation;
-  if (m.causal) {
-    pr.lo = jc;
-    pr.hi = m.window ? jc + (m.window - 1) * d : m.T - 1 - q0;
+    for (int x = 0; x < 4; ++x) w[x] = extra[x];
   } else {
-    pr.lo = m.radius >= 0 ? jc - m.radius * d : 0;
-    pr.hi = m.radius >= 0 ? jc + m.radius * d : kTile - 1;
-  }
-  pr.hi = min(pr.hi, kTile - 1);
-  pr.hb = kTile - 1;
-  pr.dil = d;
-  pr.res = d == 1 ? 0 : ((jc % d) + d) % d;  // no division when d = 1
+    if (colbit) add_span(cut, kTile - 1, extra);
+    RowPredicate pr;
+    const int d = m.dilation;
+    if (m.causal) {
+      pr.lo = jc;
+      pr.hi = m.window ? jc + (m.window - 1) * d : m.T - 1 - q0;
+    } else {
+      pr.lo = m.radius >= 0 ? jc - m.radius * d : 0;
+      pr.hi = m.radius >= 0 ? jc + m.radius * d : kTile - 1;
+    }
+    pr.hi = min(pr.hi, kTile - 1);
+    pr.hb = kTile - 1;
+    pr.dil = d;
+    pr.res = d == 1 ? 0 : ((jc % d) + d) % d;  // no division when d = 1
 #pragma unroll
-  for (int k = 0; k < 4; ++k) pr.bits[k] = extra[k];
-  row_mask(pr, w);
+    for (int x = 0; x < 4; ++x) pr.bits[x] = extra[x];
+    row_mask(pr, w);
+  }
+  // word k by value: w stays in registers
+  return k == 0 ? w[0] : (k == 1 ? w[1] : (k == 2 ? w[2] : w[3]));
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmQg, const __grid_constant__ CUtensorMap tmdOg,
@@ -663,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = smem_addr(smem);
   const uint32_t sV = sK + C::kTileBytes;
   const uint32_t sRing = sK + C::kSmemKV;  // stage s: Q at +0, dO at +kTileBytes
-  float* s_vec = reinterpret_cast<float*>(smem + C::kSmemKV + C::kSmemRing);  // [wg][buf][LSE, D][64]
+  float* s_vec = reinterpret_cast<float*>(smem + C::kSmemKV + C::kSmemRing);  // [warp][LSE, D][32]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemKV + C::kSmemRing + C::kSmemVec);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   const uint32_t bar0 = smem_addr(bars);
@@ -685,14 +675,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::kBarS + 0), 1);
     mbar_init(BAR(C::kBarS + 1), 1);
-    // one arrival per warp of the warpgroup on the chunk hand-off and on the per-query
-    // vector exchange
-    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 4);
+    // one arrival per elementwise warp on the P^T and dS^T hand-offs
+    mbar_init(BAR(C::kBarP), 16);
+    mbar_init(BAR(C::kBarDS), 16);
     mbar_init(BAR(C::kBarDone), 1);
-    for (int k = 0; k < 4; ++k) mbar_init(BAR(C::kBarVec + k), 4);
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -701,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kLoadWarp) {
+  if (warp == C::kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
       const void* mk = packed_unit ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK);
@@ -748,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kErrTimeout);
     mbar_wait(BAR(C::kBarKV), 0, p.budget, p.err, kErrTimeout);
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
     const uint64_t v_desc = smem_desc_sw128(sV, 16, 1024);
@@ -758,19 +747,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarKV), 0, p.budget, p.err, kErrTimeout));
     if (ok) {
       tc_fence_after();
-      // Query tiles in halves of 64 queries, ping-pong (as in the dQ kernel): the next
-      // tile's half-0 products go out as soon as this tile's half 0 has been handed back.
+      // Whole-tile products (128 x 128 x 16 runs at the full tensor rate; a 64-query
+      // half would take 48 cycles for half the work).  Issue order per query tile n:
+      //   S^T(n), dP^T(n), [P^T(n) written] dV(n), S^T(n+1), [dS^T(n) written] dK(n),
+      //   dP^T(n+1), ...
+      // dV needs only P, so it runs while the warps compute dS; S^T(n+1) overwrites the
+      // P^T(n) columns only after dV(n) (the products execute in issue order), and
+      // dP^T(n+1) the dS^T(n) columns only after dK(n), so the warps compute P of the
+      // next tile while dK and dP run.
       auto wait_q = [&](int n) -> bool {
         return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + n % C::kStages),
                                                  (n / C::kStages) & 1, p.budget, p.err,
                                                  kErrTimeout));
       };
-      auto issue_sdp = [&](int n, int h) {  // S^T and dP^T of query half h of tile n
-        const uint32_t s = n % C::kStages;
+      auto issue_s = [&](int n) {
         if (elect_one()) {
-          issue_half<D>(tmem + 128 * h, k_desc, ring_k + s * kStage16 + h * kHalfRows16);
-          issue_half<D>(tmem + 128 * h + 64, v_desc, ring_k + s * kStage16 + kDo16 + h * kHalfRows16);
-          mma_commit(BAR(C::kBarS + h));
+          issue_tile<D>(tmem, k_desc, ring_k + (n % C::kStages) * kStage16);
+          mma_commit(BAR(C::kBarS + 0));
+        }
+        __syncwarp();
+      };
+      auto issue_dp = [&](int n) {
+        if (elect_one()) {
+          issue_tile<D>(tmem + 128, v_desc, ring_k + (n % C::kStages) * kStage16 + kDo16);
+          mma_commit(BAR(C::kBarS + 1));
         }
         __syncwarp();
       };
@@ -778,43 +778,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_q(0)) ok = false;
         if (ok) {
           tc_fence_after();
-          issue_sdp(0, 0);
-          issue_sdp(0, 1);
+          issue_s(0);
+          issue_dp(0);
         }
       }
       for (int n = 0; ok && n < n_ent; ++n) {
         const uint32_t s = n % C::kStages;
         const uint32_t par = n & 1;
-        for (int h = 0; h < 2 && ok; ++h) {
-          // dV += P^T dO and dK += dS^T Q over this half's queries, chunk by chunk
-          for (int c = 0; c < 2; ++c) {
-            const int q = 2 * h + c;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), par, p.budget, p.err,
-                                                   kErrTimeout))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (elect_one()) {
-              issue_acc_chunk<D>(tmem + C::kColDV, tmem + 128 * h + 16 * c,
-                                 ring_mn + s * kStage16 + kDo16, q, n > 0);
-              issue_acc_chunk<D>(tmem + C::kColDK, tmem + 128 * h + 64 + 16 * c,
-                                 ring_mn + s * kStage16, q, n > 0);
-            }
-            __syncwarp();
-          }
-          if (!ok) break;
-          if (h == 1 && elect_one()) mma_commit(BAR(C::kBarEmpty + s));
-          __syncwarp();
-          if (n + 1 < n_ent) {
-            if (h == 0 && !wait_q(n + 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_sdp(n + 1, h);
-          }
+        // With more than two stages the next tile's Q and dO are long since loaded, as a
+        // rule, and are checked while the warps still compute P, so that S^T(n+1) follows
+        // dV(n) at once; with two (d = 128) the stage is refilled only after dK(n-1), and
+        // the wait is left as late as possible
+        constexpr bool kEarlyQ = C::kStages > 2;
+        if (kEarlyQ && n + 1 < n_ent && !wait_q(n + 1)) break;
+        // dV += P^T dO over the tile's four 32-query chunks
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(BAR(C::kBarP), par, p.budget, p.err, kErrTimeout)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            issue_acc_chunk<D>(tmem + C::kColDV, tmem + 32 * c, ring_mn + s * kStage16 + kDo16, c,
+                               n > 0);
         }
+        __syncwarp();
+        if (n + 1 < n_ent) {
+          if (!kEarlyQ && !wait_q(n + 1)) break;
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        // dK += dS^T Q, then the stage (Q and dO of tile n) is free
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(BAR(C::kBarDS), par, p.budget, p.err, kErrTimeout)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            issue_acc_chunk<D>(tmem + C::kColDK, tmem + 128 + 32 * c, ring_mn + s * kStage16, c,
+                               n > 0);
+          mma_commit(BAR(C::kBarEmpty + s));
+        }
+        __syncwarp();
+        if (n + 1 < n_ent) issue_dp(n + 1);
       }
     }
     if (elect_one()) mma_commit(BAR(C::kBarDone));
@@ -823,7 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise warps
-    const int wg = warp >> 2;  // query-column half (and, in the epilogue, dV or dK)
+    // warpgroup wg: query chunk wg of every tile and, in the epilogue, half of the
+    // columns of dV (wg < 2) or dK
+    const int wg = warp >> 2;
+    const int hh = wg >> 1, qc = wg & 1;
     const int kk = ((warp & 3) << 5) | lane;  // key row of the unit = TMEM lane
     const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
     const int key = unit.x + kk;
@@ -837,82 +847,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sph = 0;
     int n_done = 0;
     const KeyInfo ki = key_info(p, j);
-    // LSE and D of query column 64 wg + kk of an entry (threads kk < 64 of each
-    // warpgroup load their half's columns), one entry ahead so the global loads overlap
-    // the previous tile's work.  The loads are issued unconditionally (a row outside
-    // the sequence reads row 0) and whether the column is a row of the tile (`keep`:
-    // inside the sequence and not a global row, whose gradient comes from its gathered
-    // tile) is decided when the values are used, so nothing waits for them here
-    auto column_values = [&](const int4& e, float& lse_v, float& dd_v, uint32_t& keep) {
-      const int a = e.x + 64 * wg + kk;
+    // LSE and D of query column 32 wg + lane of an entry (every warp loads its
+    // chunk's 32 columns itself), one entry ahead so the global loads overlap the
+    // previous tile's work.  The loads are issued unconditionally (a row outside the
+    // sequence reads row 0) and whether the column is a row of the tile (inside the
+    // sequence and not a global row, whose gradient comes from its gathered tile) is
+    // decided when the values are used (`in_seq` and the loaded `is_global` flag), so
+    // nothing waits for the loads here
+    auto column_values = [&](const int4& e, float& lse_v, float& dd_v, uint32_t& in_seq,
+                             uint32_t& is_global) {
+      const int a = e.x + 32 * wg + lane;
       size_t at;
       if (e.y & kEntryGathered) {  // the row's position comes from the global list
         const int i = a < m.n_global ? m.gpos[a] : -1;
-        keep = i >= 0;
+        in_seq = i >= 0;
+        is_global = 0u;
         at = head + static_cast<size_t>(max(i, 0));
       } else {
         const int i = a < m.T ? a : 0;
-        keep = static_cast<uint32_t>(a < m.T) & (static_cast<uint32_t>(m.rowglobal[i]) ^ 1u);
+        in_seq = a < m.T;
+        is_global = m.rowglobal[i];
         at = head + seq(i);
       }
       lse_v = p.LSE[at];
       dd_v = p.Dvec[at];
     };
+    // this warp's LSE and D: lane l writes column l, every lane reads all 32
+    float* s_lse = s_vec + warp * 64;
+    float* s_dd = s_lse + 32;
+    // entries two ahead, so the next entry's row index is there when its values load
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
+    int4 e_next2 = n_ent > 1 ? ents[1] : make_int4(0, 0, 0, 0);
     float lse_next = 0.f, dd_next = 0.f;
-    uint32_t keep_next = 0u;
-    if (n_ent && kk < 64) column_values(e_next, lse_next, dd_next, keep_next);
+    uint32_t in_next = 0u, glob_next = 0u;
+    if (n_ent) column_values(e_next, lse_next, dd_next, in_next, glob_next);
     for (int n = 0; n < n_ent; ++n) {
       const int4 e = e_next;
+      const bool keep_next = in_next && !glob_next;
       const float lse_cur = keep_next ? lse_next * 1.4426950408889634f : INFINITY;
       const float dd_cur = keep_next ? dd_next * dsc : 0.f;
-      if (n + 1 < n_ent) e_next = ents[n + 1];
+      e_next = e_next2;
+      if (n + 2 < n_ent) e_next2 = ents[n + 2];
       const int kind = (e.y >> kKindShift) & 3;
-      // this warpgroup's 64 query columns' LSE and D, double-buffered per warpgroup:
-      // buffer n & 1 is rewritten at tile n + 2, after all 128 threads of the warpgroup
-      // have passed tile n + 1's barrier (and so have finished tile n); the two
-      // warpgroups never wait for each other
-      float* s_lse = s_vec + (wg * 2 + (n & 1)) * 2 * 64;
-      float* s_dd = s_lse + 64;
-      if (kk < 64) {
-        s_lse[kk] = lse_cur;
-        s_dd[kk] = dd_cur;
-      }
-      __syncwarp();  // this warp's LSE and D values are written before lane 0 arrives
-      if (lane == 0) mbar_arrive(BAR(C::kBarVec + wg * 2 + (n & 1)));
-      if (kk < 64 && n + 1 < n_ent) column_values(e_next, lse_next, dd_next, keep_next);
-      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarVec + wg * 2 + (n & 1)), (n >> 1) & 1,
-                                             p.budget, p.err, kErrTimeout)))
+      __syncwarp();  // every lane has read the previous tile's values
+      s_lse[lane] = lse_cur;
+      s_dd[lane] = dd_cur;
+      __syncwarp();
+      if (n + 1 < n_ent) column_values(e_next, lse_next, dd_next, in_next, glob_next);
+      // this chunk's word of the key's mask (rows 32 wg .. 32 wg + 31 of the tile)
+      uint32_t wq = (e.y & kEntryFull) ? 0xffffffffu : key_word(p, kind, e, e.x, j, key, ki, wg);
+      if (!key_valid) wq = 0u;
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 0), sph, p.budget, p.err, kErrTimeout)))
         break;
-      uint32_t w[4];
-      key_mask(p, kind, e, e.x, j, key, ki, w);
-      if (!key_valid) w[0] = w[1] = w[2] = w[3] = 0u;
-      const bool got = mbar_wait(BAR(C::kBarS + wg), sph, p.budget, p.err, kErrTimeout);
-      if (!__all_sync(0xffffffffu, got)) break;
-      sph ^= 1u;
       tc_fence_after();
+      // S^T of the chunk's 32 queries -> P (kept in fp32 for dS), P^T (bf16 pairs) over
+      // the first 16 of those columns, which only this warpgroup reads
+      const uint32_t cs = lane_base + 32 * wg;
+      const bool all = wq == 0xffffffffu;
+      float pf[32];
       {
-        const int hh = wg;
+        uint32_t sv[32];
+        tmem_ld32(cs, sv);
+        uint32_t pp[16];
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int q = 2 * hh + qq;
-        // S^T and dP^T of the chunk's 32 queries (P^T and dS^T of chunk 0 land over
-        // columns 0-15 of S^T and dP^T, which chunk 1 does not read)
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2(lane_base + 128 * hh + 32 * qq, sv, lane_base + 128 * hh + 64 + 32 * qq, dv);
-        uint32_t pp[16], pg[16];
-        const uint32_t wq = hh ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
-        const bool all = wq == 0xffffffffu;
-#pragma unroll
-        for (int b = 0; b < 16; b += 2) {  // four columns per step: one vector load each
-          const int c0 = 32 * qq + 2 * b;  // column within this warpgroup's 64
-          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c0);
-          const float4 d4 = *reinterpret_cast<const float4*>(s_dd + c0);
+        for (int b = 0; b < 16; b += 2) {  // four columns per step: one vector load
+          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + 2 * b);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int x = 2 * (b + h);  // column within the chunk
             const float la = h ? l4.z : l4.x, lb = h ? l4.w : l4.y;
-            const float da = h ? d4.z : d4.x, db = h ? d4.w : d4.y;
             float x0, x1;
             f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), c2x2,
                                   f32x2(-la, -lb)), x0, x1);
@@ -921,22 +924,49 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!((wq >> x) & 1u)) p0 = 0.f;
               if (!((wq >> (x + 1)) & 1u)) p1 = 0.f;
             }
+            pf[x] = p0;
+            pf[x + 1] = p1;
+            pp[b + h] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st16(cs, pp);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();  // every lane's P^T is stored before lane 0 arrives for the warp
+      if (lane == 0) mbar_arrive(BAR(C::kBarP));
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 1), sph, p.budget, p.err, kErrTimeout)))
+        break;
+      sph ^= 1u;
+      tc_fence_after();
+      // dP^T -> dS = P (dP - D) scale, 16 columns at a time, dS^T over the first 16 of
+      // the chunk's dP^T columns (each half's words over columns already read)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t dv[16];
+        tmem_ld16(cs + 128 + 16 * hf, dv);
+        uint32_t pg[8];
+#pragma unroll
+        for (int b = 0; b < 8; b += 2) {
+          const float4 d4 = *reinterpret_cast<const float4*>(s_dd + 16 * hf + 2 * b);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int x = 2 * (b + h);  // column within the half
+            const int xc = 16 * hf + x;  // column within the chunk
+            const float da = h ? d4.z : d4.x, db = h ? d4.w : d4.y;
             const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1])),
                                           dsc2, f32x2(-da, -db));
             float g0, g1;
-            f32x2_split(mul_f32x2(f32x2(p0, p1), t2), g0, g1);
-            pp[b + h] = pack_bf16x2(p0, p1);
+            f32x2_split(mul_f32x2(f32x2(pf[xc], pf[xc + 1]), t2), g0, g1);
             pg[b + h] = pack_bf16x2(g0, g1);
           }
         }
-        tmem_st16(lane_base + 128 * hh + 16 * qq, pp);       // over this half's own S^T
-        tmem_st16(lane_base + 128 * hh + 64 + 16 * qq, pg);  // over this half's own dP^T
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
-        if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // queries 32q .. 32q+31 of P^T and dS^T are in TMEM
+        tmem_st8(cs + 128 + 8 * hf, pg);
       }
-      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();  // every lane's dS^T is stored before lane 0 arrives for the warp
+      if (lane == 0) mbar_arrive(BAR(C::kBarDS));
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
@@ -947,10 +977,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int cpk = (!packed_unit && key_valid && p.n_cols) ? p.colidx[j] : -1;
     {
-      const int half = wg;  // warpgroup 0 writes dV, warpgroup 1 dK
+      const int half = hh;  // warpgroups 0, 1 write dV, warpgroups 2, 3 dK
       const uint32_t col = half ? C::kColDK : C::kColDV;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+      for (int qi = 0; qi < D / 64; ++qi) {
+        const int q = qc * (D / 64) + qi;  // this warpgroup's half of the 32-column chunks
         uint32_t o[32];
         if (have) {
           tmem_ld32(lane_base + col + 32 * q, o);
@@ -997,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1061,7 +1092,7 @@ cudaError_t launch_kv_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
       return cudaErrorInvalidValue;
     }
     kp.unit0 = pr[0];
-    bwd_dkdv_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, st>>>(
+    bwd_dkdv_tc_kernel<D><<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, st>>>(
         mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc, kp);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -28,6 +28,9 @@ constexpr int kItemSplit = 2;
 constexpr int kBwdRows = 64, kBwdKeys = 64;
 constexpr int kUnitPacked = 1;
 constexpr int kEntryGathered = 1;
+// Set on band entries whose local window alone allows every (row, key) pair of the
+// group's rows and the unit's keys: the kernels skip the per-key mask words.
+constexpr int kEntryFull = 2;
 
 // Device error word bits.
 constexpr int kErrTimeout = 1;

@@ -309,8 +309,16 @@ void build_bwd_schedule(const spattn_plan* p, spattn::Schedule* s, int64_t kRows
     for (int64_t u = kb_lo * (kTile / kKeys); u <= u_hi; ++u) {
       const int64_t k0 = u * kKeys, k1 = std::min<int64_t>(k0 + kKeys, T) - 1;
       if (h.local_meets(r0, r1, k0, k1) || h.cols_in(k0, p->causal ? std::min(k1, r1) : k1) ||
-          h.rand_in(r0, r1, k0, k1))
-        add(nat[u], r0, kKindBand << kKindShift, 0, 0);
+          h.rand_in(r0, r1, k0, k1)) {
+        // every pair inside the local window: causal 0 <= i - j < window, else
+        // |i - j| <= radius (contiguous windows only)
+        bool full = d == 1;
+        if (p->causal)
+          full = full && k1 <= r0 && (p->window == 0 || r1 - k0 < p->window);
+        else
+          full = full && (p->radius < 0 || (r1 - k0 <= p->radius && k1 - r0 <= p->radius));
+        add(nat[u], r0, (kKindBand << kKindShift) | (full ? kEntryFull : 0), 0, 0);
+      }
     }
     {  // units outside the band range that random blocks of the group's rows reach
       std::vector<int64_t> ru;

@@ -156,7 +156,8 @@ def _key_major_cover(plan, T, mask, which=3, rows_per=64, keys_per=64):
     visits the allowed pairs of its non-global rows inside its unit, a random entry
     their random-block pairs that are not sparse columns, a packed entry its packed
     columns [a, b), a gathered dense entry the allowed pairs of its global rows inside
-    its unit."""
+    its unit.  A band entry marked fully allowed (flag bit 1) must have every pair of
+    its rows and keys allowed."""
     items, ents, _ = plan.schedule(which)
     cols = plan.columns()
     g = np.asarray(sorted(mask.get("global_pos", [])), dtype=np.int64)
@@ -179,6 +180,10 @@ def _key_major_cover(plan, T, mask, which=3, rows_per=64, keys_per=64):
         packed_unit = flags & 1
         for q0, ef, a, b in ents[off:off + cnt]:
             kind = (ef >> 4) & 3
+            if ef & 2:  # marked fully allowed: every pair of its rows and keys is allowed
+                assert kind == 0 and not packed_unit and not ef & 1
+                blk = M[q0:min(q0 + rows_per, T), key0:min(key0 + keys_per, T)]
+                assert blk.all(), f"entry ({q0}, unit {key0}) marked full has disallowed pairs"
             if ef & 1:
                 rows = g[q0:q0 + rows_per]
             else:
