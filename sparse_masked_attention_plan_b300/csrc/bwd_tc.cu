@@ -9,12 +9,12 @@
 // A CTA owns one 128-row query tile of one (batch, head) and walks the key tiles the
 // forward schedule gives that tile (band tiles, packed sparse columns, dense walks of
 // global rows), with the forward's per-row predicate inside partial tiles.
-// Warp roles (320 threads):
-//   warps 0-7  elementwise: P and dS of one query row per thread (its TMEM lane), warps
-//              0-3 for key columns 0-63, warps 4-7 for columns 64-127 (two warps per
+// Warp roles (576 threads):
+//   warps 0-15 elementwise: P and dS of one query row per thread (its TMEM lane), in
+//              four warpgroups that own key columns 32c .. 32c+31 (four warps per
 //              sub-partition hide each other's latency)
-//   warp 8     TMA producer: Q and dO tiles once, then K and V tiles into a ring
-//   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
+//   warp 16    TMA producer: Q and dO tiles once, then K and V tiles into a ring
+//   warp 17    MMA issuer: S = Q K^T and dP = dO V^T (both operands K-major from shared
 //              memory), then dQ += dS K with dS (bf16) from TMEM and the same K tile
 //              read as an MN-major operand
 // TMEM: S of the key tile at 0 and dP at 128 (whole 128-key products), dQ at 256, and
@@ -38,10 +38,6 @@
 namespace spattn {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-
 template <int D>
 struct DqCfg {
   static constexpr int kChunkBytes = kTile * 64 * 2;  // 128 rows x 64 bf16, one swizzle span
@@ -50,14 +46,17 @@ struct DqCfg {
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;  // Q and dO
   static constexpr int kSmemKV = kStages * kTileBytes;
+  // four elementwise warpgroups (warpgroup c owns keys 32c .. 32c+31 of every key tile),
+  // then the TMA warp and the MMA warp (18 warps: up to 5 on one SM sub-partition, whose
+  // 16K registers leave 96 per thread)
+  static constexpr int kLoadWarp = 16, kMmaWarp = 17, kThreads = 32 * (kMmaWarp + 1);
   // kBarS + 0 / + 1: S / dP of the key tile are in TMEM
-  // kBarP + q: chunk q (keys 32q .. 32q+31) of dS is in TMEM; one barrier per chunk
-  // so each completes once per key tile and a waiter can never miss a phase
+  // kBarP: every elementwise warp has written its rows of dS (one arrival per warp)
   // kBarSfree: every elementwise warp has read its columns of S
   static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarQ = 2 * kStages,
                        kBarS = 2 * kStages + 1, kBarP = 2 * kStages + 3,
-                       kBarDone = 2 * kStages + 7, kBarSfree = 2 * kStages + 8,
-                       kNumBars = 2 * kStages + 9;
+                       kBarDone = 2 * kStages + 4, kBarSfree = 2 * kStages + 5,
+                       kNumBars = 2 * kStages + 6;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescFull = idesc_bf16_f32(128, 128, 0, 0);
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);
@@ -119,7 +118,7 @@ __device__ __forceinline__ void issue_acc_chunk(uint32_t d_tmem, uint32_t a_chun
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQg, const __grid_constant__ CUtensorMap tmdOg,
@@ -166,14 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::kBarQ), 1);
     mbar_init(BAR(C::kBarS + 0), 1);
     mbar_init(BAR(C::kBarS + 1), 1);
-    // chunk hand-off: one arrival per warp of the warpgroup (128 arrivals on one
-    // barrier word would serialise on the critical path)
-    for (int q = 0; q < 4; ++q) mbar_init(BAR(C::kBarP + q), 4);
+    // dS hand-off and S read: one arrival per elementwise warp (one per thread would
+    // serialise on the barrier word, on the critical path)
+    mbar_init(BAR(C::kBarP), 16);
     mbar_init(BAR(C::kBarDone), 1);
-    mbar_init(BAR(C::kBarSfree), 8);  // one arrival per elementwise warp
+    mbar_init(BAR(C::kBarSfree), 16);
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -182,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kLoadWarp) {
+  if (warp == C::kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     const void* mapQ = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
     const void* mapdO = gathered ? static_cast<const void*>(&tmdOg) : static_cast<const void*>(&tmdO);
@@ -232,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kErrTimeout);
     mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
     const uint64_t do_desc = smem_desc_sw128(sdO, 16, 1024);
@@ -298,19 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(it + 2);
         }
         const uint32_t dsb = C::kColDS + 64 * (done & 1);
-        for (int q = 0; q < 4; ++q) {  // dQ += dS K, 32 keys at a time as the chunks arrive
-          if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + q), par, p.budget, p.err,
-                                                 kErrTimeout))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (elect_one())
+        // dQ += dS K once every warpgroup has written its 32 keys of dS
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(BAR(C::kBarP), par, p.budget, p.err, kErrTimeout))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
             issue_acc_chunk<D>(tmem + C::kColDQ, tmem + dsb + 16 * q, kv_mndesc + ks * kSlot16, q,
                                done > 0);
-          __syncwarp();
         }
-        if (!ok) break;
+        __syncwarp();
         if (elect_one()) mma_commit(BAR(C::kBarEmpty + ks));
         __syncwarp();
         if (n1 < n_ent) issue_dp(it + 2);  // every chunk has read this tile's dP
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise warps
-    const int wg = warp >> 2;  // column half
+    const int wg = warp >> 2;  // keys 32 wg .. 32 wg + 31 of every key tile
     const int r = ((warp & 3) << 5) | lane;
     const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
     int i;
@@ -360,61 +360,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n + 2 < n_ent) e_next2 = ents[n + 2];
       if (n + 1 < n_ent) cm_next = colmask_words(p.colmask, e_next);
       if (!(e.y & active_bit)) continue;
-      // the row's mask words, computed before the wait so that they overlap the products
-      uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (!(e.y & full_bit)) row_mask(make_predicate(m, cm, e, i), w);
-      // P of this warpgroup's 64 keys from S (while dP is still being computed), then
-      // dS = scale P (dP - D) chunk by chunk as dP arrives
+      // the row's mask word for this warpgroup's 32 keys, computed before the wait so
+      // that it overlaps the products
+      uint32_t wq = 0xffffffffu;
+      if (!(e.y & full_bit)) wq = row_word(make_predicate(m, cm, e, i), wg);
+      // P of this warpgroup's 32 keys from S (while dP is still being computed), then
+      // dS = scale P (dP - D) as dP arrives
       if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 0), sph, p.budget, p.err, kErrTimeout)))
         break;
       tc_fence_after();
-      if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
-      float pr[2][32];
+      if (!valid) wq = 0u;
+      float pr[32];
       {
-        uint32_t sa[32], sb[32];  // this warpgroup's 64 columns of S, one wait
-        tmem_ld32x2(lane_base + 64 * wg, sa, lane_base + 64 * wg + 32, sb);
+        uint32_t sv[32];
+        tmem_ld32(lane_base + 32 * wg, sv);
         tc_fence_before();
         __syncwarp();  // every lane has read S before lane 0 arrives for the warp
         if (lane == 0) mbar_arrive(BAR(C::kBarSfree));
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const uint32_t* sv = qq ? sb : sa;
-          const uint32_t wq = wg ? w[2 + qq] : w[qq];  // constant indices: w stays in registers
-#pragma unroll
-          for (int b = 0; b < 16; ++b) {
-            const int c0 = 2 * b;
-            float x0, x1;
-            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])),
-                                  c2x2, nl2x2), x0, x1);
-            pr[qq][c0] = ((wq >> c0) & 1u) ? fast_exp2(x0) : 0.f;
-            pr[qq][c0 + 1] = ((wq >> (c0 + 1)) & 1u) ? fast_exp2(x1) : 0.f;
-          }
+        for (int b = 0; b < 16; ++b) {
+          const int c0 = 2 * b;
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])), c2x2,
+                                nl2x2), x0, x1);
+          pr[c0] = ((wq >> c0) & 1u) ? fast_exp2(x0) : 0.f;
+          pr[c0 + 1] = ((wq >> (c0 + 1)) & 1u) ? fast_exp2(x1) : 0.f;
         }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarS + 1), sph, p.budget, p.err, kErrTimeout)))
         break;
       sph ^= 1u;
       tc_fence_after();
+      // dS of the 32 keys, 16 at a time, into this tile's dS buffer (keys 32 wg .. at
+      // column 16 wg as bf16 pairs)
+      const uint32_t dsc_col = lane_base + C::kColDS + 64 * (n_done & 1) + 16 * wg;
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int q = 2 * wg + qq;
-        uint32_t dv[32], pk[16];
-        tmem_ld32(lane_base + 128 + 32 * q, dv);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t dv[16], pk[8];
+        tmem_ld16(lane_base + 128 + 32 * wg + 16 * hf, dv);
 #pragma unroll
-        for (int b = 0; b < 16; ++b) {
+        for (int b = 0; b < 8; ++b) {
           const int c0 = 2 * b;
           const uint64_t t2 = fma_f32x2(f32x2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
                                         dsc2, dterm2);
           float g0, g1;
-          f32x2_split(mul_f32x2(f32x2(pr[qq][c0], pr[qq][c0 + 1]), t2), g0, g1);
+          f32x2_split(mul_f32x2(f32x2(pr[16 * hf + c0], pr[16 * hf + c0 + 1]), t2), g0, g1);
           pk[b] = pack_bf16x2(g0, g1);
         }
-        tmem_st16(lane_base + C::kColDS + 64 * (n_done & 1) + 16 * q, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();  // every lane's chunk is stored before lane 0 arrives for the warp
-        if (lane == 0) mbar_arrive(BAR(C::kBarP + q));  // keys 32q .. 32q+31 of dS are in TMEM
+        tmem_st8(dsc_col + 8 * hf, pk);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();  // every lane's dS is stored before lane 0 arrives for the warp
+      if (lane == 0) mbar_arrive(BAR(C::kBarP));
       ++n_done;
     }
     // ---------------------------------------------------------- epilogue
@@ -424,33 +422,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       have = __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarDone), 0, p.budget, p.err, kErrTimeout));
       if (have) tc_fence_after();
     }
-    uint4* dst = reinterpret_cast<uint4*>(p.dQ + row * D);
-#pragma unroll
-    for (int qh = 0; qh < D / 64; ++qh) {  // this warpgroup's half of the d columns
-      const int q = wg * (D / 64) + qh;
-      uint32_t o[32];
-      if (have) {
-        tmem_ld32(lane_base + C::kColDQ + 32 * q, o);
+    // this warpgroup's quarter of the d columns (32 at d = 128, 16 at d = 64)
+    constexpr int kQc = D / 4;
+    uint4* dst = reinterpret_cast<uint4*>(p.dQ + row * D + kQc * wg);
+    uint32_t o[32];
+    if (have) {
+      if constexpr (kQc == 32) {
+        tmem_ld32(lane_base + C::kColDQ + 32 * wg, o);
       } else {
+        uint32_t h[16];
+        tmem_ld16(lane_base + C::kColDQ + 16 * wg, h);
 #pragma unroll
-        for (int b = 0; b < 32; ++b) o[b] = 0u;
+        for (int b = 0; b < 16; ++b) o[b] = h[b];
       }
-      if (write) {
+    } else {
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          uint4 x;
-          x.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]), __uint_as_float(o[8 * v4 + 1]));
-          x.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]), __uint_as_float(o[8 * v4 + 3]));
-          x.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]), __uint_as_float(o[8 * v4 + 5]));
-          x.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]), __uint_as_float(o[8 * v4 + 7]));
-          dst[4 * q + v4] = x;
-        }
+      for (int b = 0; b < kQc; ++b) o[b] = 0u;
+    }
+    if (write) {
+#pragma unroll
+      for (int v4 = 0; v4 < kQc / 8; ++v4) {
+        uint4 x;
+        x.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]), __uint_as_float(o[8 * v4 + 1]));
+        x.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]), __uint_as_float(o[8 * v4 + 3]));
+        x.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]), __uint_as_float(o[8 * v4 + 5]));
+        x.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]), __uint_as_float(o[8 * v4 + 7]));
+        dst[v4] = x;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -460,26 +463,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- dK, dV (key-major)
 //
 //     dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i   (i with j in S_i)
-// Warp roles as in the dQ kernel (warps 0-7 elementwise over the two query-column
-// halves, 8 producer, 9 MMA).
+// Warp roles as in the dQ kernel (warps 0-15 elementwise in four warpgroups, each
+// owning 32 query columns; 16 producer; 17 MMA).
 // A CTA owns one 128-key unit (natural keys, or packed sparse columns) of one (batch,
 // head): its K and V tiles stay in shared memory while the 128-row query tiles that
 // read it stream through a ring (Q and dO per stage).  Per query tile:
 //   S^T = K Q^T and dP^T = V dO^T (tensor cores, TMEM lanes = keys, columns = queries);
 //   elementwise (thread = key): P^T = 2^(S^T scale log2 e - LSE log2 e) under the
-//   key's mask, dS^T = scale P^T (dP^T - D), both to TMEM as bf16 over their own
-//   first 64 columns;
+//   key's mask, dS^T = scale P^T (dP^T - D), both to TMEM as bf16 pairs over the
+//   first 16 of each warpgroup's own 32 columns;
 //   dV += P^T dO and dK += dS^T Q (A from TMEM; dO and Q read as MN-major operands).
-// The per-query LSE and D of the tile go through shared memory; a query that is not a
-// row of this tile (past the end, or a global row summed by its own dense walk) gets
-// LSE = +inf, which makes its weight 0 without a mask.  The key-side mask is a few
-// spans per thread: the key's local window seen from the key (the rows whose window
-// holds it), all later rows for a strided or global column, the query blocks that
-// list the key's block as random (transposed lists), a range of packed columns, or
-// the suffix of gathered global rows at or after the key.
-// TMEM: per query half h (64 queries), S^T at 128h and dP^T at 128h + 64; dV at 256,
-// dK at 256 + d.  The two halves ping-pong: the next tile's half-0 products start as soon
-// as this tile's half 0 has been handed back, while warpgroup 1 works on half 1.
+// Each warp loads the LSE and D of its 32 queries itself, one tile ahead; a query that
+// is not a row of this tile (past the end, or a global row summed by its own dense walk)
+// gets LSE = +inf, which makes its weight 0 without a mask.  The key-side mask (the
+// warpgroup's one 32-row word) is a few spans per thread: the key's local window seen
+// from the key (the rows whose window holds it), all later rows for a strided or global
+// column, the query blocks that list the key's block as random (transposed lists), a
+// range of packed columns, or the suffix of gathered global rows at or after the key;
+// entries whose rows and keys all lie inside the local window skip it (host flag).
+// TMEM: S^T of the whole query tile at 0, dP^T at 128, dV at 256, dK at 256 + d.
 
 template <int D>
 struct KvCfg {
@@ -1144,7 +1146,7 @@ cudaError_t launch_dq_d(const BwdTcArgs& a, cudaStream_t st, const char** why) {
     *why = "too many work items";
     return cudaErrorInvalidValue;
   }
-  bwd_dq_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, st>>>(
+  bwd_dq_tc_kernel<D><<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, st>>>(
       mQ, mdO, mK, mV, mQg, mdOg, mKc, mVc, kp);
   return cudaGetLastError();
 }

@@ -158,6 +158,16 @@ __device__ __forceinline__ void row_mask(const RowPredicate& p, uint32_t (&w)[4]
   }
 }
 
+// Word k (columns 32k .. 32k+31) of row_mask, selected by value so that nothing is
+// indexed at run time; a contiguous window builds only that word.
+__device__ __forceinline__ uint32_t row_word(const RowPredicate& p, int k) {
+  const uint32_t bits = k == 0 ? p.bits[0] : (k == 1 ? p.bits[1] : (k == 2 ? p.bits[2] : p.bits[3]));
+  if (p.dil == 1) return span_bits(p.lo, p.hi, 32 * k) | (bits & span_bits(0, p.hb, 32 * k));
+  uint32_t w[4];
+  row_mask(p, w);
+  return k == 0 ? w[0] : (k == 1 ? w[1] : (k == 2 ? w[2] : w[3]));
+}
+
 __device__ __forceinline__ bool pred_allowed(const RowPredicate& p, int c) {
   const bool in_band = c >= p.lo && c <= p.hi && (p.dil == 1 || c % p.dil == p.res);
   const bool in_cols = ((p.bits[c >> 5] >> (c & 31)) & 1u) && c <= p.hb;
