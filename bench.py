@@ -62,7 +62,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 TRAFFIC = {"kernel_sha": "cb7a388cd4c1521a", "bytes_per_launch": 999.8e6, "workload": "t32k_w4096"}
 # The same for the backward's dominant kernel (bwd_dkdv_tc, H=4 capture x 8) and the
 # decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
-BWD_TRAFFIC = {"kernel_sha": "ec92b5e24ecb8600", "bytes_per_launch": 1353.4e6,
+BWD_TRAFFIC = {"kernel_sha": "a4acc78bd1403ef0", "bytes_per_launch": 1358.0e6,
                "workload": "t32k_w4096", "file": "bwd_tc.cu"}
 DEC_TRAFFIC = {"kernel_sha": "f291ef942120fdbd", "file": "decode.cu",
                "bytes_per_launch": {"decode_b8_w4096": 140.1e6, "decode_b32_w4096": 560.2e6}}

@@ -44,6 +44,8 @@ struct DqCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = D == 128 ? 4 : 8;
+  // a tile's K and V take consecutive slots and complete the (even) K slot's barrier
+  static_assert(kStages % 2 == 0, "K slots are the even slots");
   static constexpr int kSmemQ = 2 * kTileBytes;  // Q and dO
   static constexpr int kSmemKV = kStages * kTileBytes;
   // four elementwise warpgroups (warpgroup c owns keys 32c .. 32c+31 of every key tile),
@@ -195,40 +197,57 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       }
     }
     __syncwarp();
-    int issued = 0;
-    bool ok = true;
+    // Tile t's K takes slot 2t and its V slot 2t + 1 (mod the ring); both complete the
+    // K slot's barrier, so the MMA warp waits once per tile.  V is issued first: its
+    // slot frees after dP, K's only after the dQ products, so at that point only K's
+    // copy is still to come.
+    int tiles = 0;     // tiles whose K and V were both issued
+    bool v_only = false;  // the loop left between a tile's V and its K
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
-    for (int n = 0; n < n_ent && ok; ++n) {
+    for (int n = 0; n < n_ent; ++n) {
       const int4 e = e_next;
       if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: latency off the issue path
       if (!(e.y & active_bit)) continue;
       const bool packed = ((e.y >> kKindShift) & 3) == kKindPacked;
+      const int itk = 2 * tiles, itv = itk + 1;
+      const int sk = itk % C::kStages, sv = itv % C::kStages;
+      const void* mapk = packed ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK);
+      const void* mapv = packed ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV);
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarEmpty + sv), ((itv / C::kStages) & 1) ^ 1u,
+                                             p.budget, p.err, kErrTimeout)))
+        break;
+      if (elect_one()) {
+        mbar_expect_tx(BAR(C::kBarFull + sk), C::kTileBytes);
 #pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const int it = issued;
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout))) {
-          ok = false;
-          break;
-        }
-        const void* map = kv ? (packed ? static_cast<const void*>(&tmVc) : static_cast<const void*>(&tmV))
-                             : (packed ? static_cast<const void*>(&tmKc) : static_cast<const void*>(&tmK));
-        if (elect_one()) {
-          mbar_arrive_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, map, BAR(C::kBarFull + s),
-                        c * 64, packed ? 0 : res, e.x, bh);
-        }
-        __syncwarp();
-        ++issued;
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sKV + sv * C::kTileBytes + c * C::kChunkBytes, mapv, BAR(C::kBarFull + sk),
+                      c * 64, packed ? 0 : res, e.x, bh);
       }
+      __syncwarp();
+      v_only = true;
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarEmpty + sk), ((itk / C::kStages) & 1) ^ 1u,
+                                             p.budget, p.err, kErrTimeout)))
+        break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(BAR(C::kBarFull + sk), C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sKV + sk * C::kTileBytes + c * C::kChunkBytes, mapk, BAR(C::kBarFull + sk),
+                      c * 64, packed ? 0 : res, e.x, bh);
+      }
+      __syncwarp();
+      v_only = false;
+      ++tiles;
     }
-    for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
-      mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
-                kErrTimeout);
+    // no copy is left in flight when the CTA exits: a V whose K was never issued (the
+    // loop left on a timed-out wait) gets the missing arrival, so that its barrier
+    // completes when V lands
+    const int pending = tiles + (v_only ? 1 : 0);
+    if (v_only && elect_one()) mbar_arrive(BAR(C::kBarFull + (2 * tiles) % C::kStages));
+    __syncwarp();
+    for (int t2 = pending - 1; t2 >= 0 && t2 >= pending - C::kStages / 2; --t2)
+      mbar_wait(BAR(C::kBarFull + (2 * t2) % C::kStages), ((2 * t2) / C::kStages) & 1, p.budget,
+                p.err, kErrTimeout);
     mbar_wait(BAR(C::kBarQ), 0, p.budget, p.err, kErrTimeout);
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
@@ -247,12 +266,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         while (x < n_ent && !(ents[x].y & active_bit)) ++x;
         return x;
       };
-      auto wait_kv = [&](int it) -> bool {
+      auto wait_kv = [&](int it) -> bool {  // K (slot it) and V (slot it + 1) of a tile
         return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + it % C::kStages),
                                                  (it / C::kStages) & 1, p.budget, p.err,
-                                                 kErrTimeout)) &&
-               __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + (it + 1) % C::kStages),
-                                                 ((it + 1) / C::kStages) & 1, p.budget, p.err,
                                                  kErrTimeout));
       };
       // S and dP of the tile whose K and V copies are at `it`
@@ -499,10 +515,12 @@ struct KvCfg {
   static constexpr int kSmemVec = 16 * 2 * 32 * 4;
   // kBarS + 0 / + 1: S^T / dP^T of the query tile are in TMEM; kBarP / kBarDS: every
   // elementwise warp has written its rows of P^T / dS^T (one arrival per warp)
-  static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages,
-                       kBarS = 1 + 2 * kStages, kBarP = 3 + 2 * kStages,
-                       kBarDS = 4 + 2 * kStages, kBarDone = 5 + 2 * kStages,
-                       kNumBars = 6 + 2 * kStages;
+  // a stage's Q and dO complete one barrier (kBarFull); each has its own slot-free
+  // barrier: dO's slot is free once dV has read it, Q's only once dK has
+  static constexpr int kBarKV = 0, kBarFull = 1, kBarEmptyQ = 1 + kStages,
+                       kBarEmptyDO = 1 + 2 * kStages, kBarS = 1 + 3 * kStages,
+                       kBarP = 3 + 3 * kStages, kBarDS = 4 + 3 * kStages,
+                       kBarDone = 5 + 3 * kStages, kNumBars = 6 + 3 * kStages;
   static constexpr int kSmemBytes = kSmemKV + kSmemRing + kSmemVec + kNumBars * 8 + 16 + 1024;
   // products use the dQ kernel's issue helpers (128 x 128 tiles and 128 x d chunks).
   // TMEM: S^T of the whole query tile at 0 (query q in column q), dP^T at 128; chunk c
@@ -673,7 +691,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     mbar_init(BAR(C::kBarKV), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(BAR(C::kBarFull + s), 1);
-      mbar_init(BAR(C::kBarEmpty + s), 1);
+      mbar_init(BAR(C::kBarEmptyQ + s), 1);
+      mbar_init(BAR(C::kBarEmptyDO + s), 1);
     }
     mbar_init(BAR(C::kBarS + 0), 1);
     mbar_init(BAR(C::kBarS + 1), 1);
@@ -707,7 +726,13 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       }
     }
     __syncwarp();
+    // per query tile: dO first, then Q; both complete the stage's one barrier, dO raising
+    // its expected bytes, Q arriving.  With two stages (d = 128) dO is issued as soon as
+    // its slot is free (after dV), so that when Q's frees (after dK) only Q is still to
+    // come; with more, the stage is taken whole once Q's slot is free
+    constexpr bool kSplitFree = C::kStages == 2;
     int issued = 0;
+    bool do_only = false;  // the loop left between a tile's dO and its Q
     int4 e_next = n_ent ? ents[0] : make_int4(0, 0, 0, 0);
     for (int n = 0; n < n_ent; ++n) {
       const int4 e = e_next;
@@ -715,26 +740,42 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       const bool gathered = (e.y & kEntryGathered) != 0;
       const int s = n % C::kStages;
       const uint32_t ph = (n / C::kStages) & 1;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(BAR(C::kBarEmpty + s), ph ^ 1u, p.budget, p.err, kErrTimeout)))
-        break;
+      const int r4 = gathered ? 0 : res;
       const void* mq = gathered ? static_cast<const void*>(&tmQg) : static_cast<const void*>(&tmQ);
       const void* md = gathered ? static_cast<const void*>(&tmdOg) : static_cast<const void*>(&tmdO);
+      const uint32_t dst = sRing + s * 2 * C::kTileBytes;
+      if (!__all_sync(0xffffffffu, mbar_wait(BAR((kSplitFree ? C::kBarEmptyDO : C::kBarEmptyQ) + s),
+                                             ph ^ 1u, p.budget, p.err, kErrTimeout)))
+        break;
       if (elect_one()) {
-        const uint32_t dst = sRing + s * 2 * C::kTileBytes;
-        mbar_arrive_expect_tx(BAR(C::kBarFull + s), 2 * C::kTileBytes);
+        mbar_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          const int r4 = gathered ? 0 : res;
-          tma_load_4d(dst + c * C::kChunkBytes, mq, BAR(C::kBarFull + s), c * 64, r4, e.x, bh);
+        for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(dst + C::kTileBytes + c * C::kChunkBytes, md, BAR(C::kBarFull + s), c * 64, r4,
                       e.x, bh);
-        }
       }
       __syncwarp();
+      do_only = true;
+      if (kSplitFree && !__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarEmptyQ + s), ph ^ 1u,
+                                                           p.budget, p.err, kErrTimeout)))
+        break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(BAR(C::kBarFull + s), C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(dst + c * C::kChunkBytes, mq, BAR(C::kBarFull + s), c * 64, r4, e.x, bh);
+      }
+      __syncwarp();
+      do_only = false;
       ++issued;
     }
-    for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+    // no copy is left in flight when the CTA exits: a dO whose Q was never issued (the
+    // loop left on a timed-out wait) gets the missing arrival, so that its barrier
+    // completes when dO lands
+    const int pending = issued + (do_only ? 1 : 0);
+    if (do_only && elect_one()) mbar_arrive(BAR(C::kBarFull + issued % C::kStages));
+    __syncwarp();
+    for (int it = pending - 1; it >= 0 && it >= pending - C::kStages; --it)
       mbar_wait(BAR(C::kBarFull + it % C::kStages), (it / C::kStages) & 1, p.budget, p.err,
                 kErrTimeout);
     mbar_wait(BAR(C::kBarKV), 0, p.budget, p.err, kErrTimeout);
@@ -789,7 +830,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         const uint32_t par = n & 1;
         // With more than two stages the next tile's Q and dO are long since loaded, as a
         // rule, and are checked while the warps still compute P, so that S^T(n+1) follows
-        // dV(n) at once; with two (d = 128) the stage is refilled only after dK(n-1), and
+        // dV(n) at once; with two (d = 128) Q's slot is refilled only after dK(n-1), and
         // the wait is left as late as possible
         constexpr bool kEarlyQ = C::kStages > 2;
         if (kEarlyQ && n + 1 < n_ent && !wait_q(n + 1)) break;
@@ -803,6 +844,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           for (int c = 0; c < 4; ++c)
             issue_acc_chunk<D>(tmem + C::kColDV, tmem + 32 * c, ring_mn + s * kStage16 + kDo16, c,
                                n > 0);
+          if (C::kStages == 2) mma_commit(BAR(C::kBarEmptyDO + s));  // dV has read dO
         }
         __syncwarp();
         if (n + 1 < n_ent) {
@@ -810,7 +852,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           tc_fence_after();
           issue_s(n + 1);
         }
-        // dK += dS^T Q, then the stage (Q and dO of tile n) is free
+        // dK += dS^T Q, then Q's slot is free
         if (!__all_sync(0xffffffffu,
                         mbar_wait(BAR(C::kBarDS), par, p.budget, p.err, kErrTimeout)))
           break;
@@ -820,7 +862,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           for (int c = 0; c < 4; ++c)
             issue_acc_chunk<D>(tmem + C::kColDK, tmem + 128 + 32 * c, ring_mn + s * kStage16, c,
                                n > 0);
-          mma_commit(BAR(C::kBarEmpty + s));
+          mma_commit(BAR(C::kBarEmptyQ + s));  // dK has read Q
         }
         __syncwarp();
         if (n + 1 < n_ent) issue_dp(n + 1);
