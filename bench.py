@@ -59,7 +59,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # 32K / W=4096 workload, from the ncu capture summarised in
 # the forward kernel's profile summary (captured with H=8, 250.7 MB, scaled by 32/8 heads),
 # valid only for the kernel source with this hash; any other source reports null.
-TRAFFIC = {"kernel_sha": "cb7a388cd4c1521a", "bytes_per_launch": 999.8e6, "workload": "t32k_w4096"}
+TRAFFIC = {"kernel_sha": "c098de61ca126cd1", "bytes_per_launch": 999.9e6, "workload": "t32k_w4096"}
 # The same for the backward's dominant kernel (bwd_dkdv_tc, H=4 capture x 8) and the
 # decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
 BWD_TRAFFIC = {"kernel_sha": "a4acc78bd1403ef0", "bytes_per_launch": 1358.0e6,

@@ -290,13 +290,17 @@ __global__ void __launch_bounds__(TcCfg<D, MW>::kThreads, 1)
         }
         __syncwarp();
       };
+      // Each entry's K is checked one entry early, while this tile's softmax runs (it was
+      // loaded long before, as a rule): a wait costs the warp a few hundred cycles even
+      // when its phase is complete, and between PV(n) and S(n+1) it would lengthen
+      // the tile's chain.
       int4 e_next = ents[0];
+      if (n_ent > 0 && !wait_full(0)) ok = false;
       for (int n = 0; n < n_ent && ok; ++n) {
         const int4 e = e_next;
         if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: global latency off the issue path
         const bool a = (e.y & (kActive0 << t)) != 0;
         const int kit = 2 * n, vit = 2 * n + 1;
-        if (!wait_full(kit)) { ok = false; break; }
         tc_fence_after();
         if (a) {
           if (elect_one()) {
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(TcCfg<D, MW>::kThreads, 1)
         }
         release(kit, a);
         if (!wait_full(vit)) { ok = false; break; }
+        if (n + 1 < n_ent && !wait_full(kit + 2)) { ok = false; break; }
         tc_fence_after();
         if (a) {
           if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + t), pph, p.budget, p.err,
@@ -327,15 +332,26 @@ __global__ void __launch_bounds__(TcCfg<D, MW>::kThreads, 1)
       uint32_t pend_vs = 0;
       uint32_t pph[2] = {0u, 0u};
       bool oinit[2] = {false, false};
+      // At d = 64 each entry's K is checked one entry early, while tile 0's softmax
+      // runs (with eight slots it was loaded long before): a wait costs the warp a few
+      // hundred cycles even when its phase is complete, and between PV0(n) and S0(n+1)
+      // it lengthens both tiles' chains (16K tokens 1 % faster).  At d = 128 the check
+      // stays at the top of the entry (the early one was not faster there).
+      constexpr bool kEarlyK = D == 64;
+      auto wait_k = [&](int it) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + it % C::kStages),
+                                                 (it / C::kStages) & 1, p.budget, p.err,
+                                                 kErrTimeout));
+      };
       int4 e_next = ents[0];
-      for (int n = 0; n < n_ent; ++n) {
+      if (kEarlyK && n_ent > 0 && !wait_k(0)) ok = false;
+      for (int n = 0; ok && n < n_ent; ++n) {
         const int4 e = e_next;
         if (n + 1 < n_ent) e_next = ents[n + 1];  // load ahead: global latency off the issue path
         const bool a0 = (e.y & kActive0) != 0, a1 = (e.y & kActive1) != 0;
         const int kit = 2 * n, vit = 2 * n + 1;
         const uint32_t ks = kit % C::kStages, vs = vit % C::kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + ks), (kit / C::kStages) & 1,
-                                               p.budget, p.err, kErrTimeout))) { ok = false; break; }
+        if (!kEarlyK && !wait_k(kit)) { ok = false; break; }
         tc_fence_after();
         const uint64_t k_desc = kv_kdesc + ks * kSlot16;
         if (a0) {
@@ -371,6 +387,7 @@ __global__ void __launch_bounds__(TcCfg<D, MW>::kThreads, 1)
         __syncwarp();
         if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarFull + vs), (vit / C::kStages) & 1,
                                                p.budget, p.err, kErrTimeout))) { ok = false; break; }
+        if (kEarlyK && n + 1 < n_ent && !wait_k(kit + 2)) { ok = false; break; }
         tc_fence_after();
         if (a0) {
           if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::kBarP + 0), pph[0], p.budget, p.err,
