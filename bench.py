@@ -64,8 +64,8 @@ TRAFFIC = {"kernel_sha": "c098de61ca126cd1", "bytes_per_launch": 999.9e6, "workl
 # decode kernel (B=8 capture, x 4 for B=32), keyed by their source hashes.
 BWD_TRAFFIC = {"kernel_sha": "a4acc78bd1403ef0", "bytes_per_launch": 1358.0e6,
                "workload": "t32k_w4096", "file": "bwd_tc.cu"}
-DEC_TRAFFIC = {"kernel_sha": "f291ef942120fdbd", "file": "decode.cu",
-               "bytes_per_launch": {"decode_b8_w4096": 140.1e6, "decode_b32_w4096": 560.2e6}}
+DEC_TRAFFIC = {"kernel_sha": "01872e9be1b20281", "file": "decode.cu",
+               "bytes_per_launch": {"decode_b8_w4096": 140.0e6, "decode_b32_w4096": 560.1e6}}
 
 
 def kernel_sha(name: str = "fwd_tc.cu") -> str:

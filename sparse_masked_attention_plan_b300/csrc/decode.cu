@@ -337,7 +337,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecParams p) {
 // which keeps the eight rows of every 8 x 8 matrix load in distinct banks.
 constexpr int kMmaWarps = 4;
 constexpr int kMmaThreads = 32 * kMmaWarps;
-constexpr int kMmaStages = 2;
+// three sub-chunks in flight (96 KB at d = 128, still two CTAs per SM): with few heads a
+// CTA's share of the bandwidth needs the third stage to cover the memory latency
+constexpr int kMmaStages = 3;
 
 template <int D>
 struct MmaCfg {
@@ -718,7 +720,7 @@ cudaError_t launch_decode_typed(const DecParams& p, cudaStream_t st) {
 }  // namespace
 
 int decode_splits(int64_t B, int64_t Hkv, int64_t cap) {
-  // At most 2 x 148 CTAs in all (the bf16 kernel keeps three per SM resident, so this
+  // At most 2 x 148 CTAs in all (the bf16 kernel keeps two per SM resident, so this
   // is a single wave): few, long CTAs amortise each CTA's start-up and final merge over
   // many sub-chunks.  Measured on the bf16 kernel (graph-replayed steps): B = 8 (64 kv
   // heads) 31.7 us at 4 splits against 34.1 at 6 and 38.0 at 2; B = 32 (256 kv heads)
